@@ -1,0 +1,350 @@
+"""Pins of the fp64 CPU oracle against things other than itself.
+
+Each pin is independent of the oracle's own code: hand-derived closed forms
+(tests/golden/closed_forms.json), a loop-only restatement without the
+max-subtraction, PyTorch's float64 ``F.cross_entropy`` and its autograd (the
+routine the Automodel PR #2996 "Proof" section checks its chunked path
+against), central finite differences, and invariants of softmax
+cross-entropy.  The last tests plant mistakes in the oracle and check that the
+pins catch them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from oracle import bruteforce
+from oracle import lm_head_ce as olc
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "closed_forms.json")
+
+
+def _rand(N, D, V, seed, bias=True, ignore=(1,)):
+    rng = np.random.default_rng(seed)
+    H = rng.standard_normal((N, D))
+    W = rng.standard_normal((V, D)) * 0.7
+    b = rng.standard_normal(V) * 0.3 if bias else None
+    y = rng.integers(0, V, N)
+    for i in ignore:
+        if i < N:
+            y[i] = -100
+    return H, W, b, y
+
+
+# ------------------------------------------------------------------ golden closed forms
+
+def test_golden_probs_1234():
+    g = json.load(open(GOLDEN))["ce_probs_1234"]
+    Z = np.log(np.array(g["logits_as_log_of"], dtype=np.float64))
+    y = np.array(g["labels"])
+    f = oracle.ce_forward(Z, y, -100, "sum")
+    assert f["n_valid"] == g["n_valid"]
+    np.testing.assert_allclose(f["lse"], g["lse"], rtol=1e-14)
+    np.testing.assert_allclose(f["loss_rows"], g["loss_rows"], rtol=1e-14, atol=1e-15)
+    assert f["loss"] == pytest.approx(g["loss_sum"], rel=1e-14)
+    fm = oracle.ce_forward(Z, y, -100, "mean")
+    assert fm["loss"] == pytest.approx(g["loss_mean"], rel=1e-14)
+    dZ = oracle.ce_backward(Z, y, -100, "sum")
+    np.testing.assert_allclose(dZ, g["dZ_sum"], atol=1e-14)
+    dZm = oracle.ce_backward(Z, y, -100, "mean", grad_loss=2.0)  # mean halves, g=2 doubles
+    np.testing.assert_allclose(dZm, g["dZ_sum"], atol=1e-14)
+
+
+def test_golden_peaked_row():
+    g = json.load(open(GOLDEN))["ce_peaked_row"]
+    Z = np.array([[g["L"], 0.0, 0.0]])
+    f = oracle.ce_forward(Z, np.array([0]), -100, "sum")
+    assert f["loss"] == pytest.approx(g["loss"], rel=1e-13)
+
+
+def test_golden_zero_weight_flce():
+    g = json.load(open(GOLDEN))["flce_zero_weight"]
+    H = np.array(g["H"])
+    V = g["V"]
+    W = np.zeros((V, H.shape[1]))
+    b = np.zeros(V)
+    y = np.array(g["labels"])
+    f = oracle.flce_forward(H, W, b, y, -100, "sum")
+    assert f["n_valid"] == g["n_valid"]
+    assert f["loss"] == pytest.approx(g["loss_sum"], rel=1e-14)
+    gr = oracle.flce_backward(H, W, b, y, -100, "sum")
+    np.testing.assert_allclose(gr["grad_b"], g["grad_b"], atol=1e-14)
+    np.testing.assert_allclose(gr["grad_W"], g["grad_W"], atol=1e-14)
+    np.testing.assert_array_equal(gr["grad_H"], 0.0)
+
+
+# --------------------------------------------------------------- closed forms at size
+
+@pytest.mark.parametrize("reduction", ["sum", "mean"])
+def test_zero_weight_closed_form(reduction):
+    N, D, V = 40, 6, 1000
+    H, _, _, y = _rand(N, D, V, 3, ignore=(0, 5, 7))
+    W = np.zeros((V, D))
+    f = oracle.flce_forward(H, W, None, y, -100, reduction)
+    nv = N - 3
+    assert f["n_valid"] == nv
+    want = nv * math.log(V) if reduction == "sum" else math.log(V)
+    assert f["loss"] == pytest.approx(want, rel=1e-13)
+    g = 0.75
+    dZ = oracle.ce_backward(np.zeros((N, V)), y, -100, reduction, grad_loss=g)
+    sc = g * (1.0 if reduction == "sum" else 1.0 / nv)
+    want_dZ = np.full((N, V), 1.0 / V) * sc
+    for i in range(N):
+        if y[i] == -100:
+            want_dZ[i] = 0
+        else:
+            want_dZ[i, y[i]] -= sc
+    np.testing.assert_allclose(dZ, want_dZ, atol=1e-15)
+
+
+def test_constant_rows_give_ln_V():
+    V = 777
+    Z = np.full((5, V), 3.25)
+    y = np.array([0, 1, 776, 400, -100])
+    f = oracle.ce_forward(Z, y, -100, "sum")
+    np.testing.assert_allclose(f["loss_rows"][:4], math.log(V), rtol=1e-13)
+    assert f["loss_rows"][4] == 0.0
+
+
+def test_large_logits_do_not_overflow():
+    Z = np.array([[1000.0, 999.0, -1000.0], [-5000.0, -5001.0, -5002.0]])
+    f = oracle.ce_forward(Z, np.array([0, 2]), -100, "sum")
+    np.testing.assert_allclose(f["loss_rows"][0], math.log1p(math.exp(-1.0) + math.exp(-2000.0)),
+                               rtol=1e-13)
+    np.testing.assert_allclose(f["loss_rows"][1], 2.0 + math.log(1 + math.exp(-1) + math.exp(-2)),
+                               rtol=1e-11)  # |Z| ~ 5000: ~5000 ulp of cancellation
+
+
+# ------------------------------------------------------------ loop-only restatement
+
+@pytest.mark.parametrize("reduction,nlt", [("sum", None), ("mean", None), ("sum", 7)])
+def test_bruteforce_flce(reduction, nlt):
+    N, D, V = 6, 5, 13
+    H, W, b, y = _rand(N, D, V, 11, ignore=(2,))
+    loss, nv, gH, gW, gb = bruteforce.flce(H.tolist(), W.tolist(), b.tolist(), y.tolist(),
+                                           -100, reduction, nlt, grad_loss=1.3)
+    f = oracle.flce_forward(H, W, b, y, -100, reduction, nlt)
+    gr = oracle.flce_backward(H, W, b, y, -100, reduction, nlt, grad_loss=1.3)
+    assert f["n_valid"] == nv
+    assert f["loss"] == pytest.approx(loss, rel=1e-13)
+    np.testing.assert_allclose(gr["grad_H"], gH, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(gr["grad_W"], gW, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(gr["grad_b"], gb, rtol=1e-12, atol=1e-14)
+
+
+# ----------------------------------------------------- PyTorch float64 library routine
+
+@pytest.mark.parametrize("reduction", ["sum", "mean"])
+def test_matches_torch_cross_entropy(reduction):
+    N, V = 64, 301
+    rng = np.random.default_rng(5)
+    Z = rng.standard_normal((N, V)) * 3
+    y = rng.integers(0, V, N)
+    y[::7] = -100
+    Zt = torch.tensor(Z, requires_grad=True)
+    ref = F.cross_entropy(Zt, torch.tensor(y), ignore_index=-100, reduction=reduction)
+    ref.backward(torch.tensor(0.5, dtype=torch.float64))
+    f = oracle.ce_forward(Z, y, -100, reduction)
+    assert f["loss"] == pytest.approx(ref.item(), rel=1e-13)
+    dZ = oracle.ce_backward(Z, y, -100, reduction, grad_loss=0.5)
+    np.testing.assert_allclose(dZ, Zt.grad.numpy(), rtol=1e-12, atol=1e-15)
+
+
+@pytest.mark.parametrize("bias", [False, True])
+def test_flce_matches_torch_autograd(bias):
+    N, D, V = 37, 24, 211
+    H, W, b, y = _rand(N, D, V, 9, bias=bias, ignore=(0, 3, 30))
+    Ht = torch.tensor(H, requires_grad=True)
+    Wt = torch.tensor(W, requires_grad=True)
+    bt = torch.tensor(b, requires_grad=True) if bias else None
+    Z = Ht @ Wt.T + (bt if bias else 0)
+    nlt = 50
+    ref = F.cross_entropy(Z, torch.tensor(y), ignore_index=-100, reduction="sum") / nlt
+    ref.backward()
+    f = oracle.flce_forward(H, W, b, y, -100, "sum", nlt)
+    gr = oracle.flce_backward(H, W, b, y, -100, "sum", nlt)
+    assert f["loss"] == pytest.approx(ref.item(), rel=1e-13)
+    np.testing.assert_allclose(gr["grad_H"], Ht.grad.numpy(), rtol=1e-11, atol=1e-15)
+    np.testing.assert_allclose(gr["grad_W"], Wt.grad.numpy(), rtol=1e-11, atol=1e-15)
+    if bias:
+        np.testing.assert_allclose(gr["grad_b"], bt.grad.numpy(), rtol=1e-11, atol=1e-15)
+
+
+# ------------------------------------------------------------- finite differences
+
+def _fd(fun, x, eps=1e-6):
+    g = np.zeros_like(x)
+    it = np.nditer(x, flags=["multi_index"])
+    for _ in it:
+        i = it.multi_index
+        old = x[i]
+        x[i] = old + eps
+        fp = fun()
+        x[i] = old - eps
+        fm = fun()
+        x[i] = old
+        g[i] = (fp - fm) / (2 * eps)
+    return g
+
+
+def test_finite_differences_flce():
+    N, D, V = 5, 4, 7
+    H, W, b, y = _rand(N, D, V, 21, ignore=(1,))
+    loss = lambda: oracle.flce_forward(H, W, b, y, -100, "mean")["loss"]  # noqa: E731
+    gr = oracle.flce_backward(H, W, b, y, -100, "mean")
+    np.testing.assert_allclose(gr["grad_H"], _fd(loss, H), rtol=1e-6, atol=1e-9)
+    np.testing.assert_allclose(gr["grad_W"], _fd(loss, W), rtol=1e-6, atol=1e-9)
+    np.testing.assert_allclose(gr["grad_b"], _fd(loss, b), rtol=1e-6, atol=1e-9)
+
+
+def test_finite_differences_ce():
+    rng = np.random.default_rng(4)
+    Z = rng.standard_normal((4, 9))
+    y = np.array([3, -100, 8, 0])
+    loss = lambda: oracle.ce_forward(Z, y, -100, "sum", num_label_tokens=3)["loss"]  # noqa: E731
+    dZ = oracle.ce_backward(Z, y, -100, "sum", num_label_tokens=3)
+    np.testing.assert_allclose(dZ, _fd(loss, Z), rtol=1e-6, atol=1e-9)
+
+
+# --------------------------------------------------------------------- invariants
+
+def test_invariants():
+    N, D, V = 30, 8, 97
+    H, W, b, y = _rand(N, D, V, 17, ignore=(2, 9))
+    f = oracle.flce_forward(H, W, b, y, -100, "sum")
+    assert np.all(f["loss_rows"] >= 0)
+    dZ = oracle.ce_backward(oracle.flce_logits(H, W, b, np.arange(N)), y, -100, "sum")
+    np.testing.assert_allclose(dZ.sum(axis=1), 0.0, atol=1e-14)
+    assert np.all(dZ[[2, 9]] == 0)
+    gr = oracle.flce_backward(H, W, b, y, -100, "sum")
+    np.testing.assert_allclose(gr["grad_b"].sum(), 0.0, atol=1e-13)
+    np.testing.assert_allclose(gr["grad_W"].sum(axis=0), 0.0, atol=1e-12)
+    assert np.all(gr["grad_H"][[2, 9]] == 0)
+
+
+def test_shift_invariance():
+    N, D, V = 12, 5, 31
+    H, W, b, y = _rand(N, D, V, 23)
+    f0 = oracle.flce_forward(H, W, b, y, -100, "sum")
+    f1 = oracle.flce_forward(H, W, b + 17.5, y, -100, "sum")
+    assert f1["loss"] == pytest.approx(f0["loss"], rel=1e-12)
+    g0 = oracle.flce_backward(H, W, b, y, -100, "sum")
+    g1 = oracle.flce_backward(H, W, b + 17.5, y, -100, "sum")
+    np.testing.assert_allclose(g1["grad_H"], g0["grad_H"], atol=1e-12)
+    Z = np.random.default_rng(1).standard_normal((N, V))
+    shift = np.arange(N)[:, None] * 3.0
+    np.testing.assert_allclose(oracle.ce_backward(Z + shift, y, -100, "sum"),
+                               oracle.ce_backward(Z, y, -100, "sum"), atol=1e-13)
+
+
+def test_grad_W_is_linear_in_row_blocks():
+    N, D, V = 40, 6, 53
+    H, W, b, y = _rand(N, D, V, 31, ignore=(4, 33))
+    full = oracle.flce_backward(H, W, b, y, -100, "mean")
+    nv = int((y != -100).sum())
+    acc = np.zeros((V, D))
+    for r0 in range(0, N, 13):
+        rows = np.arange(r0, min(N, r0 + 13))
+        part = oracle.flce_backward(H, W, b, y, -100, "mean", rows=rows, n_valid_total=nv,
+                                    grad_W_init=acc)
+        acc = part["grad_W"]
+        np.testing.assert_allclose(part["grad_H"], full["grad_H"][rows], atol=1e-14)
+    np.testing.assert_allclose(acc, full["grad_W"], atol=1e-13)
+
+
+# ------------------------------------------------------------------- zero guards
+
+@pytest.mark.parametrize("reduction", ["sum", "mean"])
+def test_all_ignored_gives_zero(reduction):
+    N, D, V = 8, 4, 11
+    H, W, b, _ = _rand(N, D, V, 2)
+    y = np.full(N, -100)
+    f = oracle.flce_forward(H, W, b, y, -100, reduction)
+    assert f["loss"] == 0.0 and f["n_valid"] == 0
+    gr = oracle.flce_backward(H, W, b, y, -100, reduction)
+    for k in ("grad_H", "grad_W", "grad_b"):
+        assert np.all(gr[k] == 0)
+
+
+def test_zero_num_label_tokens_guard():
+    N, D, V = 8, 4, 11
+    H, W, b, y = _rand(N, D, V, 2)
+    f = oracle.flce_forward(H, W, b, y, -100, "sum", num_label_tokens=0)
+    assert f["loss"] == 0.0 and f["n_valid"] == N - 1
+    gr = oracle.flce_backward(H, W, b, y, -100, "sum", num_label_tokens=0)
+    for k in ("grad_H", "grad_W", "grad_b"):
+        assert np.all(gr[k] == 0)
+
+
+def test_num_label_tokens_overrides_divisor():
+    N, D, V = 10, 3, 9
+    H, W, b, y = _rand(N, D, V, 8)
+    s = oracle.flce_forward(H, W, b, y, -100, "sum")["loss"]
+    for red in ("sum", "mean"):
+        assert oracle.flce_forward(H, W, b, y, -100, red, 4)["loss"] == pytest.approx(s / 4, rel=1e-14)
+
+
+def test_ignore_index_inside_vocab_is_ignored():
+    Z = np.random.default_rng(0).standard_normal((3, 5))
+    f = oracle.ce_forward(Z, np.array([2, 4, 0]), ignore_index=4)
+    assert f["n_valid"] == 2 and f["loss_rows"][1] == 0.0
+
+
+def test_out_of_range_label_raises():
+    with pytest.raises(ValueError):
+        oracle.ce_forward(np.zeros((2, 5)), np.array([1, 5]))
+    with pytest.raises(ValueError):
+        oracle.ce_forward(np.zeros((2, 5)), np.array([-1, 0]))
+
+
+def test_bf16_inputs_are_widened_exactly():
+    t = torch.tensor([[1.0, 2.0, 3.0]], dtype=torch.float32).to(torch.bfloat16) * 1.01
+    Z = olc._f64(t)
+    assert Z.dtype == np.float64
+    assert np.all(Z == t.float().numpy().astype(np.float64))
+
+
+# ------------------------------------------------------- planted mistakes are caught
+
+def _golden_probs_ok():
+    try:
+        test_golden_probs_1234()
+        return True
+    except AssertionError:
+        return False
+
+
+def test_planted_lse_without_max_is_caught(monkeypatch):
+    monkeypatch.setattr(olc, "logsumexp_rows",
+                        lambda Z: np.log(np.exp(Z - Z.max(axis=1)[:, None]).sum(axis=1)))
+    assert not _golden_probs_ok()
+
+
+def test_planted_onehot_sign_is_caught(monkeypatch):
+    def bad(Z, lse, y, valid, coef):
+        P = np.exp(Z - lse[:, None])
+        rows = np.nonzero(valid)[0]
+        P[rows, y[rows]] += 1.0
+        P[~valid] = 0.0
+        return P * coef
+    monkeypatch.setattr(olc, "_dlogits", bad)
+    with pytest.raises(AssertionError):
+        test_finite_differences_flce()
+
+
+def test_planted_transposed_grad_W_is_caught(monkeypatch):
+    real = olc.flce_backward
+
+    def bad(*a, **k):
+        out = real(*a, **k)
+        gW = out["grad_W"]
+        out["grad_W"] = gW[::-1].copy()  # rows of grad_W swapped end for end
+        return out
+    monkeypatch.setattr(oracle, "flce_backward", bad)
+    with pytest.raises(AssertionError):
+        test_flce_matches_torch_autograd(False)
