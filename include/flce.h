@@ -1,0 +1,180 @@
+/*
+ * flce.h - C ABI of the language-model loss head for GB300 (sm_103a).
+ *
+ * Two operations, each split into a forward and a backward call:
+ *
+ *   ce_logits_*  masked cross-entropy over GIVEN logits [N, V]; the backward can
+ *                write the gradient into the logits storage (in place).
+ *                Defined by Automodel PR #2996 "feat(loss): chunked masked CE,
+ *                packing-mask preservation, scoped MoE AC", first commit message
+ *                (forward: per-row fp32 logsumexp and label-logit gather summed
+ *                into a scalar, only the logits and labels kept; backward:
+ *                softmax recomputed per chunk, gradient optionally written into
+ *                the logits storage) and its inplace_grad follow-up commit.
+ *
+ *   flce_*       fused linear cross-entropy: logits = H W^T (+ bias) are formed
+ *                tile by tile and never stored.  Defined by Liger-Kernel issue
+ *                #533 "Gradient checkpointing for grad_weight in LFCE" (feature
+ *                pitch: the chunked logits, grad_W accumulated with an addmm of
+ *                dlogits^T H at beta = 1, and the fully recomputed variant in the
+ *                follow-up comments, whose backward recomputes the logits) and
+ *                Liger-Kernel issue #941 "[Question] No gain in VRAM usage with
+ *                LigerFusedLinearCrossEntropyLoss" (input [B*T, D], weight
+ *                [V, D] in the tied-embedding layout, optional bias).
+ *
+ * Notation: N tokens (rows), V vocabulary, D hidden size; y_i the label of row
+ * i; valid_i = (y_i != ignore_index); n_valid = sum_i valid_i;
+ * lse_i = log sum_j exp(z_ij); loss_i = valid_i * (lse_i - z_{i,y_i}).
+ *
+ * Reduction.  S = sum_i loss_i.  The loss is S * scale with
+ *   scale = 1 / num_label_tokens   if num_label_tokens >= 0 is given,
+ *         = 1                      for FLCE_SUM,
+ *         = 1 / n_valid            for FLCE_MEAN,
+ * and scale = 0 whenever that divisor is 0 (all rows ignored under MEAN, or
+ * num_label_tokens == 0): the loss and every gradient are then 0.
+ * The backward gradient is dz_ij = valid_i (exp(z_ij - lse_i) - [j == y_i]) g scale
+ * with g = *grad_loss.
+ *
+ * Memory.  Every pointer is a DEVICE pointer unless stated otherwise; the
+ * caller allocates every buffer (inputs, outputs, workspace) and keeps
+ * ownership.  The library never allocates or frees device memory, never
+ * synchronises, and enqueues all its work on the caller's `stream`.
+ * Matrices are row-major with unit stride along the last dimension.
+ *
+ * Errors.  Every entry point returns a flce_status_t.  Errors that the host can
+ * see (null pointers, bad sizes, bad alignment, too small a workspace) are
+ * returned before anything is enqueued.  Errors only the device can see (a
+ * label outside [0, V) that is not ignore_index; a bounded wait that gave up)
+ * are written to the device word *status with "first error wins" semantics:
+ * the library never clears *status, so a nonzero value stays until the caller
+ * resets it.  Rows whose label is out of range contribute nothing to the loss,
+ * n_valid or the gradients.  No kernel traps or asserts.
+ *
+ * Determinism.  No floating-point atomics are used: two identical calls give
+ * bitwise-identical results.
+ */
+#ifndef FLCE_H
+#define FLCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FLCE_API __attribute__((visibility("default")))
+#else
+#define FLCE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st* flce_stream_t;
+
+typedef enum {
+  FLCE_OK = 0,
+  FLCE_EINVAL = -1,      /* null pointer, bad enum value, bad flag           */
+  FLCE_ESHAPE = -2,      /* a size is out of range or inconsistent           */
+  FLCE_EDTYPE = -3,      /* unsupported dtype                                */
+  FLCE_EALIGN = -4,      /* a pointer or row stride breaks an alignment rule */
+  FLCE_ELABEL = -5,      /* (device) label outside [0,V) and != ignore_index */
+  FLCE_EWORKSPACE = -6,  /* workspace pointer null or too small              */
+  FLCE_ECUDA = -7,       /* a CUDA runtime/driver call failed                */
+  FLCE_ENOSUP = -8,      /* valid request this build does not support        */
+  FLCE_ETIMEOUT = -9     /* (device) a bounded wait inside a kernel gave up  */
+} flce_status_t;
+
+typedef enum { FLCE_BF16 = 0, FLCE_F32 = 1 } flce_dtype_t;
+typedef enum { FLCE_SUM = 0, FLCE_MEAN = 1 } flce_reduction_t;
+
+/* Human-readable name of a status code (static storage; never NULL). */
+FLCE_API const char* flce_status_string(int status);
+
+/* ------------------------------------------------------------------------ */
+/* Cross-entropy on given logits                                            */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of device workspace ce_logits_fwd needs for N rows (4 bytes per row,
+ * rounded up to 256).  Returns 0 for N <= 0. */
+FLCE_API size_t ce_logits_workspace_bytes(int64_t N, int64_t V);
+
+/* Forward.  logits: [N, ld] of dtype dt, row i at logits + i*ld elements, the
+ * first V columns used (ld >= V).  labels: [N] int64.  Outputs:
+ *   loss      [1] f32   the reduced loss (see "Reduction")
+ *   n_valid   [1] i64   number of rows with a valid label (exact)
+ *   lse       [N] f32   per-row log-sum-exp (saved for the backward; written
+ *                       for every row, ignored ones included)
+ *   loss_rows [N] f32   optional (may be NULL): loss_i, 0 on ignored rows
+ *   label_logit [N] f32 optional (may be NULL): z_{i,y_i} widened to fp32
+ *                       exactly, NaN on ignored rows
+ * ws/ws_bytes: workspace of at least ce_logits_workspace_bytes(N, V) bytes,
+ * 16-byte aligned.  status: device word, see "Errors".
+ * N == 0 is valid (loss 0, n_valid 0).  Requires 1 <= V < 2^31, ld >= V. */
+FLCE_API int ce_logits_fwd(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
+                  const int64_t* labels, int64_t ignore_index, int reduction,
+                  int64_t num_label_tokens, float* loss, int64_t* n_valid, float* lse,
+                  float* loss_rows, float* label_logit, void* ws, size_t ws_bytes,
+                  int32_t* status, flce_stream_t stream);
+
+/* Backward.  Reads logits, labels, lse (from ce_logits_fwd), n_valid (from
+ * ce_logits_fwd; only read for FLCE_MEAN without num_label_tokens) and
+ * grad_loss ([1] f32 device: the incoming gradient g of the loss), and writes
+ * grad_logits [N, ld_grad] of dtype dt (first V columns of each row).
+ * inplace_grad != 0: grad_logits must equal logits and ld_grad == ld; the
+ * logits are overwritten by their gradient (Automodel PR #2996, inplace_grad).
+ * inplace_grad == 0: grad_logits must not overlap the logits. */
+FLCE_API int ce_logits_bwd(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
+                  const int64_t* labels, int64_t ignore_index, int reduction,
+                  int64_t num_label_tokens, const float* lse, const int64_t* n_valid,
+                  const float* grad_loss, int inplace_grad, void* grad_logits,
+                  int64_t ld_grad, int32_t* status, flce_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Fused linear cross-entropy                                               */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of device workspace for flce_fwd and flce_bwd with these sizes.
+ * `chunk` is the number of rows the backward processes per step (<= 0 picks
+ * the library default, flce_default_chunk).  The same workspace serves both
+ * calls. */
+FLCE_API size_t flce_workspace_bytes(int dt, int64_t N, int64_t D, int64_t V, int64_t chunk);
+
+/* Row chunk the backward uses when `chunk` <= 0 is passed. */
+FLCE_API int64_t flce_default_chunk(int dt, int64_t N, int64_t D, int64_t V);
+
+/* Forward.  H: [N, D], W: [V, D] (row v is the embedding of token v), bias:
+ * [V] or NULL, all of dtype dt (FLCE_BF16: tensor cores in bf16 with fp32
+ * accumulation; FLCE_F32: tensor cores in tf32 with fp32 accumulation).
+ * H and W must be 16-byte aligned and D * sizeof(dt) a multiple of 16.
+ * Outputs as in ce_logits_fwd (loss, n_valid, lse, optional loss_rows and
+ * label_logit, the latter the fp32 GEMM value of z_{i,y_i}).
+ * Requires 1 <= N, 1 <= V < 2^31, 8 <= D. */
+FLCE_API int flce_fwd(const void* H, const void* W, const void* bias, int dt, int64_t N, int64_t D,
+             int64_t V, const int64_t* labels, int64_t ignore_index, int reduction,
+             int64_t num_label_tokens, float* loss, int64_t* n_valid, float* lse,
+             float* loss_rows, float* label_logit, void* ws, size_t ws_bytes,
+             int32_t* status, flce_stream_t stream);
+
+/* Backward (fully recomputed: the logits are formed again chunk by chunk).
+ * Reads the forward's inputs plus lse and n_valid from flce_fwd and grad_loss
+ * ([1] f32 device).  Writes, each optional (NULL skips it):
+ *   grad_H    [N, D] dtype dt      = dZ W
+ *   grad_W    [V, D] f32           = dZ^T H, added to the existing contents if
+ *                                    accumulate_grad_W != 0 (addmm beta = 1)
+ *   grad_bias [V]    f32           = sum over rows of dZ (overwritten)
+ * dZ is formed per row chunk in fp32 and rounded to dt before the two
+ * gradient contractions.  chunk <= 0 picks flce_default_chunk; the workspace
+ * must have been sized with the same chunk. */
+FLCE_API int flce_bwd(const void* H, const void* W, const void* bias, int dt, int64_t N, int64_t D,
+             int64_t V, const int64_t* labels, int64_t ignore_index, int reduction,
+             int64_t num_label_tokens, const float* lse, const int64_t* n_valid,
+             const float* grad_loss, int64_t chunk, void* grad_H, float* grad_W,
+             int accumulate_grad_W, float* grad_bias, void* ws, size_t ws_bytes,
+             int32_t* status, flce_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLCE_H */

@@ -1,0 +1,98 @@
+"""ctypes binding of libflce.so (argument marshalling only).
+
+Every function here has the name and argument order of the C entry point in
+``include/flce.h`` / ``include/flce_gemm.h``.  Nothing here computes: the work
+runs in the library's kernels.  If the library is missing the import fails
+loudly; there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libflce.so")
+
+FLCE_OK = 0
+FLCE_ELABEL = -5
+FLCE_ETIMEOUT = -9
+FLCE_BF16 = 0
+FLCE_F32 = 1
+FLCE_SUM = 0
+FLCE_MEAN = 1
+
+_i = ctypes.c_int
+_i64 = ctypes.c_int64
+_sz = ctypes.c_size_t
+_p = ctypes.c_void_p
+
+_SIGNATURES = {
+    "flce_status_string": (ctypes.c_char_p, [_i]),
+    "ce_logits_workspace_bytes": (_sz, [_i64, _i64]),
+    "ce_logits_fwd": (_i, [_p, _i, _i64, _i64, _i64, _p, _i64, _i, _i64, _p, _p, _p, _p, _p,
+                           _p, _sz, _p, _p]),
+    "ce_logits_bwd": (_i, [_p, _i, _i64, _i64, _i64, _p, _i64, _i, _i64, _p, _p, _p, _i, _p,
+                           _i64, _p, _p]),
+    "flce_workspace_bytes": (_sz, [_i, _i64, _i64, _i64, _i64]),
+    "flce_default_chunk": (_i64, [_i, _i64, _i64, _i64]),
+    "flce_fwd": (_i, [_p, _p, _p, _i, _i64, _i64, _i64, _p, _i64, _i, _i64, _p, _p, _p, _p, _p,
+                      _p, _sz, _p, _p]),
+    "flce_bwd": (_i, [_p, _p, _p, _i, _i64, _i64, _i64, _p, _i64, _i, _i64, _p, _p, _p, _i64,
+                      _p, _p, _i, _p, _p, _sz, _p, _p]),
+    "flce_gemm": (_i, [_i, _i, _i, _i64, _i64, _i64, _p, _i64, _p, _i64, _p, _i64, _i, _p, _p]),
+}
+
+EXPORTED = tuple(_SIGNATURES)
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libflce.so once; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(
+            f"libflce.so not found at {path}: build it with "
+            "`python -m lm_head_linear_fwd_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load().flce_status_string(int(code)).decode()
+
+
+class FlceError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+
+
+def check(rc: int, where: str) -> None:
+    if rc != FLCE_OK:
+        raise FlceError(rc, where)
+
+
+def _call(name):
+    def f(*args):
+        return getattr(load(), name)(*args)
+    f.__name__ = name
+    return f
+
+
+flce_status_string = _call("flce_status_string")
+ce_logits_workspace_bytes = _call("ce_logits_workspace_bytes")
+ce_logits_fwd = _call("ce_logits_fwd")
+ce_logits_bwd = _call("ce_logits_bwd")
+flce_workspace_bytes = _call("flce_workspace_bytes")
+flce_default_chunk = _call("flce_default_chunk")
+flce_fwd = _call("flce_fwd")
+flce_bwd = _call("flce_bwd")
+flce_gemm = _call("flce_gemm")

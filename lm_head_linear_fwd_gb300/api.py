@@ -1,0 +1,346 @@
+"""PyTorch-facing API of the loss head: allocation, streams and autograd.
+
+PyTorch only allocates device memory and supplies the current stream; every
+step of the computation runs in libflce.so's kernels, reached through the
+C ABI (``_abi``).  There is no CPU or eager-PyTorch fallback: a missing
+library or a non-CUDA tensor raises.
+
+Low-level calls (same names as the C entry points):
+    ce_logits_fwd, ce_logits_bwd, flce_fwd, flce_bwd, flce_gemm
+Autograd front ends:
+    ce_logits(logits, labels, *, ignore_index, reduction, num_label_tokens,
+              inplace_grad=False, mask=None)
+    flce(H, W, labels, bias=None, *, ignore_index, reduction, num_label_tokens,
+         chunk=None, mask=None)
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import torch
+from torch.autograd.function import once_differentiable
+
+from . import _abi
+
+_DT = {torch.bfloat16: _abi.FLCE_BF16, torch.float32: _abi.FLCE_F32}
+_RED = {"sum": _abi.FLCE_SUM, "mean": _abi.FLCE_MEAN}
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DT:
+        raise TypeError(f"unsupported dtype {t.dtype}: expected bfloat16 or float32")
+    return _DT[t.dtype]
+
+
+def _red_code(reduction: str) -> int:
+    if reduction not in _RED:
+        raise ValueError(f"reduction must be 'sum' or 'mean', got {reduction!r}")
+    return _RED[reduction]
+
+
+def _nlt(num_label_tokens) -> int:
+    if num_label_tokens is None:
+        return -1
+    n = int(num_label_tokens)
+    if n < 0:
+        raise ValueError("num_label_tokens must be >= 0")
+    return n
+
+
+def _cuda(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the loss head has no CPU path)")
+    return t
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def new_status(device) -> torch.Tensor:
+    """A zeroed device status word (see the Errors section of flce.h)."""
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def check_status(status: torch.Tensor, where: str = "device") -> None:
+    """Reads the device status word (synchronises) and raises if it is set."""
+    code = int(status.item())
+    if code != _abi.FLCE_OK:
+        raise _abi.FlceError(code, where)
+
+
+def _labels(labels: torch.Tensor, N: int) -> torch.Tensor:
+    _cuda(labels, "labels")
+    if labels.dtype != torch.int64 or labels.dim() != 1 or labels.shape[0] != N:
+        raise ValueError(f"labels must be int64 of shape [{N}]")
+    return labels.contiguous()
+
+
+# ---------------------------------------------------------------- CE on logits
+
+@dataclasses.dataclass
+class ForwardOut:
+    loss: torch.Tensor           # [1] f32
+    n_valid: torch.Tensor        # [1] i64
+    lse: torch.Tensor            # [N] f32
+    loss_rows: Optional[torch.Tensor]
+    label_logit: Optional[torch.Tensor]
+    status: torch.Tensor         # [1] i32
+
+
+def ce_logits_workspace_bytes(N: int, V: int) -> int:
+    return int(_abi.ce_logits_workspace_bytes(N, V))
+
+
+def ce_logits_fwd(logits, labels, ignore_index=-100, reduction="sum", num_label_tokens=None, *,
+                  want_rows=False, want_label_logit=False, ws=None, status=None,
+                  out=None) -> ForwardOut:
+    _cuda(logits, "logits")
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be 2-D with unit stride along the vocabulary")
+    N, V = logits.shape
+    labels = _labels(labels, N)
+    dev = logits.device
+    if out is None:
+        out = ForwardOut(
+            loss=torch.empty(1, dtype=torch.float32, device=dev),
+            n_valid=torch.empty(1, dtype=torch.int64, device=dev),
+            lse=torch.empty(N, dtype=torch.float32, device=dev),
+            loss_rows=torch.empty(N, dtype=torch.float32, device=dev) if want_rows else None,
+            label_logit=torch.empty(N, dtype=torch.float32, device=dev) if want_label_logit else None,
+            status=status if status is not None else new_status(dev))
+    nbytes = ce_logits_workspace_bytes(N, V)
+    if ws is None:
+        ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    rc = _abi.ce_logits_fwd(_ptr(logits), _dtype_code(logits), N, V, logits.stride(0),
+                            _ptr(labels), int(ignore_index), _red_code(reduction),
+                            _nlt(num_label_tokens), _ptr(out.loss), _ptr(out.n_valid),
+                            _ptr(out.lse), _ptr(out.loss_rows), _ptr(out.label_logit),
+                            _ptr(ws), ws.numel(), _ptr(out.status), _stream(dev))
+    _abi.check(rc, "ce_logits_fwd")
+    return out
+
+
+def ce_logits_bwd(logits, labels, lse, n_valid, grad_loss, ignore_index=-100, reduction="sum",
+                  num_label_tokens=None, inplace_grad=False, grad_logits=None,
+                  status=None) -> torch.Tensor:
+    _cuda(logits, "logits")
+    N, V = logits.shape
+    labels = _labels(labels, N)
+    dev = logits.device
+    if inplace_grad:
+        grad_logits = logits
+    elif grad_logits is None:
+        grad_logits = torch.empty((N, V), dtype=logits.dtype, device=dev)
+    if grad_logits.dtype != logits.dtype or grad_logits.stride(1) != 1:
+        raise ValueError("grad_logits must have the logits dtype and unit column stride")
+    g = grad_loss.to(device=dev, dtype=torch.float32).reshape(1).contiguous()
+    status = status if status is not None else new_status(dev)
+    rc = _abi.ce_logits_bwd(_ptr(logits), _dtype_code(logits), N, V, logits.stride(0),
+                            _ptr(labels), int(ignore_index), _red_code(reduction),
+                            _nlt(num_label_tokens), _ptr(lse), _ptr(n_valid), _ptr(g),
+                            1 if inplace_grad else 0, _ptr(grad_logits), grad_logits.stride(0),
+                            _ptr(status), _stream(dev))
+    _abi.check(rc, "ce_logits_bwd")
+    return grad_logits
+
+
+class _CELogits(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, logits, labels, ignore_index, reduction, num_label_tokens, inplace_grad):
+        out = ce_logits_fwd(logits, labels, ignore_index, reduction, num_label_tokens)
+        ctx.save_for_backward(logits, labels, out.lse, out.n_valid)
+        ctx.args = (ignore_index, reduction, num_label_tokens, inplace_grad)
+        ctx.status = out.status
+        ctx.consumed = False
+        return out.loss.reshape(())
+
+    @staticmethod
+    @once_differentiable
+    def backward(ctx, g):
+        logits, labels, lse, n_valid = ctx.saved_tensors
+        ignore_index, reduction, nlt, inplace = ctx.args
+        if inplace and ctx.consumed:
+            raise RuntimeError("ce_logits(inplace_grad=True): the logits were already overwritten "
+                               "by their gradient; a second backward is not possible")
+        ctx.consumed = True
+        grad = ce_logits_bwd(logits, labels, lse, n_valid, g, ignore_index, reduction, nlt,
+                             inplace_grad=inplace, status=ctx.status)
+        return grad, None, None, None, None, None
+
+
+def _fold_mask(labels, mask, ignore_index):
+    if mask is None:
+        return labels
+    return labels.masked_fill(mask.to(device=labels.device) == 0, ignore_index)
+
+
+def ce_logits(logits, labels, *, ignore_index=-100, reduction="sum", num_label_tokens=None,
+              inplace_grad=False, mask=None):
+    """Masked cross-entropy on given logits [N, V] (bf16 or fp32).
+
+    ``inplace_grad=True`` writes the gradient into the logits storage during
+    backward (the logits are destroyed); it is keyword-only and off by default.
+    ``mask`` (same shape as labels) marks rows to ignore with 0."""
+    labels = _fold_mask(labels, mask, ignore_index)
+    return _CELogits.apply(logits, labels, int(ignore_index), reduction, num_label_tokens,
+                           bool(inplace_grad))
+
+
+# ---------------------------------------------------------- fused linear CE
+
+def flce_workspace_bytes(dt_code: int, N: int, D: int, V: int, chunk: int = 0) -> int:
+    return int(_abi.flce_workspace_bytes(dt_code, N, D, V, chunk))
+
+
+def flce_default_chunk(dt_code: int, N: int, D: int, V: int) -> int:
+    return int(_abi.flce_default_chunk(dt_code, N, D, V))
+
+
+def _flce_inputs(H, W, bias):
+    _cuda(H, "H")
+    _cuda(W, "W")
+    if H.dim() != 2 or W.dim() != 2 or H.shape[1] != W.shape[1]:
+        raise ValueError("H must be [N, D] and W [V, D]")
+    if H.dtype != W.dtype or (bias is not None and bias.dtype != H.dtype):
+        raise TypeError("H, W and bias must share one dtype")
+    if not H.is_contiguous() or not W.is_contiguous():
+        raise ValueError("H and W must be contiguous")
+    if bias is not None:
+        _cuda(bias, "bias")
+        if bias.shape != (W.shape[0],) or not bias.is_contiguous():
+            raise ValueError("bias must be a contiguous [V] tensor")
+    return H.shape[0], H.shape[1], W.shape[0]
+
+
+def flce_fwd(H, W, labels, bias=None, ignore_index=-100, reduction="sum", num_label_tokens=None,
+             *, want_rows=False, want_label_logit=False, ws=None, status=None,
+             out=None) -> ForwardOut:
+    N, D, V = _flce_inputs(H, W, bias)
+    labels = _labels(labels, N)
+    dev = H.device
+    dt = _dtype_code(H)
+    if out is None:
+        out = ForwardOut(
+            loss=torch.empty(1, dtype=torch.float32, device=dev),
+            n_valid=torch.empty(1, dtype=torch.int64, device=dev),
+            lse=torch.empty(N, dtype=torch.float32, device=dev),
+            loss_rows=torch.empty(N, dtype=torch.float32, device=dev) if want_rows else None,
+            label_logit=torch.empty(N, dtype=torch.float32, device=dev) if want_label_logit else None,
+            status=status if status is not None else new_status(dev))
+    if ws is None:
+        ws = torch.empty(flce_workspace_bytes(dt, N, D, V), dtype=torch.uint8, device=dev)
+    rc = _abi.flce_fwd(_ptr(H), _ptr(W), _ptr(bias), dt, N, D, V, _ptr(labels), int(ignore_index),
+                       _red_code(reduction), _nlt(num_label_tokens), _ptr(out.loss),
+                       _ptr(out.n_valid), _ptr(out.lse), _ptr(out.loss_rows),
+                       _ptr(out.label_logit), _ptr(ws), ws.numel(), _ptr(out.status),
+                       _stream(dev))
+    _abi.check(rc, "flce_fwd")
+    return out
+
+
+@dataclasses.dataclass
+class BackwardOut:
+    grad_H: Optional[torch.Tensor]
+    grad_W: Optional[torch.Tensor]     # fp32
+    grad_bias: Optional[torch.Tensor]  # fp32
+
+
+def flce_bwd(H, W, labels, lse, n_valid, grad_loss, bias=None, ignore_index=-100, reduction="sum",
+             num_label_tokens=None, chunk=None, *, want_grad_H=True, want_grad_W=True,
+             want_grad_bias=None, grad_W=None, accumulate_grad_W=False, grad_H=None,
+             grad_bias=None, ws=None, status=None) -> BackwardOut:
+    N, D, V = _flce_inputs(H, W, bias)
+    labels = _labels(labels, N)
+    dev = H.device
+    dt = _dtype_code(H)
+    ch = 0 if chunk is None else int(chunk)
+    if want_grad_bias is None:
+        want_grad_bias = bias is not None
+    if want_grad_H and grad_H is None:
+        grad_H = torch.empty((N, D), dtype=H.dtype, device=dev)
+    if want_grad_W and grad_W is None:
+        grad_W = torch.empty((V, D), dtype=torch.float32, device=dev)
+    if want_grad_bias and grad_bias is None:
+        grad_bias = torch.empty(V, dtype=torch.float32, device=dev)
+    if not want_grad_H:
+        grad_H = None
+    if not want_grad_W:
+        grad_W = None
+    if not want_grad_bias:
+        grad_bias = None
+    if ws is None:
+        ws = torch.empty(flce_workspace_bytes(dt, N, D, V, ch), dtype=torch.uint8, device=dev)
+    g = grad_loss.to(device=dev, dtype=torch.float32).reshape(1).contiguous()
+    status = status if status is not None else new_status(dev)
+    rc = _abi.flce_bwd(_ptr(H), _ptr(W), _ptr(bias), dt, N, D, V, _ptr(labels), int(ignore_index),
+                       _red_code(reduction), _nlt(num_label_tokens), _ptr(lse), _ptr(n_valid),
+                       _ptr(g), ch, _ptr(grad_H), _ptr(grad_W), 1 if accumulate_grad_W else 0,
+                       _ptr(grad_bias), _ptr(ws), ws.numel(), _ptr(status), _stream(dev))
+    _abi.check(rc, "flce_bwd")
+    return BackwardOut(grad_H, grad_W, grad_bias)
+
+
+class _FLCE(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, H, W, labels, bias, ignore_index, reduction, num_label_tokens, chunk):
+        out = flce_fwd(H, W, labels, bias, ignore_index, reduction, num_label_tokens)
+        ctx.save_for_backward(H, W, labels, bias, out.lse, out.n_valid)
+        ctx.args = (ignore_index, reduction, num_label_tokens, chunk)
+        ctx.status = out.status
+        return out.loss.reshape(())
+
+    @staticmethod
+    @once_differentiable
+    def backward(ctx, g):
+        H, W, labels, bias, lse, n_valid = ctx.saved_tensors
+        ignore_index, reduction, nlt, chunk = ctx.args
+        need_H, need_W, _, need_b = ctx.needs_input_grad[:4]
+        out = flce_bwd(H, W, labels, lse, n_valid, g, bias, ignore_index, reduction, nlt, chunk,
+                       want_grad_H=need_H, want_grad_W=need_W,
+                       want_grad_bias=bool(need_b and bias is not None), status=ctx.status)
+        # grad_W / grad_bias are accumulated in fp32; autograd casts them to the
+        # parameter dtype when that differs.
+        return out.grad_H, out.grad_W, None, out.grad_bias, None, None, None, None
+
+
+def flce(H, W, labels, bias=None, *, ignore_index=-100, reduction="mean", num_label_tokens=None,
+         chunk=None, mask=None):
+    """Fused linear cross-entropy: loss of logits = H @ W.T (+ bias), never materialised.
+
+    H: [N, D], W: [V, D] (tied-embedding layout), bias: [V] or None, labels:
+    [N] int64.  The backward recomputes the logits chunk by chunk (``chunk``
+    rows at a time; None picks the library default)."""
+    labels = _fold_mask(labels, mask, ignore_index)
+    return _FLCE.apply(H, W, labels, bias, int(ignore_index), reduction, num_label_tokens, chunk)
+
+
+# ------------------------------------------------------------------- raw GEMM
+
+def flce_gemm(A, B, C, a_mn_major=False, b_mn_major=False, accumulate=False, status=None):
+    """C (+)= op(A) @ op(B).T on the tensor cores (see include/flce_gemm.h).
+
+    A is [M, K] (K-major) or [K, M] (MN-major); B is [N, K] or [K, N]; C is
+    [M, N] float32."""
+    _cuda(A, "A")
+    _cuda(B, "B")
+    _cuda(C, "C")
+    if A.dtype != B.dtype or C.dtype != torch.float32:
+        raise TypeError("A and B share a dtype; C is float32")
+    M = A.shape[1] if a_mn_major else A.shape[0]
+    K = A.shape[0] if a_mn_major else A.shape[1]
+    Nn = B.shape[1] if b_mn_major else B.shape[0]
+    Kb = B.shape[0] if b_mn_major else B.shape[1]
+    if K != Kb or tuple(C.shape) != (M, Nn):
+        raise ValueError("inconsistent GEMM shapes")
+    status = status if status is not None else new_status(A.device)
+    rc = _abi.flce_gemm(_dtype_code(A), int(a_mn_major), int(b_mn_major), M, Nn, K, _ptr(A),
+                        A.stride(0), _ptr(B), B.stride(0), _ptr(C), C.stride(0),
+                        int(accumulate), _ptr(status), _stream(A.device))
+    _abi.check(rc, "flce_gemm")
+    return C

@@ -1,0 +1,357 @@
+// Cross-entropy over given logits [N, V]: bandwidth-bound row kernels.
+//
+// Forward (Automodel PR #2996 "feat(loss): chunked masked CE, ...", first commit
+// message): per row an fp32 log-sum-exp and the gathered label logit; the
+// per-row losses are reduced to a scalar by a fixed-order fp64 sum.  Only the
+// per-row lse (4 bytes per row) is kept for the backward, so the backward is
+// one read -> write pass over the logits.
+//
+// Backward (same page, backward bullet and the inplace_grad commit): the
+// softmax is recomputed from the logits and the saved lse, the one-hot label is
+// subtracted, the result is scaled and written either into the logits storage
+// (in place) or into a separate buffer.
+//
+// Both kernels stream each row with 16-byte vector loads (a scalar head and
+// tail handle rows whose start is not 16-byte aligned), keep the online
+// maximum and sum in the base-2 domain (one MUFU ex2 per element plus one
+// rescale per 32 elements), and merge per-thread states with warp shuffles.
+#include <math.h>
+
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "host.h"
+
+namespace flce {
+
+// ---------------------------------------------------------------- forward kernel
+
+template <typename T, int THREADS>
+__global__ void __launch_bounds__(THREADS) ce_fwd_rows_kernel(
+    const T* __restrict__ logits, int64_t N, int64_t V, int64_t ld,
+    const int64_t* __restrict__ labels, int64_t ignore_index, float* __restrict__ lse_out,
+    float* __restrict__ loss_rows, float* __restrict__ label_logit, int32_t* status) {
+  constexpr int EPV = Elem<T>::kPerVec;
+  constexpr int UNROLL = (EPV == 8) ? 4 : 8;  // 32 elements per batch
+  constexpr int NW = THREADS / 32;
+  __shared__ float red_m[NW], red_s[NW];
+  const int tid = threadIdx.x;
+
+  for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
+    const T* p = logits + row * ld;
+    Lse2 st;
+    int64_t head = static_cast<int64_t>(((16u - (reinterpret_cast<uintptr_t>(p) & 15u)) & 15u) /
+                                        sizeof(T));
+    if (head > V) head = V;
+    for (int64_t j = tid; j < head; j += THREADS) st.add1(Elem<T>::load(p + j) * kLog2e);
+    const uint4* vp = reinterpret_cast<const uint4*>(p + head);
+    const int64_t nvec = (V - head) / EPV;
+    int64_t v = tid;
+    for (; v + (UNROLL - 1) * THREADS < nvec; v += UNROLL * THREADS) {
+      uint4 u[UNROLL];
+#pragma unroll
+      for (int k = 0; k < UNROLL; ++k) u[k] = __ldcs(vp + v + k * THREADS);
+      float t[UNROLL * EPV];
+#pragma unroll
+      for (int k = 0; k < UNROLL; ++k) {
+        float x[EPV];
+        Elem<T>::unpack(u[k], x);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) t[k * EPV + e] = x[e] * kLog2e;
+      }
+      st.addk(t);
+    }
+    for (; v < nvec; v += THREADS) {
+      float x[EPV];
+      Elem<T>::unpack(__ldcs(vp + v), x);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) x[e] *= kLog2e;
+      st.addk(x);
+    }
+    for (int64_t j = head + nvec * EPV + tid; j < V; j += THREADS)
+      st.add1(Elem<T>::load(p + j) * kLog2e);
+
+    // warp merge, then across warps
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, st.m, o);
+      const float s2 = __shfl_xor_sync(0xffffffffu, st.s, o);
+      st.merge(m2, s2);
+    }
+    if ((tid & 31) == 0) {
+      red_m[tid >> 5] = st.m;
+      red_s[tid >> 5] = st.s;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      Lse2 all;
+      for (int w = 0; w < NW; ++w) all.merge(red_m[w], red_s[w]);
+      const float lse = all.m * kLn2 + logf(all.s);
+      lse_out[row] = lse;
+      const int64_t y = labels[row];
+      float li = 0.0f, zy = NAN;
+      if (y != ignore_index) {
+        if (label_ok(y, V)) {
+          zy = Elem<T>::load(p + y);
+          li = lse - zy;
+        } else {
+          set_status(status, FLCE_ELABEL);
+        }
+      }
+      loss_rows[row] = li;
+      if (label_logit != nullptr) label_logit[row] = zy;
+    }
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------- finalize kernel
+
+constexpr int kFinThreads = 1024;
+
+__global__ void __launch_bounds__(kFinThreads) finalize_kernel(
+    const float* __restrict__ loss_rows, const int64_t* __restrict__ labels, int64_t N,
+    int64_t V, int64_t ignore_index, int reduction, int64_t num_label_tokens,
+    float* __restrict__ loss, int64_t* __restrict__ n_valid) {
+  __shared__ double sacc[kFinThreads];
+  __shared__ long long scnt[kFinThreads];
+  const int tid = threadIdx.x;
+  double acc = 0.0;
+  long long cnt = 0;
+  for (int64_t i = tid; i < N; i += kFinThreads) {
+    acc += static_cast<double>(loss_rows[i]);
+    const int64_t y = labels[i];
+    cnt += (y != ignore_index && label_ok(y, V)) ? 1 : 0;
+  }
+  sacc[tid] = acc;
+  scnt[tid] = cnt;
+  __syncthreads();
+  for (int w = kFinThreads / 2; w > 0; w >>= 1) {
+    if (tid < w) {
+      sacc[tid] += sacc[tid + w];
+      scnt[tid] += scnt[tid + w];
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    const long long nv = scnt[0];
+    int64_t div;
+    if (num_label_tokens >= 0) div = num_label_tokens;
+    else if (reduction == FLCE_SUM) div = 1;
+    else div = nv;
+    *loss = div == 0 ? 0.0f : static_cast<float>(sacc[0] / static_cast<double>(div));
+    *n_valid = nv;
+  }
+}
+
+int launch_finalize(const float* loss_rows, const int64_t* labels, int64_t N, int64_t V,
+                    int64_t ignore_index, int reduction, int64_t num_label_tokens, float* loss,
+                    int64_t* n_valid, cudaStream_t stream) {
+  finalize_kernel<<<1, kFinThreads, 0, stream>>>(loss_rows, labels, N, V, ignore_index,
+                                                 reduction, num_label_tokens, loss, n_valid);
+  return launch_status();
+}
+
+// -------------------------------------------------------------- backward kernel
+
+template <typename T, int THREADS>
+__global__ void __launch_bounds__(THREADS) ce_bwd_rows_kernel(
+    const T* logits, int64_t N, int64_t V, int64_t ld, const int64_t* __restrict__ labels,
+    int64_t ignore_index, int reduction, int64_t num_label_tokens, const float* __restrict__ lse,
+    const int64_t* n_valid, const float* grad_loss, T* grad, int64_t ldg) {
+  constexpr int EPV = Elem<T>::kPerVec;
+  constexpr int UNROLL = 4;
+  const float coef = grad_coef(reduction, num_label_tokens, n_valid, grad_loss);
+  const int tid = threadIdx.x;
+
+  for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
+    const T* p = logits + row * ld;
+    T* q = grad + row * ldg;
+    const int64_t y = labels[row];
+    const bool valid = (y != ignore_index) && label_ok(y, V);
+    const float c = valid ? coef : 0.0f;
+    const float lse2 = lse[row] * kLog2e;
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(p) & 15u;
+    const uintptr_t qa = reinterpret_cast<uintptr_t>(q) & 15u;
+    int64_t head = (pa == qa) ? static_cast<int64_t>(((16u - pa) & 15u) / sizeof(T)) : V;
+    if (head > V) head = V;
+
+    auto one = [&](int64_t j) {
+      float d = 0.0f;
+      if (c != 0.0f) {
+        const float x = Elem<T>::load(p + j);
+        d = (ex2(fmaf(x, kLog2e, -lse2)) - (j == y ? 1.0f : 0.0f)) * c;
+      }
+      Elem<T>::store(q + j, d);
+    };
+    for (int64_t j = tid; j < head; j += THREADS) one(j);
+    const uint4* vp = reinterpret_cast<const uint4*>(p + head);
+    uint4* vq = reinterpret_cast<uint4*>(q + head);
+    const int64_t nvec = (V - head) / EPV;
+    if (c == 0.0f) {
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      for (int64_t v = tid; v < nvec; v += THREADS) __stcs(vq + v, z);
+    } else {
+      const int64_t ylocal = y - head;  // label position relative to the vector body
+      int64_t v = tid;
+      for (; v + (UNROLL - 1) * THREADS < nvec; v += UNROLL * THREADS) {
+        uint4 u[UNROLL];
+#pragma unroll
+        for (int k = 0; k < UNROLL; ++k) u[k] = __ldcs(vp + v + k * THREADS);
+#pragma unroll
+        for (int k = 0; k < UNROLL; ++k) {
+          float x[EPV];
+          Elem<T>::unpack(u[k], x);
+          const int64_t j0 = (v + k * THREADS) * EPV;
+#pragma unroll
+          for (int e = 0; e < EPV; ++e)
+            x[e] = (ex2(fmaf(x[e], kLog2e, -lse2)) - (j0 + e == ylocal ? 1.0f : 0.0f)) * c;
+          __stcs(vq + v + k * THREADS, Elem<T>::pack(x));
+        }
+      }
+      for (; v < nvec; v += THREADS) {
+        float x[EPV];
+        Elem<T>::unpack(__ldcs(vp + v), x);
+        const int64_t j0 = v * EPV;
+#pragma unroll
+        for (int e = 0; e < EPV; ++e)
+          x[e] = (ex2(fmaf(x[e], kLog2e, -lse2)) - (j0 + e == ylocal ? 1.0f : 0.0f)) * c;
+        __stcs(vq + v, Elem<T>::pack(x));
+      }
+    }
+    for (int64_t j = head + nvec * EPV + tid; j < V; j += THREADS) one(j);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+static std::mutex g_sm_mutex;
+static std::vector<int> g_sm_counts;
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  std::lock_guard<std::mutex> lock(g_sm_mutex);
+  if (static_cast<int>(g_sm_counts.size()) <= dev) g_sm_counts.resize(dev + 1, 0);
+  if (g_sm_counts[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_sm_counts[dev] = n > 0 ? n : 1;
+  }
+  return g_sm_counts[dev];
+}
+
+}  // namespace flce
+
+using namespace flce;
+
+extern "C" const char* flce_status_string(int status) {
+  switch (status) {
+    case FLCE_OK: return "FLCE_OK";
+    case FLCE_EINVAL: return "FLCE_EINVAL: null pointer or bad argument";
+    case FLCE_ESHAPE: return "FLCE_ESHAPE: size out of range or inconsistent";
+    case FLCE_EDTYPE: return "FLCE_EDTYPE: unsupported dtype";
+    case FLCE_EALIGN: return "FLCE_EALIGN: pointer or row stride misaligned";
+    case FLCE_ELABEL: return "FLCE_ELABEL: label outside [0, V) that is not ignore_index";
+    case FLCE_EWORKSPACE: return "FLCE_EWORKSPACE: workspace missing or too small";
+    case FLCE_ECUDA: return "FLCE_ECUDA: CUDA call failed";
+    case FLCE_ENOSUP: return "FLCE_ENOSUP: not supported by this build";
+    case FLCE_ETIMEOUT: return "FLCE_ETIMEOUT: a bounded wait inside a kernel gave up";
+    default: return "FLCE: unknown status";
+  }
+}
+
+extern "C" size_t ce_logits_workspace_bytes(int64_t N, int64_t V) {
+  (void)V;
+  if (N <= 0) return 0;
+  return round_up(static_cast<size_t>(N) * sizeof(float), 256);
+}
+
+static int ce_common_checks(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
+                            const int64_t* labels, int reduction) {
+  if (!valid_dtype(dt)) return FLCE_EDTYPE;
+  if (!valid_reduction(reduction)) return FLCE_EINVAL;
+  if (N < 0 || V < 1 || V >= (int64_t(1) << 31) || ld < V) return FLCE_ESHAPE;
+  if (N > 0 && (logits == nullptr || labels == nullptr)) return FLCE_EINVAL;
+  if (!aligned(logits, dtype_size(dt)) || !aligned(labels, 8)) return FLCE_EALIGN;
+  return FLCE_OK;
+}
+
+static int row_grid(int64_t N) {
+  const int64_t g = static_cast<int64_t>(sm_count()) * 4;
+  return static_cast<int>(N < g ? (N > 0 ? N : 1) : g);
+}
+
+extern "C" int ce_logits_fwd(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
+                             const int64_t* labels, int64_t ignore_index, int reduction,
+                             int64_t num_label_tokens, float* loss, int64_t* n_valid, float* lse,
+                             float* loss_rows, float* label_logit, void* ws, size_t ws_bytes,
+                             int32_t* status, flce_stream_t stream) {
+  int rc = ce_common_checks(logits, dt, N, V, ld, labels, reduction);
+  if (rc != FLCE_OK) return rc;
+  if (loss == nullptr || n_valid == nullptr || status == nullptr) return FLCE_EINVAL;
+  if (N > 0 && lse == nullptr) return FLCE_EINVAL;
+  float* rows = loss_rows;
+  if (rows == nullptr && N > 0) {
+    if (ws == nullptr || ws_bytes < ce_logits_workspace_bytes(N, V)) return FLCE_EWORKSPACE;
+    if (!aligned(ws, 16)) return FLCE_EALIGN;
+    rows = static_cast<float*>(ws);
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (N > 0) {
+    const int grid = row_grid(N);
+    if (dt == FLCE_BF16) {
+      ce_fwd_rows_kernel<__nv_bfloat16, 512><<<grid, 512, 0, s>>>(
+          static_cast<const __nv_bfloat16*>(logits), N, V, ld, labels, ignore_index, lse, rows,
+          label_logit, status);
+    } else {
+      ce_fwd_rows_kernel<float, 512><<<grid, 512, 0, s>>>(static_cast<const float*>(logits), N,
+                                                          V, ld, labels, ignore_index, lse,
+                                                          rows, label_logit, status);
+    }
+    rc = launch_status();
+    if (rc != FLCE_OK) return rc;
+  }
+  return launch_finalize(rows, labels, N, V, ignore_index, reduction, num_label_tokens, loss,
+                         n_valid, s);
+}
+
+extern "C" int ce_logits_bwd(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
+                             const int64_t* labels, int64_t ignore_index, int reduction,
+                             int64_t num_label_tokens, const float* lse, const int64_t* n_valid,
+                             const float* grad_loss, int inplace_grad, void* grad_logits,
+                             int64_t ld_grad, int32_t* status, flce_stream_t stream) {
+  int rc = ce_common_checks(logits, dt, N, V, ld, labels, reduction);
+  if (rc != FLCE_OK) return rc;
+  if (status == nullptr) return FLCE_EINVAL;
+  if (N == 0) return FLCE_OK;
+  if (lse == nullptr || n_valid == nullptr || grad_loss == nullptr || grad_logits == nullptr)
+    return FLCE_EINVAL;
+  if (inplace_grad != 0 && inplace_grad != 1) return FLCE_EINVAL;
+  if (ld_grad < V) return FLCE_ESHAPE;
+  if (!aligned(grad_logits, dtype_size(dt))) return FLCE_EALIGN;
+  const size_t es = dtype_size(dt);
+  const char* a0 = static_cast<const char*>(logits);
+  const char* a1 = a0 + ((N - 1) * ld + V) * es;
+  const char* b0 = static_cast<const char*>(grad_logits);
+  const char* b1 = b0 + ((N - 1) * ld_grad + V) * es;
+  if (inplace_grad) {
+    if (b0 != a0 || ld_grad != ld) return FLCE_EINVAL;
+  } else if (b0 < a1 && a0 < b1) {
+    return FLCE_EINVAL;  // out-of-place buffers must not overlap
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int grid = row_grid(N);
+  if (dt == FLCE_BF16) {
+    ce_bwd_rows_kernel<__nv_bfloat16, 512><<<grid, 512, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(logits), N, V, ld, labels, ignore_index, reduction,
+        num_label_tokens, lse, n_valid, grad_loss, static_cast<__nv_bfloat16*>(grad_logits),
+        ld_grad);
+  } else {
+    ce_bwd_rows_kernel<float, 512><<<grid, 512, 0, s>>>(
+        static_cast<const float*>(logits), N, V, ld, labels, ignore_index, reduction,
+        num_label_tokens, lse, n_valid, grad_loss, static_cast<float*>(grad_logits), ld_grad);
+  }
+  return launch_status();
+}

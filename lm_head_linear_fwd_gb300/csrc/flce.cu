@@ -1,0 +1,587 @@
+// Fused linear cross-entropy: logits = H W^T (+ bias) formed tile by tile on
+// the tensor cores and never stored.
+//
+// Forward (Liger-Kernel issue #533 "Gradient checkpointing for grad_weight in
+// LFCE": chunked logits; the fully recomputed variant of its follow-up
+// comments keeps no gradient from the forward): one persistent tcgen05 GEMM
+// over (token tile, vocab tile) pairs whose epilogue turns each 128 x BN
+// logits tile into a per-row partial (max, sum of exp) in the base-2 domain
+// and picks out the label logit; a combine kernel merges the partials of a row
+// in a fixed order into lse_i and loss_i; the shared finalize kernel reduces.
+//
+// Backward, per chunk of C rows:
+//   1. the same GEMM recomputes the logits of the chunk; its epilogue forms
+//      dZ = valid (exp(z - lse) - onehot) g scale and writes it, rounded to the
+//      input dtype, to a [C, ldV] workspace buffer (Liger's feature pitch
+//      casts the chunk's gradient to the input dtype before the addmm);
+//   2. grad_bias += column sums of dZ (two fixed-order passes, no atomics);
+//   3. grad_H[chunk] = dZ W                (A = dZ K-major, B = W MN-major);
+//   4. grad_W (+)= dZ^T H[chunk] in fp32   (A = dZ MN-major, B = H MN-major),
+//      the addmm with beta = 1 of the same page, chunk after chunk.
+#include <math.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/flce_gemm.h"
+#include "host.h"
+#include "tc_gemm.cuh"
+
+namespace flce {
+
+// ----------------------------------------------------------------- epilogues
+
+template <typename T>
+__device__ __forceinline__ float load_elem(const void* p, int64_t i) {
+  return Elem<T>::load(static_cast<const T*>(p) + i);
+}
+
+// Forward: per-row partial log-sum-exp of one logits tile + label gather.
+template <typename T>
+struct EpiLse {
+  struct Params {
+    const void* bias;  // [V] of T or null
+    const int64_t* labels;
+    int64_t ignore_index;
+    int M, V;
+    int64_t part_ld;   // row stride of part_m / part_s (>= M)
+    float* part_m;     // [nNt, part_ld], base-2 max
+    float* part_s;     // [nNt, part_ld], sum of 2^(t - max)
+    float* zlab;       // [M] label logit (written by the tile holding the label)
+  };
+  template <int BN>
+  __device__ static void tile(const Params& p, int mt, int nt, int row_in_tile, uint32_t taddr) {
+    const int row = mt * kBM + row_in_tile;
+    const bool row_ok = row < p.M;
+    const int64_t y = row_ok ? p.labels[row] : -1;
+    const int col_base = nt * BN;
+    const int64_t ylocal = y - col_base;
+    Lse2 st;
+    float zy = 0.0f;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int col0 = col_base + c * 32;
+      if (col0 >= p.V) break;  // uniform across the warp
+      float v[32];
+      tmem_ld32(taddr + c * 32, v);
+      float t[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float x = v[j];
+        if (p.bias != nullptr && col0 + j < p.V) x += load_elem<T>(p.bias, col0 + j);
+        if (c * 32 + j == ylocal) zy = x;
+        t[j] = (col0 + j < p.V) ? x * kLog2e : -INFINITY;
+      }
+      st.addk(t);
+    }
+    if (row_ok) {
+      p.part_m[nt * p.part_ld + row] = st.m;
+      p.part_s[nt * p.part_ld + row] = st.s;
+      if (ylocal >= 0 && ylocal < BN) p.zlab[row] = zy;
+    }
+  }
+};
+
+// Backward step 1: dZ of one recomputed logits tile, stored as T.
+template <typename T>
+struct EpiDlogits {
+  struct Params {
+    const void* bias;
+    const int64_t* labels;  // chunk-relative (already offset)
+    int64_t ignore_index;
+    const float* lse;       // chunk-relative
+    int reduction;
+    int64_t num_label_tokens;
+    const int64_t* n_valid;
+    const float* grad_loss;
+    int M, V;               // M = rows in this chunk
+    T* dz;                  // [M, ldd]
+    int64_t ldd;
+  };
+  template <int BN>
+  __device__ static void tile(const Params& p, int mt, int nt, int row_in_tile, uint32_t taddr) {
+    const int row = mt * kBM + row_in_tile;
+    const bool row_ok = row < p.M;
+    const int64_t y = row_ok ? p.labels[row] : p.ignore_index;
+    const bool valid = row_ok && y != p.ignore_index && label_ok(y, p.V);
+    const float c = valid ? grad_coef(p.reduction, p.num_label_tokens, p.n_valid, p.grad_loss)
+                          : 0.0f;
+    const float lse2 = row_ok ? p.lse[row] * kLog2e : 0.0f;
+    const int col_base = nt * BN;
+    const int64_t ylocal = y - col_base;
+    T* out = p.dz + static_cast<int64_t>(row) * p.ldd;
+#pragma unroll 1
+    for (int cc = 0; cc < BN / 32; ++cc) {
+      const int col0 = col_base + cc * 32;
+      if (col0 >= p.V) break;
+      float v[32];
+      tmem_ld32(taddr + cc * 32, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float x = v[j];
+        if (p.bias != nullptr && col0 + j < p.V) x += load_elem<T>(p.bias, col0 + j);
+        v[j] = (ex2(fmaf(x, kLog2e, -lse2)) - (cc * 32 + j == ylocal ? 1.0f : 0.0f)) * c;
+      }
+      if (!row_ok) continue;
+      constexpr int EPV = Elem<T>::kPerVec;
+      if (col0 + 32 <= p.V) {
+        uint4* q = reinterpret_cast<uint4*>(out + col0);
+#pragma unroll
+        for (int k = 0; k < 32 / EPV; ++k) {
+          float x[EPV];
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) x[e] = v[k * EPV + e];
+          q[k] = Elem<T>::pack(x);
+        }
+      } else {
+        for (int j = 0; j < 32 && col0 + j < p.V; ++j) Elem<T>::store(out + col0 + j, v[j]);
+      }
+    }
+  }
+};
+
+// Store the accumulator as OutT (grad_H), or add it into an fp32 matrix (grad_W).
+template <typename OutT, bool kAccumulate>
+struct EpiStore {
+  struct Params {
+    OutT* out;
+    int64_t ldo;
+    int M, N;
+    int beta;  // fp32 accumulate variant: 1 adds to the existing contents
+  };
+  template <int BN>
+  __device__ static void tile(const Params& p, int mt, int nt, int row_in_tile, uint32_t taddr) {
+    const int row = mt * kBM + row_in_tile;
+    const bool row_ok = row < p.M;
+    OutT* out = p.out + static_cast<int64_t>(row) * p.ldo;
+#pragma unroll 1
+    for (int cc = 0; cc < BN / 32; ++cc) {
+      const int col0 = nt * BN + cc * 32;
+      if (col0 >= p.N) break;
+      float v[32];
+      tmem_ld32(taddr + cc * 32, v);
+      if (!row_ok) continue;
+      constexpr int EPV = Elem<OutT>::kPerVec;
+      if (col0 + 32 <= p.N) {
+        uint4* q = reinterpret_cast<uint4*>(out + col0);
+#pragma unroll
+        for (int k = 0; k < 32 / EPV; ++k) {
+          float x[EPV];
+          if (kAccumulate && p.beta) {
+            Elem<OutT>::unpack(q[k], x);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) x[e] += v[k * EPV + e];
+          } else {
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) x[e] = v[k * EPV + e];
+          }
+          q[k] = Elem<OutT>::pack(x);
+        }
+      } else {
+        for (int j = 0; j < 32 && col0 + j < p.N; ++j) {
+          float x = v[j];
+          if (kAccumulate && p.beta) x += Elem<OutT>::load(out + col0 + j);
+          Elem<OutT>::store(out + col0 + j, x);
+        }
+      }
+    }
+  }
+};
+
+// ------------------------------------------------------------ small kernels
+
+// Merges the per-tile partials of each row in a fixed order.
+__global__ void __launch_bounds__(256) lse_combine_kernel(
+    const float* __restrict__ part_m, const float* __restrict__ part_s, int nparts,
+    int64_t part_ld, const float* __restrict__ zlab, const int64_t* __restrict__ labels,
+    int64_t N, int64_t V, int64_t ignore_index, float* __restrict__ lse_out,
+    float* __restrict__ loss_rows, float* __restrict__ label_logit, int32_t* status) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (row >= N) return;
+  Lse2 st;
+  for (int p = 0; p < nparts; ++p) st.merge(part_m[p * part_ld + row], part_s[p * part_ld + row]);
+  const float lse = st.m * kLn2 + logf(st.s);
+  lse_out[row] = lse;
+  const int64_t y = labels[row];
+  float li = 0.0f, zy = NAN;
+  if (y != ignore_index) {
+    if (label_ok(y, V)) {
+      zy = zlab[row];
+      li = lse - zy;
+    } else {
+      set_status(status, FLCE_ELABEL);
+    }
+  }
+  loss_rows[row] = li;
+  if (label_logit != nullptr) label_logit[row] = zy;
+}
+
+constexpr int kColSplits = 16;
+
+// Column sums of dZ [M, ldd] over row slices: part[s, v] = sum of rows in slice s.
+template <typename T>
+__global__ void __launch_bounds__(256) colsum_partial_kernel(const T* __restrict__ dz, int M,
+                                                             int64_t ldd, int V,
+                                                             float* __restrict__ part) {
+  const int v = blockIdx.x * blockDim.x + threadIdx.x;
+  if (v >= V) return;
+  const int s = blockIdx.y;
+  const int per = (M + kColSplits - 1) / kColSplits;
+  const int r0 = s * per, r1 = min(M, r0 + per);
+  float acc = 0.0f;
+  for (int r = r0; r < r1; ++r) acc += Elem<T>::load(dz + static_cast<int64_t>(r) * ldd + v);
+  part[static_cast<int64_t>(s) * V + v] = acc;
+}
+
+__global__ void __launch_bounds__(256) colsum_final_kernel(const float* __restrict__ part, int V,
+                                                           float* __restrict__ out, int beta) {
+  const int v = blockIdx.x * blockDim.x + threadIdx.x;
+  if (v >= V) return;
+  float acc = beta ? out[v] : 0.0f;
+  for (int s = 0; s < kColSplits; ++s) acc += part[static_cast<int64_t>(s) * V + v];
+  out[v] = acc;
+}
+
+// --------------------------------------------------------------- host: TMA
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D map over a row-major matrix [outer, inner] with the given row stride, box
+// {128 bytes of inner, box_outer rows}, 128-byte swizzle, zero fill outside.
+static int make_map(CUtensorMap* m, const void* base, int dt, uint64_t inner, uint64_t outer,
+                    uint64_t row_stride_elems, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return FLCE_ECUDA;
+  const uint64_t es = dtype_size(dt);
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride_elems * es};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / es), box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, dt == FLCE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                  2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FLCE_OK : FLCE_ECUDA;
+}
+
+// Operand description for the host launcher.
+struct Operand {
+  const void* ptr;
+  int64_t rows;      // extent along M (for A) or N (for B)
+  int64_t k;         // extent along K
+  int64_t ld;        // row stride in elements of the stored matrix
+  bool mn_major;     // stored as [K, rows] (true) or [rows, K] (false)
+};
+
+static int make_operand_map(CUtensorMap* m, const Operand& op, int dt, int tile_rows) {
+  const int ek = 128 / static_cast<int>(dtype_size(dt));
+  if (!op.mn_major) return make_map(m, op.ptr, dt, op.k, op.rows, op.ld, tile_rows);
+  return make_map(m, op.ptr, dt, op.rows, op.k, op.ld, ek);
+}
+
+template <typename T, int BN, bool A_MN, bool B_MN, class Epi>
+static int launch_gemm(const Operand& a, const Operand& b, int M, int N, int K, int group_m,
+                       const typename Epi::Params& ep, int32_t* status, cudaStream_t s) {
+  using G = GemmGeo<T, BN>;
+  const int dt = sizeof(T) == 2 ? FLCE_BF16 : FLCE_F32;
+  CUtensorMap ma, mb;
+  int rc = make_operand_map(&ma, a, dt, kBM);
+  if (rc != FLCE_OK) return rc;
+  rc = make_operand_map(&mb, b, dt, BN);
+  if (rc != FLCE_OK) return rc;
+  GemmArgs ga;
+  ga.M = M;
+  ga.N = N;
+  ga.K = K;
+  ga.nMt = (M + kBM - 1) / kBM;
+  ga.nNt = (N + BN - 1) / BN;
+  ga.nK = (K + G::kEK - 1) / G::kEK;
+  ga.group_m = std::max(1, std::min(group_m, ga.nMt));
+  ga.status = status;
+  const int tiles = ga.nMt * ga.nNt;
+  if (tiles == 0) return FLCE_OK;
+  auto kern = tc_gemm_kernel<T, BN, A_MN, B_MN, Epi>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes) !=
+      cudaSuccess)
+    return FLCE_ECUDA;
+  const int grid = std::min(tiles, sm_count());
+  kern<<<grid, kGemmThreads, G::kSmemBytes, s>>>(ma, mb, ga, ep);
+  return launch_status();
+}
+
+// Group of M-tiles sharing one sweep over the N-tiles: as many 128-row slabs of
+// the A operand as fit in about 40 MB of L2.
+static int group_for(int64_t K, int dt, int nMt) {
+  const int64_t slab = static_cast<int64_t>(kBM) * K * static_cast<int64_t>(dtype_size(dt));
+  int64_t g = (40ll << 20) / std::max<int64_t>(slab, 1);
+  g = std::max<int64_t>(1, std::min<int64_t>(g, nMt));
+  return static_cast<int>(g);
+}
+
+// ------------------------------------------------------------ workspace plan
+
+constexpr int kBNFwd = 256;
+
+struct FlcePlan {
+  int64_t ldV;         // row stride of the dZ chunk buffer (elements)
+  int64_t chunk;
+  int nparts;          // vocab tiles of the forward
+  int64_t part_ld;
+  size_t off_part_m, off_part_s, off_zlab, off_rows, fwd_bytes;
+  size_t off_dz, off_colsum, bwd_bytes;
+  size_t total;
+};
+
+static int64_t default_chunk(int dt, int64_t N, int64_t D, int64_t V) {
+  (void)dt;
+  (void)D;
+  (void)V;
+  int64_t c = 4096;
+  const int64_t n128 = (N + 127) / 128 * 128;
+  return std::max<int64_t>(128, std::min(c, n128));
+}
+
+static FlcePlan plan(int dt, int64_t N, int64_t D, int64_t V, int64_t chunk) {
+  (void)D;
+  FlcePlan p;
+  const size_t es = dtype_size(dt);
+  p.chunk = chunk > 0 ? chunk : default_chunk(dt, N, D, V);
+  p.ldV = (V + 63) / 64 * 64;
+  p.nparts = static_cast<int>((V + kBNFwd - 1) / kBNFwd);
+  p.part_ld = (N + 63) / 64 * 64;
+  size_t o = 0;
+  p.off_part_m = o;
+  o += round_up(static_cast<size_t>(p.nparts) * p.part_ld * 4, 256);
+  p.off_part_s = o;
+  o += round_up(static_cast<size_t>(p.nparts) * p.part_ld * 4, 256);
+  p.off_zlab = o;
+  o += round_up(static_cast<size_t>(N) * 4, 256);
+  p.off_rows = o;
+  o += round_up(static_cast<size_t>(N) * 4, 256);
+  p.fwd_bytes = o;
+  o = 0;
+  p.off_dz = o;
+  o += round_up(static_cast<size_t>(std::min<int64_t>(p.chunk, N)) * p.ldV * es, 256);
+  p.off_colsum = o;
+  o += round_up(static_cast<size_t>(kColSplits) * V * 4, 256);
+  p.bwd_bytes = o;
+  p.total = std::max(p.fwd_bytes, p.bwd_bytes);
+  return p;
+}
+
+static int flce_checks(const void* H, const void* W, int dt, int64_t N, int64_t D, int64_t V,
+                       const int64_t* labels, int reduction) {
+  if (!valid_dtype(dt)) return FLCE_EDTYPE;
+  if (!valid_reduction(reduction)) return FLCE_EINVAL;
+  if (N < 1 || D < 8 || V < 1 || V >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) ||
+      D >= (int64_t(1) << 31))
+    return FLCE_ESHAPE;
+  if (H == nullptr || W == nullptr || labels == nullptr) return FLCE_EINVAL;
+  if (!aligned(H, 16) || !aligned(W, 16) || (D * static_cast<int64_t>(dtype_size(dt))) % 16 != 0)
+    return FLCE_EALIGN;
+  if (!aligned(labels, 8)) return FLCE_EALIGN;
+  return FLCE_OK;
+}
+
+}  // namespace flce
+
+using namespace flce;
+
+extern "C" int64_t flce_default_chunk(int dt, int64_t N, int64_t D, int64_t V) {
+  return default_chunk(dt, N, D, V);
+}
+
+extern "C" size_t flce_workspace_bytes(int dt, int64_t N, int64_t D, int64_t V, int64_t chunk) {
+  if (!valid_dtype(dt) || N < 1 || V < 1) return 0;
+  return plan(dt, N, D, V, chunk).total;
+}
+
+extern "C" int flce_fwd(const void* H, const void* W, const void* bias, int dt, int64_t N,
+                        int64_t D, int64_t V, const int64_t* labels, int64_t ignore_index,
+                        int reduction, int64_t num_label_tokens, float* loss, int64_t* n_valid,
+                        float* lse, float* loss_rows, float* label_logit, void* ws,
+                        size_t ws_bytes, int32_t* status, flce_stream_t stream) {
+  int rc = flce_checks(H, W, dt, N, D, V, labels, reduction);
+  if (rc != FLCE_OK) return rc;
+  if (loss == nullptr || n_valid == nullptr || lse == nullptr || status == nullptr)
+    return FLCE_EINVAL;
+  if (bias != nullptr && !aligned(bias, dtype_size(dt))) return FLCE_EALIGN;
+  const FlcePlan p = plan(dt, N, D, V, 0);
+  if (ws == nullptr || ws_bytes < p.fwd_bytes) return FLCE_EWORKSPACE;
+  if (!aligned(ws, 256)) return FLCE_EALIGN;
+  char* w = static_cast<char*>(ws);
+  float* part_m = reinterpret_cast<float*>(w + p.off_part_m);
+  float* part_s = reinterpret_cast<float*>(w + p.off_part_s);
+  float* zlab = reinterpret_cast<float*>(w + p.off_zlab);
+  float* rows = loss_rows != nullptr ? loss_rows : reinterpret_cast<float*>(w + p.off_rows);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  const Operand a{H, N, D, D, false};
+  const Operand b{W, V, D, D, false};
+  const int group = group_for(D, dt, static_cast<int>((N + kBM - 1) / kBM));
+  if (dt == FLCE_BF16) {
+    using E = EpiLse<__nv_bfloat16>;
+    E::Params ep{bias, labels, ignore_index, static_cast<int>(N), static_cast<int>(V),
+                 p.part_ld, part_m, part_s, zlab};
+    rc = launch_gemm<__nv_bfloat16, kBNFwd, false, false, E>(a, b, (int)N, (int)V, (int)D, group,
+                                                             ep, status, s);
+  } else {
+    using E = EpiLse<float>;
+    E::Params ep{bias, labels, ignore_index, static_cast<int>(N), static_cast<int>(V),
+                 p.part_ld, part_m, part_s, zlab};
+    rc = launch_gemm<float, kBNFwd, false, false, E>(a, b, (int)N, (int)V, (int)D, group, ep,
+                                                     status, s);
+  }
+  if (rc != FLCE_OK) return rc;
+  lse_combine_kernel<<<static_cast<unsigned>((N + 255) / 256), 256, 0, s>>>(
+      part_m, part_s, p.nparts, p.part_ld, zlab, labels, N, V, ignore_index, lse, rows,
+      label_logit, status);
+  rc = launch_status();
+  if (rc != FLCE_OK) return rc;
+  return launch_finalize(rows, labels, N, V, ignore_index, reduction, num_label_tokens, loss,
+                         n_valid, s);
+}
+
+template <typename T>
+static int flce_bwd_impl(const void* H, const void* W, const void* bias, int64_t N, int64_t D,
+                         int64_t V, const int64_t* labels, int64_t ignore_index, int reduction,
+                         int64_t num_label_tokens, const float* lse, const int64_t* n_valid,
+                         const float* grad_loss, const FlcePlan& p, void* grad_H,
+                         float* grad_W, int accumulate_grad_W, float* grad_bias, char* w,
+                         int32_t* status, cudaStream_t s) {
+  const int dt = sizeof(T) == 2 ? FLCE_BF16 : FLCE_F32;
+  T* dz = reinterpret_cast<T*>(w + p.off_dz);
+  float* colsum = reinterpret_cast<float*>(w + p.off_colsum);
+  const T* Ht = static_cast<const T*>(H);
+  int rc = FLCE_OK;
+  for (int64_t r0 = 0; r0 < N; r0 += p.chunk) {
+    const int C = static_cast<int>(std::min<int64_t>(p.chunk, N - r0));
+    const int nMt = (C + kBM - 1) / kBM;
+    // 1. recompute logits, form dZ
+    {
+      using E = EpiDlogits<T>;
+      typename E::Params ep{bias, labels + r0, ignore_index, lse + r0, reduction,
+                            num_label_tokens, n_valid, grad_loss, C, static_cast<int>(V), dz,
+                            p.ldV};
+      const Operand a{Ht + r0 * D, C, D, D, false};
+      const Operand b{W, V, D, D, false};
+      rc = launch_gemm<T, kBNFwd, false, false, E>(a, b, C, (int)V, (int)D,
+                                                   group_for(D, dt, nMt), ep, status, s);
+      if (rc != FLCE_OK) return rc;
+    }
+    // 2. bias gradient
+    if (grad_bias != nullptr) {
+      dim3 g1(static_cast<unsigned>((V + 255) / 256), kColSplits);
+      colsum_partial_kernel<T><<<g1, 256, 0, s>>>(dz, C, p.ldV, (int)V, colsum);
+      colsum_final_kernel<<<static_cast<unsigned>((V + 255) / 256), 256, 0, s>>>(
+          colsum, (int)V, grad_bias, r0 > 0 ? 1 : 0);
+      rc = launch_status();
+      if (rc != FLCE_OK) return rc;
+    }
+    // 3. grad_H[chunk] = dZ W
+    if (grad_H != nullptr) {
+      using E = EpiStore<T, false>;
+      typename E::Params ep{static_cast<T*>(grad_H) + r0 * D, D, C, static_cast<int>(D), 0};
+      const Operand a{dz, C, V, p.ldV, false};
+      const Operand b{W, D, V, D, true};
+      rc = launch_gemm<T, 256, false, true, E>(a, b, C, (int)D, (int)V, 8, ep, status, s);
+      if (rc != FLCE_OK) return rc;
+    }
+    // 4. grad_W (+)= dZ^T H[chunk]
+    if (grad_W != nullptr) {
+      using E = EpiStore<float, true>;
+      typename E::Params ep{grad_W, D, static_cast<int>(V), static_cast<int>(D),
+                            (r0 > 0 || accumulate_grad_W) ? 1 : 0};
+      const Operand a{dz, V, C, p.ldV, true};
+      const Operand b{Ht + r0 * D, D, C, D, true};
+      rc = launch_gemm<T, 256, true, true, E>(a, b, (int)V, (int)D, C, 8, ep, status, s);
+      if (rc != FLCE_OK) return rc;
+    }
+  }
+  return rc;
+}
+
+extern "C" int flce_bwd(const void* H, const void* W, const void* bias, int dt, int64_t N,
+                        int64_t D, int64_t V, const int64_t* labels, int64_t ignore_index,
+                        int reduction, int64_t num_label_tokens, const float* lse,
+                        const int64_t* n_valid, const float* grad_loss, int64_t chunk,
+                        void* grad_H, float* grad_W, int accumulate_grad_W, float* grad_bias,
+                        void* ws, size_t ws_bytes, int32_t* status, flce_stream_t stream) {
+  int rc = flce_checks(H, W, dt, N, D, V, labels, reduction);
+  if (rc != FLCE_OK) return rc;
+  if (lse == nullptr || n_valid == nullptr || grad_loss == nullptr || status == nullptr)
+    return FLCE_EINVAL;
+  if (accumulate_grad_W != 0 && accumulate_grad_W != 1) return FLCE_EINVAL;
+  if (chunk > 0 && chunk % kBM != 0 && chunk < N) return FLCE_ESHAPE;
+  if (bias != nullptr && !aligned(bias, dtype_size(dt))) return FLCE_EALIGN;
+  if (grad_H != nullptr && !aligned(grad_H, 16)) return FLCE_EALIGN;
+  if (grad_W != nullptr && !aligned(grad_W, 16)) return FLCE_EALIGN;
+  if (grad_bias != nullptr && !aligned(grad_bias, 4)) return FLCE_EALIGN;
+  const FlcePlan p = plan(dt, N, D, V, chunk);
+  if (ws == nullptr || ws_bytes < p.bwd_bytes) return FLCE_EWORKSPACE;
+  if (!aligned(ws, 256)) return FLCE_EALIGN;
+  if (grad_H == nullptr && grad_W == nullptr && grad_bias == nullptr) return FLCE_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  if (dt == FLCE_BF16)
+    return flce_bwd_impl<__nv_bfloat16>(H, W, bias, N, D, V, labels, ignore_index, reduction,
+                                        num_label_tokens, lse, n_valid, grad_loss, p, grad_H,
+                                        grad_W, accumulate_grad_W, grad_bias, w, status, s);
+  return flce_bwd_impl<float>(H, W, bias, N, D, V, labels, ignore_index, reduction,
+                              num_label_tokens, lse, n_valid, grad_loss, p, grad_H, grad_W,
+                              accumulate_grad_W, grad_bias, w, status, s);
+}
+
+// ------------------------------------------------------ raw GEMM entry point
+
+extern "C" int flce_gemm(int dt, int a_mn_major, int b_mn_major, int64_t M, int64_t N, int64_t K,
+                         const void* A, int64_t lda, const void* B, int64_t ldb, float* C,
+                         int64_t ldc, int accumulate, int32_t* status, flce_stream_t stream) {
+  if (!valid_dtype(dt)) return FLCE_EDTYPE;
+  if (M < 1 || N < 1 || K < 1 || M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) ||
+      K >= (int64_t(1) << 31))
+    return FLCE_ESHAPE;
+  if (A == nullptr || B == nullptr || C == nullptr || status == nullptr) return FLCE_EINVAL;
+  if ((a_mn_major != 0 && a_mn_major != 1) || (b_mn_major != 0 && b_mn_major != 1) ||
+      (accumulate != 0 && accumulate != 1))
+    return FLCE_EINVAL;
+  const int64_t es = static_cast<int64_t>(dtype_size(dt));
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || (lda * es) % 16 != 0 ||
+      (ldb * es) % 16 != 0 || ldc % 4 != 0)
+    return FLCE_EALIGN;
+  if (lda < (a_mn_major ? M : K) || ldb < (b_mn_major ? N : K) || ldc < N) return FLCE_ESHAPE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const Operand a{A, M, K, lda, a_mn_major != 0};
+  const Operand b{B, N, K, ldb, b_mn_major != 0};
+  using E = EpiStore<float, true>;
+  E::Params ep{C, ldc, static_cast<int>(M), static_cast<int>(N), accumulate};
+  const int code = (dt == FLCE_BF16 ? 0 : 4) | (a_mn_major ? 2 : 0) | (b_mn_major ? 1 : 0);
+  switch (code) {
+    case 0: return launch_gemm<__nv_bfloat16, 256, false, false, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
+    case 1: return launch_gemm<__nv_bfloat16, 256, false, true, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
+    case 2: return launch_gemm<__nv_bfloat16, 256, true, false, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
+    case 3: return launch_gemm<__nv_bfloat16, 256, true, true, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
+    case 4: return launch_gemm<float, 256, false, false, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
+    case 5: return launch_gemm<float, 256, false, true, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
+    case 6: return launch_gemm<float, 256, true, false, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
+    default: return launch_gemm<float, 256, true, true, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
+  }
+}

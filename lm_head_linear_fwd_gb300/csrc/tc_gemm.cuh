@@ -1,0 +1,282 @@
+// Persistent tcgen05 GEMM with a pluggable epilogue, for sm_103a.
+//
+//   acc[m, n] = sum_k A[m, k] * B[n, k]          (fp32 accumulation in TMEM)
+//
+// A and B are each either K-major (row-major [rows, K]) or MN-major (row-major
+// [K, rows]); both come from global memory through TMA with 128-byte swizzle.
+// The tile is 128 x BN (BN = 256 or 128) with 128 bytes of K per pipeline
+// stage (64 bf16 or 32 fp32 elements).
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer (one lane): fills the shared-memory ring
+//   warp 1      TMEM allocator + MMA issuer (one lane)
+//   warps 2..5  epilogue: each warp drains the 32 TMEM lanes (tile rows) it
+//               may access, 32 columns at a time, and hands the values to
+//               Epi::tile.
+// The accumulator is double-buffered in TMEM (2 * BN columns), so the
+// epilogue of one tile overlaps the main loop of the next.  Tiles are handed
+// out statically (tile = blockIdx.x + i * gridDim.x) in a grouped raster
+// (group_m M-tiles share each sweep over the N-tiles) for L2 reuse.
+//
+// Every wait is bounded; on a timeout the kernel records FLCE_ETIMEOUT in the
+// status word, stops issuing work, waits (bounded) for work in flight and
+// frees its TMEM before returning.
+#pragma once
+
+#include "common.cuh"
+
+namespace flce {
+
+constexpr int kBM = 128;
+constexpr int kGemmThreads = 192;
+
+template <typename T>
+struct MmaTraits;
+template <>
+struct MmaTraits<__nv_bfloat16> {
+  static constexpr uint32_t kFormat = 1;  // bf16 in kind::f16
+  static constexpr int kUmmaK = 16;
+  __device__ static void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t i, uint32_t acc) {
+    mma_f16(d, a, b, i, acc);
+  }
+};
+template <>
+struct MmaTraits<float> {
+  static constexpr uint32_t kFormat = 2;  // tf32 in kind::tf32
+  static constexpr int kUmmaK = 8;
+  __device__ static void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t i, uint32_t acc) {
+    mma_tf32(d, a, b, i, acc);
+  }
+};
+
+template <typename T, int BN>
+struct GemmGeo {
+  static constexpr int kEK = 128 / static_cast<int>(sizeof(T));  // K elements per stage
+  static constexpr int kStageA = kBM * 128;
+  static constexpr int kStageB = BN * 128;
+  static constexpr int kStageBytes = kStageA + kStageB;
+  static constexpr int kStages = (BN == 256) ? 4 : 6;
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + 1024-byte alignment slack
+  static constexpr int kMmaPerStage = 128 / (MmaTraits<T>::kUmmaK * static_cast<int>(sizeof(T)));
+};
+
+struct GemmArgs {
+  int M, N, K;     // problem size (elements)
+  int nMt, nNt, nK;
+  int group_m;
+  int32_t* status;
+};
+
+__device__ __forceinline__ void tile_coords(int t, int nMt, int nNt, int group_m, int& mt,
+                                            int& nt) {
+  const int per_group = group_m * nNt;
+  const int g = t / per_group;
+  const int first = g * group_m;
+  const int gsize = min(group_m, nMt - first);
+  const int r = t - g * per_group;
+  nt = r / gsize;
+  mt = first + (r - nt * gsize);
+}
+
+// Loads one operand's share of a stage: `rows` rows starting at row0, K block kb.
+template <typename T, bool MN>
+__device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
+                                             int rows, int row0, int kb) {
+  constexpr int EK = 128 / static_cast<int>(sizeof(T));
+  if (!MN) {
+    // K-major: one box {EK (K), rows}
+    tma_load_2d(dst, map, bar, kb * EK, row0);
+  } else {
+    // MN-major: rows/EK slabs, each a box {EK (MN), EK (K rows)} of EK*128 bytes
+    for (int s = 0; s < rows / EK; ++s)
+      tma_load_2d(dst + s * EK * 128, map, bar, row0 + s * EK, kb * EK);
+  }
+}
+
+// Descriptor of the k-th MMA of a stage for one operand.
+template <typename T, bool MN>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int k) {
+  constexpr int EK = 128 / static_cast<int>(sizeof(T));
+  constexpr int UK = MmaTraits<T>::kUmmaK;
+  if (!MN) {
+    // K-major SW128: rows of 128 B, 8-row atoms 1024 B apart; step 32 B along K.
+    return smem_desc_sw128(base + k * UK * static_cast<int>(sizeof(T)), 16, 1024);
+  } else {
+    // MN-major SW128: slabs of EK MN-elements x EK K-rows (EK*128 B apart, the
+    // leading byte offset); 8-row K groups 1024 B apart (stride byte offset).
+    return smem_desc_sw128(base + k * UK * 128, EK * 128, 1024);
+  }
+}
+
+template <typename T, int BN, bool A_MN, bool B_MN, class Epi>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmArgs ga, const typename Epi::Params ep) {
+  using G = GemmGeo<T, BN>;
+  constexpr int S = G::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full_bar[S], empty_bar[S], accf_bar[2], acce_bar[2], drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile int* abort_flag = &abort_sh;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&accf_bar[i], 1);
+      mbar_init(&acce_bar[i], 4);
+    }
+    mbar_init(&drain_bar, 1);
+    abort_sh = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, G::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_sh;
+  const int num_tiles = ga.nMt * ga.nNt;
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    set_status(ga.status, FLCE_ETIMEOUT);
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      uint32_t stage = 0, phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        int mt, nt;
+        tile_coords(t, ga.nMt, ga.nNt, ga.group_m, mt, nt);
+        for (int kb = 0; kb < ga.nK; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * G::kStageBytes;
+          mbar_arrive_expect_tx(&full_bar[stage], G::kStageBytes);
+          load_operand<T, A_MN>(sa, &tmA, &full_bar[stage], kBM, mt * kBM, kb);
+          load_operand<T, B_MN>(sa + G::kStageA, &tmB, &full_bar[stage], BN, nt * BN, kb);
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        fail();
+        // let the copies already in flight land before the CTA exits
+        for (int i = 0; i < S && i < issued; ++i) {
+          if (stage == 0) {
+            stage = S;
+            phase ^= 1u;
+          }
+          --stage;
+          const uint64_t t0 = global_ns();
+          while (!mbar_try_wait(smem_u32(&full_bar[stage]), phase) &&
+                 global_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ----------------------------------------------------------------- MMA
+      constexpr uint32_t idesc = make_idesc(MmaTraits<T>::kFormat, kBM, BN, A_MN, B_MN);
+      uint32_t stage = 0, phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
+        const int buf = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!mbar_wait(&acce_bar[buf], acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+        for (int kb = 0; kb < ga.nK; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * G::kStageBytes);
+          const uint32_t sb = sa + G::kStageA;
+#pragma unroll
+          for (int k = 0; k < G::kMmaPerStage; ++k) {
+            MmaTraits<T>::mma(d_tmem, operand_desc<T, A_MN>(sa, k), operand_desc<T, B_MN>(sb, k),
+                              idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit(&empty_bar[stage]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&accf_bar[buf]);
+      }
+      if (!ok) fail();
+      // wait (bounded) until every MMA issued above has finished
+      mma_commit(&drain_bar);
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(smem_u32(&drain_bar), 0) && global_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int quad = warp & 3;  // TMEM lanes this warp may access: 32*quad .. +31
+    const int row_in_tile = quad * 32 + lane;
+    int local = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
+      const int buf = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&accf_bar[buf], acc_phase, abort_flag) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) fail();
+        break;
+      }
+      tc_fence_after();
+      int mt, nt;
+      tile_coords(t, ga.nMt, ga.nNt, ga.group_m, mt, nt);
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(buf * BN);
+      Epi::template tile<BN>(ep, mt, nt, row_in_tile, taddr);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce_bar[buf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, G::kTmemCols);
+  }
+}
+
+}  // namespace flce

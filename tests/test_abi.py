@@ -1,0 +1,169 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library loads, exports every function the headers declare, and rejects
+bad arguments with the documented status codes before touching the device.
+Only argument combinations that fail host validation are passed here, and the
+validation tests are skipped on a machine with a GPU so that no call with a
+stand-in pointer can ever reach a kernel.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in ("flce.h", "flce_gemm.h")]
+
+
+def _declared():
+    names = []
+    for h in HEADERS:
+        src = open(h).read()
+        names += re.findall(r"FLCE_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from lm_head_linear_fwd_gb300 import build
+    build.build()
+    from lm_head_linear_fwd_gb300 import _abi
+    return _abi.load()
+
+
+def test_headers_declare_the_boundary():
+    names = set(_declared())
+    for n in ("ce_logits_fwd", "ce_logits_bwd", "ce_logits_workspace_bytes", "flce_fwd",
+              "flce_bwd", "flce_workspace_bytes", "flce_default_chunk", "flce_status_string",
+              "flce_gemm"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    from lm_head_linear_fwd_gb300 import _abi
+    assert set(_abi.EXPORTED) == set(_declared())
+
+
+def test_status_strings(lib):
+    from lm_head_linear_fwd_gb300 import _abi
+    for code in range(0, -10, -1):
+        assert _abi.status_string(code).startswith("FLCE")
+
+
+def test_workspace_sizes(lib):
+    from lm_head_linear_fwd_gb300 import _abi
+    assert _abi.ce_logits_workspace_bytes(0, 10) == 0
+    assert _abi.ce_logits_workspace_bytes(16384, 128256) >= 16384 * 4
+    n = _abi.flce_workspace_bytes(0, 8192, 4096, 128256, 0)
+    chunk = _abi.flce_default_chunk(0, 8192, 4096, 128256)
+    assert chunk % 128 == 0 and 128 <= chunk <= 8192
+    # the dZ chunk buffer (bf16) is at most half of a [chunk, V] fp32 tile,
+    # plus a per-row-and-vocab-tile partial buffer of the forward
+    assert n >= chunk * 128256 * 2
+    assert n <= chunk * 128256 * 4 + 2 * 8192 * ((128256 + 255) // 256) * 4 + (1 << 22)
+    assert _abi.flce_workspace_bytes(7, 8, 8, 8, 0) == 0  # bad dtype
+
+
+no_gpu = pytest.mark.skipif(torch.cuda.is_available(),
+                            reason="host-validation tests use stand-in pointers; CPU only")
+FAKE = 0x10000  # never dereferenced: every call below fails host validation first
+
+
+@no_gpu
+def test_ce_fwd_rejects_bad_arguments(lib):
+    from lm_head_linear_fwd_gb300 import _abi
+    args = dict(logits=FAKE, dt=0, N=4, V=10, ld=10, labels=FAKE, ig=-100, red=0, nlt=-1,
+                loss=FAKE, nv=FAKE, lse=FAKE, rows=None, zl=None, ws=FAKE, wsb=1024,
+                status=FAKE, stream=None)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return _abi.ce_logits_fwd(*a.values())
+    assert call(dt=5) == -3
+    assert call(red=7) == -1
+    assert call(V=0) == -2
+    assert call(ld=9) == -2
+    assert call(N=-1) == -2
+    assert call(labels=None) == -1
+    assert call(status=None) == -1
+    assert call(ws=None) == -6
+    assert call(wsb=8) == -6
+    assert call(logits=FAKE + 1) == -4
+
+
+@no_gpu
+def test_ce_bwd_rejects_bad_arguments(lib):
+    from lm_head_linear_fwd_gb300 import _abi
+    base = [FAKE, 0, 4, 10, 10, FAKE, -100, 0, -1, FAKE, FAKE, FAKE, 1, FAKE, 10, FAKE, None]
+
+    def call(i, v):
+        a = list(base)
+        a[i] = v
+        return _abi.ce_logits_bwd(*a)
+    assert call(12, 2) == -1            # inplace flag not 0/1
+    assert call(13, FAKE + 4096) == -1  # in place but grad pointer differs
+    assert call(14, 12) == -1           # in place but row strides differ
+    assert call(9, None) == -1          # lse missing
+    assert call(1, 3) == -3
+
+
+@no_gpu
+def test_flce_rejects_bad_arguments(lib):
+    from lm_head_linear_fwd_gb300 import _abi
+    base = [FAKE, FAKE, None, 0, 256, 128, 1000, FAKE, -100, 0, -1, FAKE, FAKE, FAKE, None, None,
+            FAKE, 1 << 30, FAKE, None]
+
+    def call(i, v):
+        a = list(base)
+        a[i] = v
+        return _abi.flce_fwd(*a)
+    assert call(5, 4) == -2          # D < 8
+    assert call(5, 100) == -4        # D*2 not a multiple of 16
+    assert call(0, FAKE + 2) == -4   # H not 16-byte aligned
+    assert call(3, 9) == -3
+    assert call(17, 16) == -6        # workspace too small
+    assert call(2, FAKE + 1) == -4   # bias misaligned
+    bb = [FAKE, FAKE, None, 0, 256, 128, 1000, FAKE, -100, 0, -1, FAKE, FAKE, FAKE, 100, FAKE,
+          FAKE, 0, None, FAKE, 1 << 30, FAKE, None]
+    b2 = list(bb)
+    b2[14] = 100                     # chunk not a multiple of 128 (and < N)
+    assert _abi.flce_bwd(*b2) == -2
+    b3 = list(bb)
+    b3[17] = 2
+    assert _abi.flce_bwd(*b3) == -1
+
+
+@no_gpu
+def test_gemm_rejects_bad_arguments(lib):
+    from lm_head_linear_fwd_gb300 import _abi
+    base = [0, 0, 0, 64, 64, 64, FAKE, 64, FAKE, 64, FAKE, 64, 0, FAKE, None]
+
+    def call(i, v):
+        a = list(base)
+        a[i] = v
+        return _abi.flce_gemm(*a)
+    assert call(7, 60) == -4   # lda*2 not a multiple of 16
+    assert call(7, 32) == -2   # lda < K
+    assert call(1, 3) == -1
+    assert call(3, 0) == -2
+    assert call(0, 2) == -3
+
+
+def test_product_path_has_no_fallback():
+    """The package never imports the oracle, and a missing library raises."""
+    import subprocess
+    import sys
+    pkg = os.path.join(ROOT, "lm_head_linear_fwd_gb300")
+    for f in os.listdir(pkg):
+        if f.endswith(".py"):
+            src = open(os.path.join(pkg, f)).read()
+            assert "import oracle" not in src and "from oracle" not in src, f
+    code = ("import lm_head_linear_fwd_gb300._abi as a\na._lib = None\n"
+            "try:\n    a.load('/nonexistent/libflce.so')\nexcept ImportError:\n    print('raised')\n")
+    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True)
+    assert "raised" in out.stdout
+    ctypes  # noqa: B018  (ctypes import kept for symbol lookups above)

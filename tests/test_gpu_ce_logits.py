@@ -1,0 +1,217 @@
+"""Cross-entropy on given logits: CUDA path through the C ABI vs the fp64 oracle.
+
+Tolerances (the loss and gradient bars of the hot-path specification, plus
+what the arithmetic gives):
+* loss: |gpu - ref| <= 1e-3 |ref| (fp32 per-row lse, fp64 reduction; the
+  observed error is far smaller);
+* per-row lse: |gpu - ref| <= 5e-5 (1 + |ref|): fp32 sums of up to 1.3e5
+  terms, each from ex2.approx (relative error ~2^-22);
+* n_valid and the gathered label logit: exact;
+* dlogits (bf16 output): max relative <= 2e-2 and normwise <= 5e-3 (one bf16
+  rounding, 2^-9 relative, per element).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lh():
+    import lm_head_linear_fwd_gb300 as m
+    return m
+
+
+def _dev(p):
+    return p.logits.cuda(), p.labels.cuda()
+
+
+def _check_fwd(out, ref, rows=None):
+    torch.cuda.synchronize()
+    lse = out.lse.cpu().double().numpy()
+    want = ref["lse"]
+    if rows is not None:
+        lse = lse[rows]
+    assert np.all(np.abs(lse - want) <= 5e-5 * (1 + np.abs(want))), np.max(np.abs(lse - want))
+
+
+def _check_grad(got, want):
+    assert oracle.max_rel_err(got.float().cpu(), want) <= 2e-2
+    assert oracle.normwise_err(got.float().cpu(), want) <= 5e-3
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("reduction,nlt", [("sum", None), ("mean", None), ("sum", 1000)])
+@pytest.mark.parametrize("N,V,ld", [(300, 1000, 1000), (77, 1003, 1011), (5, 32777, 32777),
+                                    (130, 4099, 4099)])
+def test_ce_parity(lh, dtype, reduction, nlt, N, V, ld):
+    p = wl.random_ce(N, V, dtype, seed=N + V, reduction=reduction, num_label_tokens=nlt, ld=ld)
+    logits, labels = _dev(p)
+    out = lh.ce_logits_fwd(logits, labels, -100, reduction, nlt, want_rows=True,
+                           want_label_logit=True)
+    ref = oracle.ce_forward(p.logits, p.labels, -100, reduction, nlt)
+    _check_fwd(out, ref)
+    assert int(out.n_valid.item()) == ref["n_valid"]
+    assert abs(out.loss.item() - ref["loss"]) <= 1e-3 * abs(ref["loss"])
+    zl = out.label_logit.cpu().double().numpy()
+    valid = p.labels.numpy() != -100
+    assert np.array_equal(zl[valid], ref["label_logit"][valid])  # exact widening
+    assert np.all(np.isnan(zl[~valid]))
+    g = torch.tensor([0.7], device="cuda")
+    grad = lh.ce_logits_bwd(logits, labels, out.lse, out.n_valid, g, -100, reduction, nlt)
+    torch.cuda.synchronize()
+    lh.check_status(out.status)
+    _check_grad(grad, oracle.ce_backward(p.logits, p.labels, -100, reduction, nlt, grad_loss=0.7))
+
+
+def test_inplace_grad_aliases_logits(lh):
+    p = wl.random_ce(64, 5000, torch.bfloat16, seed=3)
+    logits, labels = _dev(p)
+    logits = logits.contiguous().requires_grad_(True)
+    ptr = logits.data_ptr()
+    loss = lh.ce_logits(logits, labels, inplace_grad=True)
+    loss.backward()
+    torch.cuda.synchronize()
+    assert logits.grad.data_ptr() == ptr
+    _check_grad(logits.grad, oracle.ce_backward(p.logits, p.labels))
+    # the logits storage now holds the gradient
+    assert torch.equal(logits.detach(), logits.grad)
+
+
+def test_default_does_not_mutate_logits(lh):
+    p = wl.random_ce(32, 3000, torch.bfloat16, seed=4)
+    logits = p.logits.cuda().contiguous().requires_grad_(True)
+    before = logits.detach().clone()
+    lh.ce_logits(logits, p.labels.cuda()).backward()
+    torch.cuda.synchronize()
+    assert torch.equal(logits.detach(), before)
+    assert logits.grad.data_ptr() != logits.data_ptr()
+
+
+def test_second_inplace_backward_raises(lh):
+    p = wl.random_ce(8, 300, torch.bfloat16, seed=5)
+    logits = p.logits.cuda().contiguous().requires_grad_(True)
+    loss = lh.ce_logits(logits, p.labels.cuda(), inplace_grad=True)
+    loss.backward(retain_graph=True)
+    with pytest.raises(RuntimeError):
+        loss.backward()
+
+
+def test_double_backward_raises(lh):
+    p = wl.random_ce(8, 300, torch.float32, seed=6)
+    logits = p.logits.cuda().contiguous().requires_grad_(True)
+    loss = lh.ce_logits(logits, p.labels.cuda())
+    (g,) = torch.autograd.grad(loss, logits, create_graph=True)
+    with pytest.raises(RuntimeError):
+        g.sum().backward()
+
+
+@pytest.mark.parametrize("reduction", ["sum", "mean"])
+def test_all_ignored(lh, reduction):
+    logits = torch.randn(16, 500, device="cuda").bfloat16()
+    labels = torch.full((16,), -100, dtype=torch.int64, device="cuda")
+    out = lh.ce_logits_fwd(logits, labels, -100, reduction)
+    grad = lh.ce_logits_bwd(logits, labels, out.lse, out.n_valid, torch.ones(1, device="cuda"),
+                            -100, reduction)
+    torch.cuda.synchronize()
+    assert out.loss.item() == 0.0 and out.n_valid.item() == 0
+    assert torch.count_nonzero(grad).item() == 0
+
+
+def test_zero_num_label_tokens(lh):
+    p = wl.random_ce(16, 700, torch.bfloat16, seed=8)
+    logits, labels = _dev(p)
+    out = lh.ce_logits_fwd(logits, labels, -100, "sum", 0)
+    grad = lh.ce_logits_bwd(logits, labels, out.lse, out.n_valid, torch.ones(1, device="cuda"),
+                            -100, "sum", 0)
+    torch.cuda.synchronize()
+    assert out.loss.item() == 0.0 and out.n_valid.item() == int((p.labels != -100).sum())
+    assert torch.count_nonzero(grad).item() == 0
+
+
+def test_bad_label_sets_status_and_row_is_ignored(lh):
+    p = wl.random_ce(20, 600, torch.bfloat16, seed=9, ignore_frac=0.0)
+    logits, labels = _dev(p)
+    labels[3] = 600  # out of range
+    labels[7] = -5
+    out = lh.ce_logits_fwd(logits, labels, -100, "mean")
+    grad = lh.ce_logits_bwd(logits, labels, out.lse, out.n_valid, torch.ones(1, device="cuda"),
+                            -100, "mean")
+    torch.cuda.synchronize()
+    assert int(out.status.item()) == -5
+    with pytest.raises(lh.FlceError):
+        lh.check_status(out.status)
+    ref_labels = p.labels.clone()
+    ref_labels[3] = -100
+    ref_labels[7] = -100
+    ref = oracle.ce_forward(p.logits, ref_labels, -100, "mean")
+    assert out.n_valid.item() == ref["n_valid"] == 18
+    assert abs(out.loss.item() - ref["loss"]) <= 1e-3 * ref["loss"]
+    _check_grad(grad, oracle.ce_backward(p.logits, ref_labels, -100, "mean"))
+
+
+def test_ignore_index_inside_vocab(lh):
+    p = wl.random_ce(40, 900, torch.bfloat16, seed=10, ignore_frac=0.0)
+    logits, labels = _dev(p)
+    out = lh.ce_logits_fwd(logits, labels, 5, "sum")
+    torch.cuda.synchronize()
+    ref = oracle.ce_forward(p.logits, p.labels, 5, "sum")
+    assert out.n_valid.item() == ref["n_valid"]
+    assert abs(out.loss.item() - ref["loss"]) <= 1e-3 * ref["loss"]
+
+
+def test_label_in_last_column(lh):
+    p = wl.random_ce(9, 1001, torch.bfloat16, seed=13, ignore_frac=0.0)
+    logits, labels = _dev(p)
+    labels[:] = 1000
+    out = lh.ce_logits_fwd(logits, labels, -100, "sum", want_label_logit=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out.label_logit.cpu(), p.logits[:, 1000].float())
+
+
+def test_empty_batch(lh):
+    logits = torch.empty(0, 128, device="cuda").bfloat16()
+    labels = torch.empty(0, dtype=torch.int64, device="cuda")
+    out = lh.ce_logits_fwd(logits, labels)
+    torch.cuda.synchronize()
+    assert out.loss.item() == 0.0 and out.n_valid.item() == 0
+
+
+def test_deterministic(lh):
+    p = wl.random_ce(256, 20000, torch.bfloat16, seed=14)
+    logits, labels = _dev(p)
+    a = lh.ce_logits_fwd(logits, labels, want_rows=True)
+    b = lh.ce_logits_fwd(logits, labels, want_rows=True)
+    ga = lh.ce_logits_bwd(logits, labels, a.lse, a.n_valid, torch.ones(1, device="cuda"))
+    gb = lh.ce_logits_bwd(logits, labels, b.lse, b.n_valid, torch.ones(1, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.equal(a.loss, b.loss) and torch.equal(a.loss_rows, b.loss_rows)
+    assert torch.equal(ga, gb)
+
+
+def test_full_size_workload_sampled(lh):
+    """[16384, 128256] bf16, 5% ignored, sum, in place: the launch the benchmark
+    times.  Sampled rows are checked one by one against the oracle; the loss is
+    checked against the fp64 sum of the per-row losses (exact property)."""
+    p = wl.ce_logits_large(device="cuda")
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(p.N, 48, replace=False))
+    host_rows = p.logits[rows].cpu()
+    host_labels = p.labels[rows].cpu()
+    out = lh.ce_logits_fwd(p.logits, p.labels, -100, "sum", want_rows=True)
+    g = torch.ones(1, device="cuda")
+    lh.ce_logits_bwd(p.logits, p.labels, out.lse, out.n_valid, g, inplace_grad=True)
+    torch.cuda.synchronize()
+    lh.check_status(out.status)
+    ref = oracle.ce_forward(host_rows, host_labels)
+    _check_fwd(out, ref, rows)
+    lr = out.loss_rows.cpu().double().numpy()
+    assert np.allclose(lr[rows], ref["loss_rows"], atol=5e-5 * 20)
+    assert out.n_valid.item() == int((p.labels != -100).sum())
+    assert abs(out.loss.item() - lr.sum()) <= 1e-6 * abs(lr.sum())
+    dz = oracle.ce_backward(host_rows, host_labels)  # scale 1 (sum)
+    _check_grad(p.logits[rows].cpu(), dz)

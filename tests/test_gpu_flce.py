@@ -1,0 +1,235 @@
+"""Fused linear cross-entropy: CUDA path through the C ABI vs the fp64 oracle.
+
+Tolerances:
+* loss: |gpu - ref| <= 1e-3 |ref|;
+* per-row lse: |gpu - ref| <= 2e-3 (1 + |ref|) for bf16 inputs (the logits are
+  fp32 accumulations of D products of bf16 values, exact products, so the lse
+  error is the fp32 accumulation error, ~1e-5 here; the bound leaves room)
+  and the same for tf32 (fp32 inputs rounded to 10 mantissa bits:
+  |z| * 2^-11 ~ 1e-4 at |z| ~ 0.3);
+* n_valid exact;
+* grad_H, grad_W, grad_b: max relative <= 2e-2, normwise <= 5e-3 (dZ is rounded
+  to the input dtype before the two gradient contractions).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lh():
+    import lm_head_linear_fwd_gb300 as m
+    return m
+
+
+def _to(p):
+    b = p.bias.cuda() if p.bias is not None else None
+    return p.H.cuda(), p.W.cuda(), b, p.labels.cuda()
+
+
+def _grad_ok(got, want, name):
+    mr = oracle.max_rel_err(got.float().cpu(), want)
+    nw = oracle.normwise_err(got.float().cpu(), want)
+    assert mr <= 2e-2 and nw <= 5e-3, (name, mr, nw)
+
+
+def _run(lh, p, chunk=None, g=1.0, accumulate_init=None):
+    H, W, b, y = _to(p)
+    out = lh.flce_fwd(H, W, y, b, -100, p.reduction, p.num_label_tokens, want_rows=True,
+                      want_label_logit=True)
+    gw = None
+    if accumulate_init is not None:
+        gw = accumulate_init.cuda().clone()
+    bw = lh.flce_bwd(H, W, y, out.lse, out.n_valid, torch.tensor([g], device="cuda"), b, -100,
+                     p.reduction, p.num_label_tokens, chunk, grad_W=gw,
+                     accumulate_grad_W=accumulate_init is not None, status=out.status)
+    torch.cuda.synchronize()
+    lh.check_status(out.status)
+    return out, bw
+
+
+def _check_all(p, out, bw, g=1.0, grad_W_init=None, W64=None):
+    W = p.W if W64 is None else W64
+    ref = oracle.flce_forward(p.H, W, p.bias, p.labels, -100, p.reduction, p.num_label_tokens)
+    assert int(out.n_valid.item()) == ref["n_valid"]
+    assert abs(out.loss.item() - ref["loss"]) <= 1e-3 * abs(ref["loss"]), (out.loss.item(), ref["loss"])
+    lse = out.lse.cpu().double().numpy()
+    assert np.max(np.abs(lse - ref["lse"]) / (1 + np.abs(ref["lse"]))) <= 2e-3
+    gr = oracle.flce_backward(p.H, W, p.bias, p.labels, -100, p.reduction, p.num_label_tokens,
+                              grad_loss=g, grad_W_init=grad_W_init)
+    _grad_ok(bw.grad_H, gr["grad_H"], "grad_H")
+    _grad_ok(bw.grad_W, gr["grad_W"], "grad_W")
+    if p.bias is not None:
+        _grad_ok(bw.grad_bias, gr["grad_b"], "grad_b")
+
+
+@pytest.mark.parametrize("reduction", ["sum", "mean"])
+def test_tiny_fp32_workload(lh, reduction):
+    """N=256, D=128, V=1000, fp32 (tf32 tensor cores), 10% ignored."""
+    p = wl.tiny_flce(reduction)
+    out, bw = _run(lh, p, g=1.5)
+    _check_all(p, out, bw, g=1.5)
+
+
+def test_small_model_workload(lh):
+    """B=2, T=1024, D=768, V=32777 (odd), bf16 with bias, mean."""
+    p = wl.small_flce()
+    out, bw = _run(lh, p)
+    _check_all(p, out, bw)
+
+
+@pytest.mark.parametrize("N,D,V,chunk,bias", [(700, 256, 3001, 256, True), (129, 64, 777, 128, False),
+                                              (1000, 520, 2048, None, False)])
+def test_ragged_multi_chunk(lh, N, D, V, chunk, bias):
+    p = wl.random_flce(N, D, V, torch.bfloat16, bias=bias, seed=N, reduction="mean")
+    out, bw = _run(lh, p, chunk=chunk, g=0.5)
+    _check_all(p, out, bw, g=0.5)
+
+
+def test_fp32_multi_chunk_with_bias(lh):
+    p = wl.random_flce(300, 96, 1234, torch.float32, bias=True, seed=31, reduction="sum",
+                       num_label_tokens=250)
+    out, bw = _run(lh, p, chunk=128)
+    _check_all(p, out, bw)
+
+
+def test_accumulate_grad_W(lh):
+    p = wl.random_flce(256, 128, 1000, torch.bfloat16, seed=41)
+    init = torch.randn(1000, 128) * 0.01
+    out, bw = _run(lh, p, accumulate_init=init)
+    _check_all(p, out, bw, grad_W_init=init.double().numpy())
+
+
+def test_label_logit_and_rows(lh):
+    p = wl.random_flce(200, 64, 1000, torch.bfloat16, seed=51)
+    p.labels[:5] = 999   # label in the last (partial) vocabulary tile
+    p.labels[5:9] = 0
+    out, _ = _run(lh, p)
+    ref = oracle.flce_forward(p.H, p.W, p.bias, p.labels, -100, "sum")
+    zl = out.label_logit.cpu().double().numpy()
+    v = p.labels.numpy() != -100
+    assert np.max(np.abs(zl[v] - ref["label_logit"][v])) <= 2e-3
+    assert np.all(np.isnan(zl[~v]))
+    lr = out.loss_rows.cpu().double().numpy()
+    assert np.all(lr[~v] == 0) and np.all(lr >= -1e-4)
+
+
+@pytest.mark.parametrize("reduction,nlt", [("mean", None), ("sum", 0)])
+def test_zero_guards(lh, reduction, nlt):
+    p = wl.random_flce(150, 64, 500, torch.bfloat16, bias=True, seed=61, reduction=reduction,
+                       num_label_tokens=nlt)
+    if nlt is None:
+        p.labels[:] = -100
+    out, bw = _run(lh, p)
+    assert out.loss.item() == 0.0
+    for t in (bw.grad_H, bw.grad_W, bw.grad_bias):
+        assert torch.count_nonzero(t).item() == 0
+
+
+def test_bad_label_status(lh):
+    p = wl.random_flce(64, 64, 300, torch.bfloat16, seed=71, ignore_frac=0.0)
+    H, W, b, y = _to(p)
+    y[10] = 300
+    out = lh.flce_fwd(H, W, y, b)
+    torch.cuda.synchronize()
+    assert int(out.status.item()) == -5
+    assert out.n_valid.item() == 63
+
+
+def test_autograd_module(lh):
+    p = wl.random_flce(300, 128, 2000, torch.bfloat16, bias=True, seed=81, reduction="mean")
+    H, W, b, y = _to(p)
+    for t in (H, W, b):
+        t.requires_grad_(True)
+    loss = lh.flce(H, W, y, b, reduction="mean", chunk=128)
+    loss.backward()
+    torch.cuda.synchronize()
+    gr = oracle.flce_backward(p.H, p.W, p.bias, p.labels, -100, "mean")
+    _grad_ok(H.grad, gr["grad_H"], "grad_H")
+    _grad_ok(W.grad, gr["grad_W"], "grad_W")
+    _grad_ok(b.grad, gr["grad_b"], "grad_b")
+    with pytest.raises(RuntimeError):
+        (gH,) = torch.autograd.grad(lh.flce(H, W, y, b), H, create_graph=True)
+        gH.sum().backward()
+
+
+def test_mask_argument(lh):
+    p = wl.random_flce(128, 64, 400, torch.bfloat16, seed=91, ignore_frac=0.0)
+    H, W, b, y = _to(p)
+    mask = torch.ones(128, dtype=torch.int64, device="cuda")
+    mask[::3] = 0
+    loss = lh.flce(H, W, y, None, mask=mask, reduction="sum")
+    labels = p.labels.clone()
+    labels[::3] = -100
+    ref = oracle.flce_forward(p.H, p.W, None, labels, -100, "sum")
+    assert abs(loss.item() - ref["loss"]) <= 1e-3 * ref["loss"]
+
+
+def test_deterministic(lh):
+    p = wl.random_flce(600, 256, 5000, torch.bfloat16, bias=True, seed=101)
+    o1, b1 = _run(lh, p, chunk=256)
+    o2, b2 = _run(lh, p, chunk=256)
+    assert torch.equal(o1.loss, o2.loss) and torch.equal(o1.lse, o2.lse)
+    for a, c in ((b1.grad_H, b2.grad_H), (b1.grad_W, b2.grad_W), (b1.grad_bias, b2.grad_bias)):
+        assert torch.equal(a, c)
+
+
+def _sampled_full_size(lh, p, n_rows=32, sub_rows=256):
+    """Full-size run (the benchmark's launches) checked on sampled rows and by the
+    row-linearity of grad_W; the complete gradients are then checked on a
+    row subset run as its own problem."""
+    H, W, b, y = _to(p)
+    out = lh.flce_fwd(H, W, y, b, -100, p.reduction, p.num_label_tokens, want_rows=True)
+    one = torch.ones(1, device="cuda")
+    bw = lh.flce_bwd(H, W, y, out.lse, out.n_valid, one, b, -100, p.reduction,
+                     p.num_label_tokens)
+    torch.cuda.synchronize()
+    lh.check_status(out.status)
+    nv = int((p.labels != -100).sum())
+    assert out.n_valid.item() == nv
+    rng = np.random.default_rng(1)
+    rows = np.sort(rng.choice(p.N, n_rows, replace=False))
+    Hc, yc = p.H.cpu(), p.labels.cpu()
+    W64 = p.W.cpu().double().numpy()  # widened once, reused by every oracle call
+    ref = oracle.flce_forward(Hc, W64, None, yc, -100, p.reduction, p.num_label_tokens, rows=rows)
+    lse = out.lse.cpu().double().numpy()[rows]
+    assert np.max(np.abs(lse - ref["lse"]) / (1 + np.abs(ref["lse"]))) <= 2e-3
+    lr = out.loss_rows.cpu().double().numpy()
+    assert np.max(np.abs(lr[rows] - ref["loss_rows"])) <= 2e-3 * (1 + np.max(ref["loss_rows"]))
+    total = lr.sum() / (p.num_label_tokens if p.num_label_tokens else 1)
+    assert abs(out.loss.item() - total) <= 1e-5 * abs(total)
+    gr = oracle.flce_backward(Hc, W64, None, yc, -100, p.reduction, p.num_label_tokens, rows=rows,
+                              n_valid_total=nv, want_grad_W=False)
+    _grad_ok(bw.grad_H[torch.as_tensor(rows, device="cuda")], gr["grad_H"], "grad_H rows")
+    # grad_W is linear in the rows: a full run equals two half runs accumulated
+    half = (p.N // 2) // 128 * 128
+    gW2 = torch.zeros_like(bw.grad_W)
+    for r0, r1, acc in ((0, half, False), (half, p.N, True)):
+        lh.flce_bwd(H[r0:r1], W, y[r0:r1], out.lse[r0:r1], out.n_valid, one, None, -100,
+                    p.reduction, p.num_label_tokens, want_grad_H=False, grad_W=gW2,
+                    accumulate_grad_W=acc)
+    torch.cuda.synchronize()
+    assert oracle.normwise_err(gW2.cpu(), bw.grad_W.cpu().double().numpy()) <= 1e-5
+    # complete gradients of a row subset, as a problem of its own
+    sub = torch.as_tensor(np.sort(rng.choice(p.N, sub_rows, replace=False)))
+    q = wl.FLCEInputs("subset", Hc[sub].contiguous(), p.W, None, yc[sub].contiguous(), -100,
+                      p.reduction, None)
+    out_s, bw_s = _run(lh, q)
+    _check_all(q, out_s, bw_s, W64=W64)
+
+
+def test_llama3_8b_workload_sampled(lh):
+    """N=8192, D=4096, V=128256 bf16, Zipf labels, 3% ignored, sum / num_label_tokens."""
+    p = wl.llama3_8b_flce(device="cuda")
+    _sampled_full_size(lh, p)
+
+
+def test_long_packed_workload_sampled(lh):
+    """N=65536 (4 x 16384 packed), D=5120, V=151936 bf16, ~8% ignored, sum."""
+    p = wl.long_packed_flce(device="cuda")
+    _sampled_full_size(lh, p, n_rows=16, sub_rows=128)
