@@ -3,7 +3,7 @@ and fused linear cross-entropy, as hand-written CUDA kernels behind a C ABI
 (``include/flce.h``), with a thin PyTorch binding.
 
 Importing the package loads ``_lib/libflce.so``; it raises if the library has
-not been built (``python -m lm_head_linear_fwd_gb300.build``).
+not been built (``python lm_head_linear_fwd_gb300/build.py``).
 """
 from . import _abi
 

@@ -9,9 +9,10 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "_lib", "libflce.so")
+LIB_PATH = os.path.join(_PKG, "_lib", platform.machine(), "libflce.so")
 
 FLCE_OK = 0
 FLCE_ELABEL = -5
@@ -55,7 +56,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     if not os.path.exists(path):
         raise ImportError(
             f"libflce.so not found at {path}: build it with "
-            "`python -m lm_head_linear_fwd_gb300.build` (needs nvcc)")
+            "`python lm_head_linear_fwd_gb300/build.py` (needs nvcc)")
     lib = ctypes.CDLL(path)
     for name, (res, args) in _SIGNATURES.items():
         fn = getattr(lib, name)

@@ -1,13 +1,14 @@
 """Builds the loss-head shared library (libflce.so) in-tree with nvcc for sm_103a.
 
 Each translation unit is compiled in parallel, then linked into
-``lm_head_linear_fwd_gb300/_lib/libflce.so`` (static CUDA runtime, no torch
-dependency).  ``python -m lm_head_linear_fwd_gb300.build`` runs it.
+``lm_head_linear_fwd_gb300/_lib/<machine>/libflce.so`` (static CUDA runtime, no torch
+dependency).  ``python lm_head_linear_fwd_gb300/build.py`` runs it.
 """
 from __future__ import annotations
 
 import concurrent.futures
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -15,7 +16,8 @@ import sys
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
-LIBDIR = os.path.join(PKG, "_lib")
+# per machine architecture, so that objects built on one host are never linked on another
+LIBDIR = os.path.join(PKG, "_lib", platform.machine())
 LIB = os.path.join(LIBDIR, "libflce.so")
 SOURCES = ["ce_logits.cu", "flce.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -27,8 +27,8 @@ def _declared():
 
 @pytest.fixture(scope="module")
 def lib():
-    from lm_head_linear_fwd_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     from lm_head_linear_fwd_gb300 import _abi
     return _abi.load()
 
