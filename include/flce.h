@@ -91,6 +91,10 @@ typedef enum { FLCE_SUM = 0, FLCE_MEAN = 1 } flce_reduction_t;
 /* Human-readable name of a status code (static storage; never NULL). */
 FLCE_API const char* flce_status_string(int status);
 
+/* Description of the last CUDA runtime/driver failure behind an FLCE_ECUDA
+ * returned on the calling thread (thread-local storage; never NULL). */
+FLCE_API const char* flce_last_cuda_error(void);
+
 /* ------------------------------------------------------------------------ */
 /* Cross-entropy on given logits                                            */
 /* ------------------------------------------------------------------------ */

@@ -13,6 +13,8 @@
  * A is K-major (a_mn_major = 0: row m at A + m*lda, K contiguous) or MN-major
  * (a_mn_major = 1: row k at A + k*lda, M contiguous); likewise B.  Inputs are
  * bf16 (FLCE_BF16, tcgen05 kind::f16) or fp32 (FLCE_F32, tcgen05 kind::tf32).
+ * The tf32 tensor-core path reads K-major operands only: FLCE_F32 with either
+ * operand MN-major returns FLCE_ENOSUP.
  * accumulate = 1 adds to the existing C (beta = 1), 0 overwrites it.
  *
  * All pointers are device pointers, 16-byte aligned; lda*sizeof(dt) and

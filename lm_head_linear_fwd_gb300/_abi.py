@@ -29,6 +29,7 @@ _p = ctypes.c_void_p
 
 _SIGNATURES = {
     "flce_status_string": (ctypes.c_char_p, [_i]),
+    "flce_last_cuda_error": (ctypes.c_char_p, []),
     "ce_logits_workspace_bytes": (_sz, [_i64, _i64]),
     "ce_logits_fwd": (_i, [_p, _i, _i64, _i64, _i64, _p, _i64, _i, _i64, _p, _p, _p, _p, _p,
                            _p, _sz, _p, _p]),
@@ -73,7 +74,10 @@ def status_string(code: int) -> str:
 class FlceError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = int(code)
-        super().__init__(f"{where}: {status_string(code)} ({code})")
+        msg = f"{where}: {status_string(code)} ({code})"
+        if self.code == -7:
+            msg += " [" + load().flce_last_cuda_error().decode() + "]"
+        super().__init__(msg)
 
 
 def check(rc: int, where: str) -> None:
@@ -89,6 +93,7 @@ def _call(name):
 
 
 flce_status_string = _call("flce_status_string")
+flce_last_cuda_error = _call("flce_last_cuda_error")
 ce_logits_workspace_bytes = _call("ce_logits_workspace_bytes")
 ce_logits_fwd = _call("ce_logits_fwd")
 ce_logits_bwd = _call("ce_logits_bwd")

@@ -16,6 +16,7 @@
 // maximum and sum in the base-2 domain (one MUFU ex2 per element plus one
 // rescale per 32 elements), and merge per-thread states with warp shuffles.
 #include <math.h>
+#include <stdio.h>
 
 #include <mutex>
 #include <vector>
@@ -150,7 +151,7 @@ int launch_finalize(const float* loss_rows, const int64_t* labels, int64_t N, in
                     int64_t* n_valid, cudaStream_t stream) {
   finalize_kernel<<<1, kFinThreads, 0, stream>>>(loss_rows, labels, N, V, ignore_index,
                                                  reduction, num_label_tokens, loss, n_valid);
-  return launch_status();
+  return launch_status("finalize_kernel launch");
 }
 
 // -------------------------------------------------------------- backward kernel
@@ -226,6 +227,13 @@ __global__ void __launch_bounds__(THREADS) ce_bwd_rows_kernel(
 
 // ------------------------------------------------------------------ host side
 
+static thread_local char g_last_error[256] = "no CUDA error recorded";
+
+void record_cuda_error(cudaError_t e, const char* where) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, cudaGetErrorString(e),
+           static_cast<int>(e));
+}
+
 static std::mutex g_sm_mutex;
 static std::vector<int> g_sm_counts;
 
@@ -261,6 +269,8 @@ extern "C" const char* flce_status_string(int status) {
     default: return "FLCE: unknown status";
   }
 }
+
+extern "C" const char* flce_last_cuda_error(void) { return g_last_error; }
 
 extern "C" size_t ce_logits_workspace_bytes(int64_t N, int64_t V) {
   (void)V;
@@ -310,7 +320,7 @@ extern "C" int ce_logits_fwd(const void* logits, int dt, int64_t N, int64_t V, i
                                                           V, ld, labels, ignore_index, lse,
                                                           rows, label_logit, status);
     }
-    rc = launch_status();
+    rc = launch_status("ce_fwd_rows_kernel launch");
     if (rc != FLCE_OK) return rc;
   }
   return launch_finalize(rows, labels, N, V, ignore_index, reduction, num_label_tokens, loss,
@@ -353,5 +363,5 @@ extern "C" int ce_logits_bwd(const void* logits, int dt, int64_t N, int64_t V, i
         static_cast<const float*>(logits), N, V, ld, labels, ignore_index, reduction,
         num_label_tokens, lse, n_valid, grad_loss, static_cast<float*>(grad_logits), ld_grad);
   }
-  return launch_status();
+  return launch_status("ce_bwd_rows_kernel launch");
 }

@@ -18,6 +18,9 @@
 //   3. grad_H[chunk] = dZ W                (A = dZ K-major, B = W MN-major);
 //   4. grad_W (+)= dZ^T H[chunk] in fp32   (A = dZ MN-major, B = H MN-major),
 //      the addmm with beta = 1 of the same page, chunk after chunk.
+// The tf32 tensor-core path (fp32 inputs) reads K-major operands only, so for
+// fp32 the MN-major operands of steps 3 and 4 are first transposed into the
+// workspace (W once per call, dZ and H[chunk] once per chunk).
 #include <math.h>
 
 #include <algorithm>
@@ -242,6 +245,34 @@ __global__ void __launch_bounds__(256) colsum_final_kernel(const float* __restri
   out[v] = acc;
 }
 
+// out[c, r] = in[r, c] for a [R, Cc] matrix of 4-byte elements (32 x 32 tiles
+// through shared memory; both sides coalesced).  The tf32 tensor-core path
+// takes only K-major operands, so the fp32 backward transposes its MN-major
+// operands with this kernel.
+__global__ void __launch_bounds__(256) transpose32_kernel(const float* __restrict__ in, int R,
+                                                          int Cc, int64_t ld_in,
+                                                          float* __restrict__ out,
+                                                          int64_t ld_out) {
+  __shared__ float tile[32][33];
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (int k = ty; k < 32; k += 8) {
+    const int r = r0 + k, c = c0 + tx;
+    if (r < R && c < Cc) tile[k][tx] = in[static_cast<int64_t>(r) * ld_in + c];
+  }
+  __syncthreads();
+  for (int k = ty; k < 32; k += 8) {
+    const int c = c0 + k, r = r0 + tx;
+    if (c < Cc && r < R) out[static_cast<int64_t>(c) * ld_out + r] = tile[tx][k];
+  }
+}
+
+static void transpose32(const float* in, int R, int Cc, int64_t ld_in, float* out,
+                        int64_t ld_out, cudaStream_t s) {
+  dim3 grid(static_cast<unsigned>((Cc + 31) / 32), static_cast<unsigned>((R + 31) / 32));
+  transpose32_kernel<<<grid, 256, 0, s>>>(in, R, Cc, ld_in, out, ld_out);
+}
+
 // --------------------------------------------------------------- host: TMA
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -268,7 +299,10 @@ static EncodeTiledFn encode_fn() {
 static int make_map(CUtensorMap* m, const void* base, int dt, uint64_t inner, uint64_t outer,
                     uint64_t row_stride_elems, uint32_t box_outer) {
   EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return FLCE_ECUDA;
+  if (fn == nullptr) {
+    record_cuda_error(cudaErrorUnknown, "cuTensorMapEncodeTiled entry point");
+    return FLCE_ECUDA;
+  }
   const uint64_t es = dtype_size(dt);
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {row_stride_elems * es};
@@ -279,7 +313,11 @@ static int make_map(CUtensorMap* m, const void* base, int dt, uint64_t inner, ui
                   2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? FLCE_OK : FLCE_ECUDA;
+  if (r != CUDA_SUCCESS) {
+    record_cuda_error(cudaErrorUnknown, "cuTensorMapEncodeTiled");
+    return FLCE_ECUDA;
+  }
+  return FLCE_OK;
 }
 
 // Operand description for the host launcher.
@@ -319,12 +357,13 @@ static int launch_gemm(const Operand& a, const Operand& b, int M, int N, int K, 
   const int tiles = ga.nMt * ga.nNt;
   if (tiles == 0) return FLCE_OK;
   auto kern = tc_gemm_kernel<T, BN, A_MN, B_MN, Epi>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes) !=
-      cudaSuccess)
-    return FLCE_ECUDA;
+  rc = cuda_status(
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes),
+      "cudaFuncSetAttribute(tc_gemm_kernel)");
+  if (rc != FLCE_OK) return rc;
   const int grid = std::min(tiles, sm_count());
   kern<<<grid, kGemmThreads, G::kSmemBytes, s>>>(ma, mb, ga, ep);
-  return launch_status();
+  return launch_status("tc_gemm_kernel launch");
 }
 
 // Group of M-tiles sharing one sweep over the N-tiles: as many 128-row slabs of
@@ -347,6 +386,9 @@ struct FlcePlan {
   int64_t part_ld;
   size_t off_part_m, off_part_s, off_zlab, off_rows, fwd_bytes;
   size_t off_dz, off_colsum, bwd_bytes;
+  // fp32 only: K-major copies of the operands the tf32 MMA cannot read MN-major
+  int64_t ldVt, ldCt;
+  size_t off_Wt, off_dzT, off_HT;
   size_t total;
 };
 
@@ -360,7 +402,6 @@ static int64_t default_chunk(int dt, int64_t N, int64_t D, int64_t V) {
 }
 
 static FlcePlan plan(int dt, int64_t N, int64_t D, int64_t V, int64_t chunk) {
-  (void)D;
   FlcePlan p;
   const size_t es = dtype_size(dt);
   p.chunk = chunk > 0 ? chunk : default_chunk(dt, N, D, V);
@@ -382,6 +423,17 @@ static FlcePlan plan(int dt, int64_t N, int64_t D, int64_t V, int64_t chunk) {
   o += round_up(static_cast<size_t>(std::min<int64_t>(p.chunk, N)) * p.ldV * es, 256);
   p.off_colsum = o;
   o += round_up(static_cast<size_t>(kColSplits) * V * 4, 256);
+  p.ldVt = (V + 3) / 4 * 4;
+  p.ldCt = (std::min<int64_t>(p.chunk, N) + 3) / 4 * 4;
+  p.off_Wt = p.off_dzT = p.off_HT = 0;
+  if (dt == FLCE_F32) {
+    p.off_Wt = o;
+    o += round_up(static_cast<size_t>(D) * p.ldVt * 4, 256);
+    p.off_dzT = o;
+    o += round_up(static_cast<size_t>(V) * p.ldCt * 4, 256);
+    p.off_HT = o;
+    o += round_up(static_cast<size_t>(D) * p.ldCt * 4, 256);
+  }
   p.bwd_bytes = o;
   p.total = std::max(p.fwd_bytes, p.bwd_bytes);
   return p;
@@ -454,7 +506,7 @@ extern "C" int flce_fwd(const void* H, const void* W, const void* bias, int dt, 
   lse_combine_kernel<<<static_cast<unsigned>((N + 255) / 256), 256, 0, s>>>(
       part_m, part_s, p.nparts, p.part_ld, zlab, labels, N, V, ignore_index, lse, rows,
       label_logit, status);
-  rc = launch_status();
+  rc = launch_status("lse_combine_kernel launch");
   if (rc != FLCE_OK) return rc;
   return launch_finalize(rows, labels, N, V, ignore_index, reduction, num_label_tokens, loss,
                          n_valid, s);
@@ -471,7 +523,16 @@ static int flce_bwd_impl(const void* H, const void* W, const void* bias, int64_t
   T* dz = reinterpret_cast<T*>(w + p.off_dz);
   float* colsum = reinterpret_cast<float*>(w + p.off_colsum);
   const T* Ht = static_cast<const T*>(H);
+  constexpr bool kTf32 = sizeof(T) == 4;
+  float* Wt = reinterpret_cast<float*>(w + p.off_Wt);    // [D, ldVt]  (fp32 only)
+  float* dzT = reinterpret_cast<float*>(w + p.off_dzT);  // [V, ldCt]  (fp32 only)
+  float* HT = reinterpret_cast<float*>(w + p.off_HT);    // [D, ldCt]  (fp32 only)
   int rc = FLCE_OK;
+  if (kTf32 && grad_H != nullptr) {
+    transpose32(static_cast<const float*>(W), (int)V, (int)D, D, Wt, p.ldVt, s);
+    rc = launch_status("transpose32(W) launch");
+    if (rc != FLCE_OK) return rc;
+  }
   for (int64_t r0 = 0; r0 < N; r0 += p.chunk) {
     const int C = static_cast<int>(std::min<int64_t>(p.chunk, N - r0));
     const int nMt = (C + kBM - 1) / kBM;
@@ -493,7 +554,7 @@ static int flce_bwd_impl(const void* H, const void* W, const void* bias, int64_t
       colsum_partial_kernel<T><<<g1, 256, 0, s>>>(dz, C, p.ldV, (int)V, colsum);
       colsum_final_kernel<<<static_cast<unsigned>((V + 255) / 256), 256, 0, s>>>(
           colsum, (int)V, grad_bias, r0 > 0 ? 1 : 0);
-      rc = launch_status();
+      rc = launch_status("colsum kernels launch");
       if (rc != FLCE_OK) return rc;
     }
     // 3. grad_H[chunk] = dZ W
@@ -501,8 +562,13 @@ static int flce_bwd_impl(const void* H, const void* W, const void* bias, int64_t
       using E = EpiStore<T, false>;
       typename E::Params ep{static_cast<T*>(grad_H) + r0 * D, D, C, static_cast<int>(D), 0};
       const Operand a{dz, C, V, p.ldV, false};
-      const Operand b{W, D, V, D, true};
-      rc = launch_gemm<T, 256, false, true, E>(a, b, C, (int)D, (int)V, 8, ep, status, s);
+      if (kTf32) {
+        const Operand b{Wt, D, V, p.ldVt, false};
+        rc = launch_gemm<T, 256, false, false, E>(a, b, C, (int)D, (int)V, 8, ep, status, s);
+      } else {
+        const Operand b{W, D, V, D, true};
+        rc = launch_gemm<T, 256, false, true, E>(a, b, C, (int)D, (int)V, 8, ep, status, s);
+      }
       if (rc != FLCE_OK) return rc;
     }
     // 4. grad_W (+)= dZ^T H[chunk]
@@ -510,9 +576,19 @@ static int flce_bwd_impl(const void* H, const void* W, const void* bias, int64_t
       using E = EpiStore<float, true>;
       typename E::Params ep{grad_W, D, static_cast<int>(V), static_cast<int>(D),
                             (r0 > 0 || accumulate_grad_W) ? 1 : 0};
-      const Operand a{dz, V, C, p.ldV, true};
-      const Operand b{Ht + r0 * D, D, C, D, true};
-      rc = launch_gemm<T, 256, true, true, E>(a, b, (int)V, (int)D, C, 8, ep, status, s);
+      if (kTf32) {
+        transpose32(reinterpret_cast<const float*>(dz), C, (int)V, p.ldV, dzT, p.ldCt, s);
+        transpose32(reinterpret_cast<const float*>(Ht + r0 * D), C, (int)D, D, HT, p.ldCt, s);
+        rc = launch_status("transpose32(dZ, H) launch");
+        if (rc != FLCE_OK) return rc;
+        const Operand a{dzT, V, C, p.ldCt, false};
+        const Operand b{HT, D, C, p.ldCt, false};
+        rc = launch_gemm<T, 256, false, false, E>(a, b, (int)V, (int)D, C, 8, ep, status, s);
+      } else {
+        const Operand a{dz, V, C, p.ldV, true};
+        const Operand b{Ht + r0 * D, D, C, D, true};
+        rc = launch_gemm<T, 256, true, true, E>(a, b, (int)V, (int)D, C, 8, ep, status, s);
+      }
       if (rc != FLCE_OK) return rc;
     }
   }
@@ -573,15 +649,14 @@ extern "C" int flce_gemm(int dt, int a_mn_major, int b_mn_major, int64_t M, int6
   const Operand b{B, N, K, ldb, b_mn_major != 0};
   using E = EpiStore<float, true>;
   E::Params ep{C, ldc, static_cast<int>(M), static_cast<int>(N), accumulate};
+  // The tf32 tensor-core path reads K-major operands only.
+  if (dt == FLCE_F32 && (a_mn_major || b_mn_major)) return FLCE_ENOSUP;
   const int code = (dt == FLCE_BF16 ? 0 : 4) | (a_mn_major ? 2 : 0) | (b_mn_major ? 1 : 0);
   switch (code) {
     case 0: return launch_gemm<__nv_bfloat16, 256, false, false, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
     case 1: return launch_gemm<__nv_bfloat16, 256, false, true, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
     case 2: return launch_gemm<__nv_bfloat16, 256, true, false, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
     case 3: return launch_gemm<__nv_bfloat16, 256, true, true, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
-    case 4: return launch_gemm<float, 256, false, false, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
-    case 5: return launch_gemm<float, 256, false, true, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
-    case 6: return launch_gemm<float, 256, true, false, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
-    default: return launch_gemm<float, 256, true, true, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
+    default: return launch_gemm<float, 256, false, false, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
   }
 }

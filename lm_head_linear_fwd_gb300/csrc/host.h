@@ -23,10 +23,19 @@ inline bool valid_dtype(int dt) { return dt == FLCE_BF16 || dt == FLCE_F32; }
 
 inline bool valid_reduction(int r) { return r == FLCE_SUM || r == FLCE_MEAN; }
 
+// Records a failed CUDA call for flce_last_cuda_error (per thread).
+void record_cuda_error(cudaError_t e, const char* where);
+
+// Maps a CUDA result to a status, recording failures.
+inline int cuda_status(cudaError_t e, const char* where) {
+  if (e == cudaSuccess) return FLCE_OK;
+  record_cuda_error(e, where);
+  return FLCE_ECUDA;
+}
+
 // Launch-time error of the last kernel launch (configuration errors only).
-inline int launch_status() {
-  cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? FLCE_OK : FLCE_ECUDA;
+inline int launch_status(const char* where = "kernel launch") {
+  return cuda_status(cudaGetLastError(), where);
 }
 
 // Per-row loss reduction shared by both operations: sums loss_rows[0..N) in a

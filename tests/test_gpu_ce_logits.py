@@ -70,16 +70,19 @@ def test_ce_parity(lh, dtype, reduction, nlt, N, V, ld):
 
 def test_inplace_grad_aliases_logits(lh):
     p = wl.random_ce(64, 5000, torch.bfloat16, seed=3)
-    logits, labels = _dev(p)
-    logits = logits.contiguous().requires_grad_(True)
-    ptr = logits.data_ptr()
+    base, labels = _dev(p)
+    base = base.contiguous().requires_grad_(True)
+    logits = base * 1.0  # a non-leaf, like the output of an lm_head
+    seen = {}
+    logits.register_hook(lambda g: seen.setdefault("g", g))
     loss = lh.ce_logits(logits, labels, inplace_grad=True)
     loss.backward()
     torch.cuda.synchronize()
-    assert logits.grad.data_ptr() == ptr
-    _check_grad(logits.grad, oracle.ce_backward(p.logits, p.labels))
-    # the logits storage now holds the gradient
-    assert torch.equal(logits.detach(), logits.grad)
+    # the gradient handed to autograd is the logits storage itself
+    assert seen["g"].data_ptr() == logits.data_ptr()
+    _check_grad(seen["g"], oracle.ce_backward(p.logits, p.labels))
+    assert torch.equal(logits.detach(), seen["g"])
+    _check_grad(base.grad, oracle.ce_backward(p.logits, p.labels))
 
 
 def test_default_does_not_mutate_logits(lh):

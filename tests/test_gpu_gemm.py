@@ -31,7 +31,7 @@ def _ref(A, B, a_mn, b_mn):
     return A64 @ B64.T
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
 @pytest.mark.parametrize("a_mn,b_mn", [(False, False), (False, True), (True, False), (True, True)])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (296, 520, 200), (1000, 264, 1032)])
 def test_gemm_layouts(lh, dtype, a_mn, b_mn, M, N, K):
@@ -40,6 +40,12 @@ def test_gemm_layouts(lh, dtype, a_mn, b_mn, M, N, K):
     B = torch.randn((K, N) if b_mn else (N, K), generator=g, device="cuda").to(dtype)
     C = torch.full((M, N), float("nan"), device="cuda")
     st = lh.new_status("cuda")
+    if dtype == torch.float32 and (a_mn or b_mn):
+        # the tf32 tensor-core path reads K-major operands only
+        with pytest.raises(lh.FlceError) as e:
+            lh.flce_gemm(A, B, C, a_mn, b_mn, accumulate=False, status=st)
+        assert e.value.code == -8
+        return
     lh.flce_gemm(A, B, C, a_mn, b_mn, accumulate=False, status=st)
     torch.cuda.synchronize()
     lh.check_status(st)
