@@ -1,0 +1,519 @@
+"""Benchmark of the language-model loss head on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  * fused linear CE forward + backward (logits = H W^T recomputed in the
+    backward; grad_H, fp32 grad_W) on the chosen FLCE workload, default the
+    Llama3-8B shape N=8192, D=4096, V=128256 bf16;
+  * CE on given logits forward + in-place backward on [16384, 128256] bf16.
+``value`` is the FLCE tokens/s of the step (the metric's first part); the
+given-logits part is reported beside it (GB/s and its HBM roofline).
+
+Timing: W warm-up steps, then exactly K timed steps between a barrier +
+synchronize on both sides, CUDA events on the launching stream, max over
+ranks.  Every input is larger than L2 (129 MB), so no flush is needed.
+With --impl reference the fp64 CPU oracle is timed instead, on a bounded row
+sample of the same workload, on the host cores.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload llama3_8b_flce|long_packed_flce|small_flce]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "tokens/s and % bf16 tensor peak for FLCE fwd+bwd; ce_logits HBM GB/s; peak extra GiB"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            out = {}
+            for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+                if k in d and d[k]:
+                    out[k] = float(d[k])
+            if len(out) == 3:
+                return out, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------- distributed
+
+def dist_setup(n_gpus):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        rank = int(os.environ["RANK"])
+        local = int(os.environ.get("LOCAL_RANK", rank))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        return rank, ws, local
+    return 0, 1, 0
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    smax.append(float(f[2]))
+                except ValueError:
+                    continue
+                for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                    "sw_power_cap"), f[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(name)
+        except Exception:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except Exception:
+                pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def _events_time(fn, steps, stream, before=None):
+    """Runs fn() `steps` times; returns per-step device ms (CUDA events on `stream`).
+    `before()` (untimed) runs ahead of each step."""
+    import torch
+    times = []
+    for _ in range(steps):
+        if before is not None:
+            before()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        times.append((e0, e1))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in times]
+
+
+def run_ours(args, rank, ws, local):
+    import torch
+    import workloads as wl
+    import lm_head_linear_fwd_gb300 as lh
+    from lm_head_linear_fwd_gb300 import _abi
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peaks, peak_src = load_peaks()
+
+    # ---------------------------------------------------------------- FLCE
+    if args.tokens and args.workload == "llama3_8b_flce":
+        p = wl.llama3_8b_flce(device=dev, N=args.tokens)
+    elif args.tokens and args.workload == "long_packed_flce":
+        p = wl.long_packed_flce(device=dev, B=1, T=args.tokens)
+    else:
+        p = wl.WORKLOADS[args.workload](device=dev)
+    H, W, b, y = p.H, p.W, p.bias, p.labels
+    N, D, V = p.N, p.D, p.V
+    dt = _abi.FLCE_BF16 if H.dtype == torch.bfloat16 else _abi.FLCE_F32
+    chunk = lh.flce_default_chunk(dt, N, D, V)
+    torch.cuda.synchronize()
+    base_mem = torch.cuda.memory_allocated(dev)
+    ws_bytes = lh.flce_workspace_bytes(dt, N, D, V, chunk)
+    wsbuf = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    status = lh.new_status(dev)
+    fo = lh.flce_fwd(H, W, y, b, p.ignore_index, p.reduction, p.num_label_tokens, ws=wsbuf,
+                     status=status)
+    one = torch.ones(1, device=dev)
+    gH = torch.empty_like(H)
+    gW = torch.empty((V, D), dtype=torch.float32, device=dev)
+    gb = torch.empty(V, dtype=torch.float32, device=dev) if b is not None else None
+    outputs_bytes = (gH.numel() * gH.element_size() + gW.numel() * 4 +
+                     (gb.numel() * 4 if gb is not None else 0) + N * 4 + 16)
+
+    def fwd():
+        lh.flce_fwd(H, W, y, b, p.ignore_index, p.reduction, p.num_label_tokens, ws=wsbuf,
+                    status=status, out=fo)
+
+    def bwd():
+        lh.flce_bwd(H, W, y, fo.lse, fo.n_valid, one, b, p.ignore_index, p.reduction,
+                    p.num_label_tokens, chunk, grad_H=gH, grad_W=gW, grad_bias=gb, ws=wsbuf,
+                    status=status)
+
+    def step():
+        fwd()
+        bwd()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats(dev)
+    step()
+    torch.cuda.synchronize()
+    peak_extra = torch.cuda.max_memory_allocated(dev) - base_mem - outputs_bytes
+    lh.check_status(status, "flce")
+
+    fwd_ms = _events_time(fwd, max(1, min(args.steps, 3)), stream)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_host0 = time.perf_counter()
+        step_ms = _events_time(step, args.steps, stream)
+        torch.cuda.synchronize()
+        host_s = time.perf_counter() - t_host0
+    barrier(ws)
+    clocks = clk.summary()
+    flce_ms = max_over_ranks(sum(step_ms) / len(step_ms), ws)
+    fwd_avg = sum(fwd_ms) / len(fwd_ms)
+    flops = 8.0 * N * D * V
+    tflops = flops / (flce_ms * 1e-3) / 1e12
+    tok_s = N * ws / (flce_ms * 1e-3)
+    n_chunks = (N + chunk - 1) // chunk
+    launches_flce = 3 + n_chunks * (3 + (2 if b is not None else 0))
+
+    # ------------------------------------------------------- e2e (host buffers)
+    Hh = H.cpu().pin_memory()
+    Wh = W.cpu().pin_memory()
+    yh = y.cpu().pin_memory()
+    bh = b.cpu().pin_memory() if b is not None else None
+    loss_h = torch.empty(1, dtype=torch.float32).pin_memory()
+    Hd, Wd, yd = torch.empty_like(H), torch.empty_like(W), torch.empty_like(y)
+    bd = torch.empty_like(b) if b is not None else None
+
+    def e2e_step():
+        Hd.copy_(Hh, non_blocking=True)
+        Wd.copy_(Wh, non_blocking=True)
+        yd.copy_(yh, non_blocking=True)
+        if bd is not None:
+            bd.copy_(bh, non_blocking=True)
+        lh.flce_fwd(Hd, Wd, yd, bd, p.ignore_index, p.reduction, p.num_label_tokens, ws=wsbuf,
+                    status=status, out=fo)
+        lh.flce_bwd(Hd, Wd, yd, fo.lse, fo.n_valid, one, bd, p.ignore_index, p.reduction,
+                    p.num_label_tokens, chunk, grad_H=gH, grad_W=gW, grad_bias=gb, ws=wsbuf,
+                    status=status)
+        loss_h.copy_(fo.loss, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(sum(_events_time(e2e_step, max(1, min(args.steps, 5)), stream)) /
+                            max(1, min(args.steps, 5)), ws)
+    h2d = (H.numel() * H.element_size() + W.numel() * W.element_size() + y.numel() * 8 +
+           (b.numel() * b.element_size() if b is not None else 0))
+    del Hh, Wh, yh, bh, Hd, Wd, yd, bd
+
+    # free the FLCE buffers before the given-logits part
+    del H, W, b, y, p, gH, gW, gb, wsbuf, fo
+    torch.cuda.empty_cache()
+
+    # ------------------------------------------------------ CE on given logits
+    if args.only == "flce":
+        line = {"metric": METRIC, "value": round(tok_s, 1), "unit": "tokens/s", "n_gpus": ws,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(flce_ms, 4),
+                "config": {"workload": f"FLCE only {args.workload} N={N} D={D} V={V}"},
+                "flce_tflops_8NDV": round(tflops, 2), "clocks": clocks,
+                "note": "profiling run: FLCE part only"}
+        if rank == 0:
+            print(json.dumps(line))
+        return
+    c = wl.ce_logits_large(device=dev)
+    pristine = c.logits.clone()
+    logits, labels = c.logits, c.labels
+    cws = torch.empty(max(1, lh.ce_logits_workspace_bytes(c.N, c.V)), dtype=torch.uint8,
+                      device=dev)
+    cst = lh.new_status(dev)
+    co = lh.ce_logits_fwd(logits, labels, c.ignore_index, c.reduction, c.num_label_tokens,
+                          ws=cws, status=cst)
+
+    def ce_step():
+        lh.ce_logits_fwd(logits, labels, c.ignore_index, c.reduction, c.num_label_tokens,
+                         ws=cws, status=cst, out=co)
+        lh.ce_logits_bwd(logits, labels, co.lse, co.n_valid, one, c.ignore_index, c.reduction,
+                         c.num_label_tokens, inplace_grad=True, status=cst)
+
+    def restore():
+        logits.copy_(pristine)
+
+    for _ in range(args.warmup):
+        restore()
+        ce_step()
+    torch.cuda.synchronize()
+    base_ce = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    ce_step()
+    torch.cuda.synchronize()
+    ce_peak_extra = torch.cuda.max_memory_allocated(dev) - base_ce
+    lh.check_status(cst, "ce_logits")
+    barrier(ws)
+    ce_times = _events_time(ce_step, args.steps, stream, before=restore)
+    ce_ms = max_over_ranks(sum(ce_times) / len(ce_times), ws)
+    ce_bytes = 3.0 * c.N * c.V * 2  # fwd read + bwd read + bwd write of the bf16 logits
+    ce_gbs = ce_bytes / (ce_ms * 1e-3) / 1e9
+    del pristine, logits, c, cws, co
+    torch.cuda.empty_cache()
+
+    # ------------------------------------------------------------ CPU baseline
+    cpu = cpu_baseline(args) if (rank == 0 and not args.no_cpu_baseline) else None
+
+    peak_t = peaks["bf16_tflops_sustained"]
+    line = {
+        "metric": METRIC,
+        "value": round(tok_s, 1),
+        "unit": "tokens/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(flce_ms + ce_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; random-init weights of the workload's shape)",
+        "config": {
+            "workload": (f"FLCE fwd+bwd {args.workload}: N={N} D={D} V={V} bf16, chunk={chunk}; "
+                         "plus CE on given logits [16384,128256] bf16 fwd+in-place bwd"),
+            "global_batch": N * ws,
+            "l2": "inputs larger than L2 (W and logits >= 1 GB); no flush",
+            "parallelism": f"replicas x{ws} (tokens sharded, no collective)",
+        },
+        "flce": {
+            "ms": round(flce_ms, 4),
+            "fwd_ms": round(fwd_avg, 4),
+            "tokens_per_s": round(tok_s, 1),
+            "tflops_8NDV": round(tflops, 2),
+            "mfu_6NDV_tflops": round(6.0 * N * D * V / (flce_ms * 1e-3) / 1e12, 2),
+            "frac_of_peak": round(tflops / peak_t, 4),
+            "peak_extra_gib": round(peak_extra / 2**30, 4),
+            "bound_one_chunk_fp32_tile_gib": round(chunk * V * 4 / 2**30, 4),
+            "chunk": chunk,
+        },
+        "ce_logits": {
+            "ms": round(ce_ms, 4),
+            "gb_s": round(ce_gbs, 1),
+            "frac_of_hbm": round(ce_gbs / peaks["hbm_gbs"], 4),
+            "frac_of_8tbs": round(ce_gbs / 8000.0, 4),
+            "peak_extra_gib": round(ce_peak_extra / 2**30, 6),
+            "tokens_per_s": round(16384 * ws / (ce_ms * 1e-3), 1),
+        },
+        "roofline": {
+            "bound": "tensor",
+            "kernel": "tc_gemm_kernel (all four FLCE contractions), whole fwd+bwd step",
+            "achieved": round(tflops, 2),
+            "peak": peak_t,
+            "unit": "TFLOP/s",
+            "frac": round(tflops / peak_t, 4),
+            "traffic": None,
+            "peak_source": f"bf16_tflops_sustained ({peak_src})",
+        },
+        "roofline_fwd": {
+            "bound": "tensor",
+            "kernel": "tc_gemm_kernel<EpiLse> + combine + finalize (flce_fwd)",
+            "achieved": round(2.0 * N * D * V / (fwd_avg * 1e-3) / 1e12, 2),
+            "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s",
+            "frac": round(2.0 * N * D * V / (fwd_avg * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+            "peak_source": f"bf16_tflops burst ({peak_src})",
+        },
+        "roofline_ce_logits": {
+            "bound": "hbm",
+            "kernel": "ce_fwd_rows_kernel + ce_bwd_rows_kernel (+ finalize)",
+            "achieved": round(ce_gbs, 1),
+            "peak": peaks["hbm_gbs"],
+            "unit": "GB/s",
+            "frac": round(ce_gbs / peaks["hbm_gbs"], 4),
+            "traffic": None,
+            "peak_source": f"hbm_gbs ({peak_src})",
+        },
+        "e2e": {
+            "value": round(N * ws / (e2e_ms * 1e-3), 1),
+            "unit": "tokens/s",
+            "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": 4,
+            "ms": round(e2e_ms, 4),
+            "what": "pinned host H, W, labels -> device, flce_fwd + flce_bwd, loss -> host",
+        },
+        "gpu_launches": int(args.steps * (launches_flce + 3)),
+        "clocks": clocks,
+        "host_wall_s_timed": round(host_s, 3),
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+
+
+# ------------------------------------------------------------- oracle timing
+
+def cpu_baseline(args, rows=None, workload=None):
+    """The fp64 oracle (as it stands) on a bounded row sample of the FLCE workload."""
+    import numpy as np
+    import torch
+
+    import oracle
+    import workloads as wl
+    wname = workload or args.workload
+    rows = rows or args.cpu_rows
+    p = wl.WORKLOADS[wname](device="cpu") if wname != "long_packed_flce" else \
+        wl.long_packed_flce(device="cpu")
+    rng = np.random.default_rng(0)
+    sel = np.sort(rng.choice(p.N, rows, replace=False))
+    t0 = time.perf_counter()
+    oracle.flce_forward(p.H, p.W, p.bias, p.labels, p.ignore_index, p.reduction,
+                        p.num_label_tokens, rows=sel)
+    oracle.flce_backward(p.H, p.W, p.bias, p.labels, p.ignore_index, p.reduction,
+                         p.num_label_tokens, rows=sel)
+    dt = time.perf_counter() - t0
+    return {"value": round(rows / dt, 3), "unit": "tokens/s", "cores": os.cpu_count(),
+            "threads": torch.get_num_threads(), "kind": "oracle",
+            "sample": f"{rows} sampled rows of {wname} (N={p.N}, D={p.D}, V={p.V}), fwd+bwd in "
+                      f"fp64 numpy, {dt:.2f} s"}
+
+
+def run_reference(args, rank, ws):
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+
+    import oracle
+    import workloads as wl
+    p = wl.WORKLOADS[args.workload](device="cpu")
+    rng = np.random.default_rng(0)
+    rows = args.cpu_rows
+    W64 = None
+    times = []
+    for i in range(args.warmup + args.steps):
+        sel = np.sort(rng.choice(p.N, rows, replace=False))
+        t0 = time.perf_counter()
+        oracle.flce_forward(p.H, p.W, p.bias, p.labels, p.ignore_index, p.reduction,
+                            p.num_label_tokens, rows=sel)
+        oracle.flce_backward(p.H, p.W, p.bias, p.labels, p.ignore_index, p.reduction,
+                             p.num_label_tokens, rows=sel)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    del W64
+    per = sum(times) / len(times)
+    v = rows / per
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(v, 3),
+        "unit": "tokens/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(per * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": f"FLCE fwd+bwd {args.workload}: N={p.N} D={p.D} V={p.V}; each "
+                               f"step a {rows}-row sample",
+                   "global_batch": rows, "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "cores": os.cpu_count(),
+                         "threads": torch.get_num_threads(), "kind": "oracle",
+                         "sample": f"{rows} rows per step of {args.workload}"},
+        "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama3_8b_flce",
+                    choices=["llama3_8b_flce", "long_packed_flce", "small_flce"])
+    ap.add_argument("--cpu-rows", type=int, default=32)
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override N of the FLCE workload (smaller cases for profiling)")
+    ap.add_argument("--only", choices=["all", "flce"], default="all",
+                    help="flce: skip the given-logits part (profiling runs)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, ws, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, ws)
+    else:
+        run_ours(args, rank, ws, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
