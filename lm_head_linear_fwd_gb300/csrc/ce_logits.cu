@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(THREADS) ce_bwd_rows_kernel(
 
 // ------------------------------------------------------------------ host side
 
-static thread_local char g_last_error[256] = "no CUDA error recorded";
+static thread_local char g_last_error[320] = "no CUDA error recorded";
 
 void record_cuda_error(cudaError_t e, const char* where) {
   snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, cudaGetErrorString(e),

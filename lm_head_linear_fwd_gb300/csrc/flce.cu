@@ -22,6 +22,7 @@
 // fp32 the MN-major operands of steps 3 and 4 are first transposed into the
 // workspace (W once per call, dZ and H[chunk] once per chunk).
 #include <math.h>
+#include <stdio.h>
 
 #include <algorithm>
 #include <mutex>
@@ -294,6 +295,17 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// cuTensorMapEncodeTiled is a driver call and needs a current context on the
+// calling thread.  A thread that has only launched kernels through a runtime
+// may have none bound yet (e.g. an autograd worker thread), so bind the
+// current device's primary context explicitly.
+static int bind_context() {
+  int dev = 0;
+  int rc = cuda_status(cudaGetDevice(&dev), "cudaGetDevice");
+  if (rc != FLCE_OK) return rc;
+  return cuda_status(cudaSetDevice(dev), "cudaSetDevice");
+}
+
 // 2-D map over a row-major matrix [outer, inner] with the given row stride, box
 // {128 bytes of inner, box_outer rows}, 128-byte swizzle, zero fill outside.
 static int make_map(CUtensorMap* m, const void* base, int dt, uint64_t inner, uint64_t outer,
@@ -314,7 +326,15 @@ static int make_map(CUtensorMap* m, const void* base, int dt, uint64_t inner, ui
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
-    record_cuda_error(cudaErrorUnknown, "cuTensorMapEncodeTiled");
+    char msg[200];
+    snprintf(msg, sizeof(msg),
+             "cuTensorMapEncodeTiled CUresult=%d addr=%p dims={%llu,%llu} stride=%llu "
+             "box={%u,%u} map@%p",
+             static_cast<int>(r), base, static_cast<unsigned long long>(inner),
+             static_cast<unsigned long long>(outer),
+             static_cast<unsigned long long>(row_stride_elems * es), box[0], box[1],
+             static_cast<void*>(m));
+    record_cuda_error(cudaErrorUnknown, msg);
     return FLCE_ECUDA;
   }
   return FLCE_OK;
@@ -479,6 +499,8 @@ extern "C" int flce_fwd(const void* H, const void* W, const void* bias, int dt, 
   const FlcePlan p = plan(dt, N, D, V, 0);
   if (ws == nullptr || ws_bytes < p.fwd_bytes) return FLCE_EWORKSPACE;
   if (!aligned(ws, 256)) return FLCE_EALIGN;
+  rc = bind_context();
+  if (rc != FLCE_OK) return rc;
   char* w = static_cast<char*>(ws);
   float* part_m = reinterpret_cast<float*>(w + p.off_part_m);
   float* part_s = reinterpret_cast<float*>(w + p.off_part_s);
@@ -615,6 +637,8 @@ extern "C" int flce_bwd(const void* H, const void* W, const void* bias, int dt, 
   if (ws == nullptr || ws_bytes < p.bwd_bytes) return FLCE_EWORKSPACE;
   if (!aligned(ws, 256)) return FLCE_EALIGN;
   if (grad_H == nullptr && grad_W == nullptr && grad_bias == nullptr) return FLCE_OK;
+  rc = bind_context();
+  if (rc != FLCE_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
   if (dt == FLCE_BF16)
@@ -644,13 +668,15 @@ extern "C" int flce_gemm(int dt, int a_mn_major, int b_mn_major, int64_t M, int6
       (ldb * es) % 16 != 0 || ldc % 4 != 0)
     return FLCE_EALIGN;
   if (lda < (a_mn_major ? M : K) || ldb < (b_mn_major ? N : K) || ldc < N) return FLCE_ESHAPE;
+  // The tf32 tensor-core path reads K-major operands only.
+  if (dt == FLCE_F32 && (a_mn_major || b_mn_major)) return FLCE_ENOSUP;
+  const int brc = bind_context();
+  if (brc != FLCE_OK) return brc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const Operand a{A, M, K, lda, a_mn_major != 0};
   const Operand b{B, N, K, ldb, b_mn_major != 0};
   using E = EpiStore<float, true>;
   E::Params ep{C, ldc, static_cast<int>(M), static_cast<int>(N), accumulate};
-  // The tf32 tensor-core path reads K-major operands only.
-  if (dt == FLCE_F32 && (a_mn_major || b_mn_major)) return FLCE_ENOSUP;
   const int code = (dt == FLCE_BF16 ? 0 : 4) | (a_mn_major ? 2 : 0) | (b_mn_major ? 1 : 0);
   switch (code) {
     case 0: return launch_gemm<__nv_bfloat16, 256, false, false, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
