@@ -121,6 +121,38 @@ FLCE_API int ce_logits_fwd(const void* logits, int dt, int64_t N, int64_t V, int
                   float* loss_rows, float* label_logit, void* ws, size_t ws_bytes,
                   int32_t* status, flce_stream_t stream);
 
+/* Largest N ce_logits_fwd_noalloc accepts. */
+#define CE_LOGITS_NOALLOC_MAX_ROWS (1 << 20)
+
+/* ce_logits_fwd without a workspace argument, for callers that cannot
+ * allocate device memory: for example a runtime that hands all device memory
+ * to its own pool at start-up and forbids further cudaMalloc, or a
+ * latency-critical loop where the device-wide synchronisation a cudaMalloc or
+ * cudaFree can cause is not acceptable.  The source pages have no counterpart;
+ * it is an addition of this library.
+ *
+ * Same arguments and results as ce_logits_fwd, without ws/ws_bytes and the
+ * optional loss_rows/label_logit outputs.  The caller still allocates and
+ * passes every input and output.  The per-row scratch lives in a static
+ * device array of CE_LOGITS_NOALLOC_MAX_ROWS floats (4 MiB) that every GPU
+ * which loads the library holds until the process exits; N above that
+ * maximum returns FLCE_ESHAPE and enqueues nothing.  No cudaMalloc, cudaFree
+ * or other allocating call is made.
+ *
+ * The first call on each device looks up the device address of the scratch
+ * array (cudaGetSymbolAddress, with that device current) and caches it; make
+ * that first call before any stream capture on the device.
+ *
+ * All calls share the one array and it keeps the last call's contents (none
+ * of which has to be cleared: each call writes every row it later reads).
+ * Calls whose work overlaps on the GPU (on different streams, or from
+ * different threads without ordering) race on the array and give wrong
+ * results: order them on one stream or with events. */
+FLCE_API int ce_logits_fwd_noalloc(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
+                  const int64_t* labels, int64_t ignore_index, int reduction,
+                  int64_t num_label_tokens, float* loss, int64_t* n_valid, float* lse,
+                  int32_t* status, flce_stream_t stream);
+
 /* Backward.  Reads logits, labels, lse (from ce_logits_fwd), n_valid (from
  * ce_logits_fwd; only read for FLCE_MEAN without num_label_tokens) and
  * grad_loss ([1] f32 device: the incoming gradient g of the loss), and writes

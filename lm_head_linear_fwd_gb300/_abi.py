@@ -33,6 +33,8 @@ _SIGNATURES = {
     "ce_logits_workspace_bytes": (_sz, [_i64, _i64]),
     "ce_logits_fwd": (_i, [_p, _i, _i64, _i64, _i64, _p, _i64, _i, _i64, _p, _p, _p, _p, _p,
                            _p, _sz, _p, _p]),
+    "ce_logits_fwd_noalloc": (_i, [_p, _i, _i64, _i64, _i64, _p, _i64, _i, _i64, _p, _p, _p, _p,
+                                   _p]),
     "ce_logits_bwd": (_i, [_p, _i, _i64, _i64, _i64, _p, _i64, _i, _i64, _p, _p, _p, _i, _p,
                            _i64, _p, _p]),
     "flce_workspace_bytes": (_sz, [_i, _i64, _i64, _i64, _i64]),
@@ -96,6 +98,7 @@ flce_status_string = _call("flce_status_string")
 flce_last_cuda_error = _call("flce_last_cuda_error")
 ce_logits_workspace_bytes = _call("ce_logits_workspace_bytes")
 ce_logits_fwd = _call("ce_logits_fwd")
+ce_logits_fwd_noalloc = _call("ce_logits_fwd_noalloc")
 ce_logits_bwd = _call("ce_logits_bwd")
 flce_workspace_bytes = _call("flce_workspace_bytes")
 flce_default_chunk = _call("flce_default_chunk")

@@ -327,6 +327,53 @@ extern "C" int ce_logits_fwd(const void* logits, int dt, int64_t N, int64_t V, i
                          n_valid, s);
 }
 
+// ------------------------------------------------- allocation-free forward
+
+// Per-row loss scratch of ce_logits_fwd_noalloc.  Every GPU that loads the
+// library holds this array (4 MiB) until the process exits.  All calls share it.
+static __device__ __align__(256) float g_noalloc_rows[CE_LOGITS_NOALLOC_MAX_ROWS];
+
+static std::mutex g_noalloc_mutex;
+static std::vector<float*> g_noalloc_ptr;  // device address of the array, per device id
+
+// Device address of g_noalloc_rows on the current device.  In host code the
+// array's name only stands in for the symbol, so the address is looked up once
+// per device, with that device current, and cached.
+static int noalloc_scratch(float** out) {
+  int dev = 0;
+  int rc = cuda_status(cudaGetDevice(&dev), "cudaGetDevice");
+  if (rc != FLCE_OK) return rc;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (static_cast<int>(g_noalloc_ptr.size()) <= dev) g_noalloc_ptr.resize(dev + 1, nullptr);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    rc = cuda_status(cudaGetSymbolAddress(&p, g_noalloc_rows), "cudaGetSymbolAddress");
+    if (rc != FLCE_OK) return rc;
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return FLCE_OK;
+}
+
+extern "C" int ce_logits_fwd_noalloc(const void* logits, int dt, int64_t N, int64_t V,
+                                     int64_t ld, const int64_t* labels, int64_t ignore_index,
+                                     int reduction, int64_t num_label_tokens, float* loss,
+                                     int64_t* n_valid, float* lse, int32_t* status,
+                                     flce_stream_t stream) {
+  int rc = ce_common_checks(logits, dt, N, V, ld, labels, reduction);
+  if (rc != FLCE_OK) return rc;
+  if (N > CE_LOGITS_NOALLOC_MAX_ROWS) return FLCE_ESHAPE;
+  if (loss == nullptr || n_valid == nullptr || status == nullptr) return FLCE_EINVAL;
+  if (N > 0 && lse == nullptr) return FLCE_EINVAL;
+  float* rows = nullptr;
+  rc = noalloc_scratch(&rows);
+  if (rc != FLCE_OK) return rc;
+  // Nothing in the scratch has to start at zero: the row kernel writes the loss
+  // of every row 0..N-1 before the finalize kernel reads it.
+  return ce_logits_fwd(logits, dt, N, V, ld, labels, ignore_index, reduction, num_label_tokens,
+                       loss, n_valid, lse, rows, nullptr, nullptr, 0, status, stream);
+}
+
 extern "C" int ce_logits_bwd(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
                              const int64_t* labels, int64_t ignore_index, int reduction,
                              int64_t num_label_tokens, const float* lse, const int64_t* n_valid,
