@@ -176,6 +176,9 @@ def run_ours(args, rank, ws, local):
     stream = torch.cuda.current_stream(dev)
     peaks, peak_src = load_peaks()
 
+    if args.only == "ce":
+        return run_ce_only(args, rank, ws, local, dev, stream, peaks, peak_src)
+
     # ---------------------------------------------------------------- FLCE
     if args.tokens and args.workload == "llama3_8b_flce":
         p = wl.llama3_8b_flce(device=dev, N=args.tokens)
@@ -285,7 +288,7 @@ def run_ours(args, rank, ws, local):
         if rank == 0:
             print(json.dumps(line))
         return
-    c = wl.ce_logits_large(device=dev)
+    c = wl.ce_logits_large(device=dev, N=args.ce_rows)
     pristine = c.logits.clone()
     logits, labels = c.logits, c.labels
     cws = torch.empty(max(1, lh.ce_logits_workspace_bytes(c.N, c.V)), dtype=torch.uint8,
@@ -317,6 +320,7 @@ def run_ours(args, rank, ws, local):
     ce_times = _events_time(ce_step, args.steps, stream, before=restore)
     ce_ms = max_over_ranks(sum(ce_times) / len(ce_times), ws)
     ce_bytes = 3.0 * c.N * c.V * 2  # fwd read + bwd read + bwd write of the bf16 logits
+    ce_N = c.N
     ce_gbs = ce_bytes / (ce_ms * 1e-3) / 1e9
     del pristine, logits, c, cws, co
     torch.cuda.empty_cache()
@@ -362,7 +366,7 @@ def run_ours(args, rank, ws, local):
             "frac_of_hbm": round(ce_gbs / peaks["hbm_gbs"], 4),
             "frac_of_8tbs": round(ce_gbs / 8000.0, 4),
             "peak_extra_gib": round(ce_peak_extra / 2**30, 6),
-            "tokens_per_s": round(16384 * ws / (ce_ms * 1e-3), 1),
+            "tokens_per_s": round(ce_N * ws / (ce_ms * 1e-3), 1),
         },
         "roofline": {
             "bound": "tensor",
@@ -408,6 +412,38 @@ def run_ours(args, rank, ws, local):
     }
     if rank == 0:
         print(json.dumps(line))
+
+
+def run_ce_only(args, rank, ws, local, dev, stream, peaks, peak_src):
+    """Given-logits part alone (profiling runs)."""
+    import torch
+    import workloads as wl
+    import lm_head_linear_fwd_gb300 as lh
+    c = wl.ce_logits_large(device=dev, N=args.ce_rows)
+    logits, labels = c.logits, c.labels
+    cws = torch.empty(max(1, lh.ce_logits_workspace_bytes(c.N, c.V)), dtype=torch.uint8,
+                      device=dev)
+    cst = lh.new_status(dev)
+    one = torch.ones(1, device=dev)
+    co = lh.ce_logits_fwd(logits, labels, c.ignore_index, c.reduction, ws=cws, status=cst)
+
+    def ce_step():
+        lh.ce_logits_fwd(logits, labels, c.ignore_index, c.reduction, ws=cws, status=cst, out=co)
+        lh.ce_logits_bwd(logits, labels, co.lse, co.n_valid, one, c.ignore_index, c.reduction,
+                         inplace_grad=True, status=cst)
+
+    for _ in range(args.warmup):
+        ce_step()
+    t = _events_time(ce_step, args.steps, stream)
+    ms = max_over_ranks(sum(t) / len(t), ws)
+    gbs = 3.0 * c.N * c.V * 2 / (ms * 1e-3) / 1e9
+    if rank == 0:
+        print(json.dumps({"metric": METRIC, "value": round(gbs, 1), "unit": "GB/s",
+                          "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": round(ms, 4),
+                          "config": {"workload": f"CE on logits only [{c.N},{c.V}] bf16"},
+                          "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                          "note": "profiling run: given-logits part only"}))
 
 
 # ------------------------------------------------------------- oracle timing
@@ -499,8 +535,10 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=32)
     ap.add_argument("--tokens", type=int, default=None,
                     help="override N of the FLCE workload (smaller cases for profiling)")
-    ap.add_argument("--only", choices=["all", "flce"], default="all",
-                    help="flce: skip the given-logits part (profiling runs)")
+    ap.add_argument("--only", choices=["all", "flce", "ce"], default="all",
+                    help="run one part only (profiling runs)")
+    ap.add_argument("--ce-rows", type=int, default=16384,
+                    help="rows of the given-logits workload (smaller cases for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -225,6 +225,232 @@ __global__ void __launch_bounds__(THREADS) ce_bwd_rows_kernel(
   }
 }
 
+
+// ------------------------------------------------ bulk-copy (TMA) row streaming
+
+// Rows whose start and length are 16-byte multiples are streamed through a
+// shared-memory ring instead: one producer thread copies 16 KB row segments
+// with cp.async.bulk (a 4-stage mbarrier ring, so up to 64 KB per CTA is in
+// flight without holding registers), and 8 consumer warps reduce (forward) or
+// transform and store (backward) each segment from shared memory.
+constexpr int kSegBytes = 16384;
+constexpr int kRingStages = 4;
+constexpr int kConsumers = 256;
+constexpr int kConsumerWarps = kConsumers / 32;
+constexpr int kStreamThreads = kConsumers + 32;
+constexpr int kStreamSmem = kRingStages * kSegBytes + 128;
+constexpr int kStreamCtasPerSm = 3;
+
+struct StreamArgs {
+  const void* logits;
+  int64_t N, V, ld;
+  const int64_t* labels;
+  int64_t ignore_index;
+  // forward
+  float* lse_out;
+  float* loss_rows;
+  float* label_logit;
+  // backward
+  int reduction;
+  int64_t num_label_tokens;
+  const float* lse_in;
+  const int64_t* n_valid;
+  const float* grad_loss;
+  void* grad;
+  int64_t ldg;
+  int32_t* status;
+};
+
+template <typename T, bool kBwd>
+__global__ void __launch_bounds__(kStreamThreads) ce_stream_kernel(const StreamArgs a) {
+  constexpr int EPV = Elem<T>::kPerVec;
+  constexpr int kVecPerSeg = kSegBytes / 16;
+  constexpr int kVecPerThread = kVecPerSeg / kConsumers;  // 4
+  extern __shared__ uint8_t ring_raw[];
+  __shared__ uint64_t full_bar[kRingStages], empty_bar[kRingStages];
+  __shared__ int abort_sh;
+  __shared__ float red_m[kConsumerWarps], red_s[kConsumerWarps];
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(ring_raw) + 127) & ~static_cast<uintptr_t>(127));
+  volatile int* abort_flag = &abort_sh;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int i = 0; i < kRingStages; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], kConsumerWarps);
+    }
+    abort_sh = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const int64_t row_bytes = a.V * static_cast<int64_t>(sizeof(T));
+  const int nseg = static_cast<int>((row_bytes + kSegBytes - 1) / kSegBytes);
+  const int seg_elems = kSegBytes / static_cast<int>(sizeof(T));
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int64_t row = blockIdx.x; row < a.N && ok; row += gridDim.x) {
+        const char* src = reinterpret_cast<const char*>(static_cast<const T*>(a.logits) +
+                                                        row * a.ld);
+        for (int sg = 0; sg < nseg; ++sg) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bytes = static_cast<uint32_t>(
+              min(static_cast<int64_t>(kSegBytes), row_bytes - static_cast<int64_t>(sg) * kSegBytes));
+          mbar_arrive_expect_tx(&full_bar[stage], bytes);
+          bulk_load(ring + stage * kSegBytes, src + static_cast<int64_t>(sg) * kSegBytes, bytes,
+                    &full_bar[stage]);
+          ++issued;
+          if (++stage == kRingStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        set_status(a.status, FLCE_ETIMEOUT);
+        for (int i = 0; i < kRingStages && i < issued; ++i) {
+          if (stage == 0) {
+            stage = kRingStages;
+            phase ^= 1u;
+          }
+          --stage;
+          const uint64_t t0 = global_ns();
+          while (!mbar_try_wait(smem_u32(&full_bar[stage]), phase) &&
+                 global_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  // --------------------------------------------------------------- consumers
+  float coef = 0.0f;
+  if (kBwd) coef = grad_coef(a.reduction, a.num_label_tokens, a.n_valid, a.grad_loss);
+  uint32_t stage = 0, phase = 0;
+  for (int64_t row = blockIdx.x; row < a.N; row += gridDim.x) {
+    const int64_t y = a.labels[row];
+    const bool valid = (y != a.ignore_index) && label_ok(y, a.V);
+    float c = 0.0f, lse2 = 0.0f;
+    if (kBwd) {
+      c = valid ? coef : 0.0f;
+      lse2 = a.lse_in[row] * kLog2e;
+    }
+    T* out = kBwd ? static_cast<T*>(a.grad) + row * a.ldg : nullptr;
+    Lse2 st;
+    for (int sg = 0; sg < nseg; ++sg) {
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&full_bar[stage], phase, abort_flag) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (ok) {
+        const int64_t e0 = static_cast<int64_t>(sg) * seg_elems;
+        const int nvec = static_cast<int>(
+            min(static_cast<int64_t>(kSegBytes), row_bytes - static_cast<int64_t>(sg) * kSegBytes) / 16);
+        const uint4* sv = reinterpret_cast<const uint4*>(ring + stage * kSegBytes);
+        if (!kBwd) {
+          float t[kVecPerThread * EPV];
+#pragma unroll
+          for (int k = 0; k < kVecPerThread; ++k) {
+            const int v = tid + k * kConsumers;
+            if (v < nvec) {
+              float x[EPV];
+              Elem<T>::unpack(sv[v], x);
+#pragma unroll
+              for (int e = 0; e < EPV; ++e) t[k * EPV + e] = x[e] * kLog2e;
+            } else {
+#pragma unroll
+              for (int e = 0; e < EPV; ++e) t[k * EPV + e] = -INFINITY;
+            }
+          }
+          st.addk(t);
+        } else {
+          const int64_t ylocal = y - e0;
+#pragma unroll
+          for (int k = 0; k < kVecPerThread; ++k) {
+            const int v = tid + k * kConsumers;
+            if (v < nvec) {
+              float x[EPV];
+              Elem<T>::unpack(sv[v], x);
+              const int64_t j0 = static_cast<int64_t>(v) * EPV;
+#pragma unroll
+              for (int e = 0; e < EPV; ++e)
+                x[e] = (c == 0.0f) ? 0.0f
+                                   : (ex2(fmaf(x[e], kLog2e, -lse2)) -
+                                      (j0 + e == ylocal ? 1.0f : 0.0f)) * c;
+              __stcs(reinterpret_cast<uint4*>(out + e0) + v, Elem<T>::pack(x));
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[stage]);
+      if (++stage == kRingStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!kBwd) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, st.m, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, st.s, o);
+        st.merge(m2, s2);
+      }
+      if (lane == 0) {
+        red_m[warp] = st.m;
+        red_s[warp] = st.s;
+      }
+      named_barrier(1, kConsumers);
+      if (tid == 0) {
+        Lse2 all;
+        for (int w = 0; w < kConsumerWarps; ++w) all.merge(red_m[w], red_s[w]);
+        const float lse = all.m * kLn2 + logf(all.s);
+        a.lse_out[row] = lse;
+        float li = 0.0f, zy = NAN;
+        if (y != a.ignore_index) {
+          if (valid) {
+            zy = Elem<T>::load(static_cast<const T*>(a.logits) + row * a.ld + y);
+            li = lse - zy;
+          } else {
+            set_status(a.status, FLCE_ELABEL);
+          }
+        }
+        a.loss_rows[row] = li;
+        if (a.label_logit != nullptr) a.label_logit[row] = zy;
+      }
+      named_barrier(1, kConsumers);
+    }
+  }
+}
+
+template <typename T, bool kBwd>
+static int launch_stream(const StreamArgs& a, cudaStream_t s) {
+  auto kern = ce_stream_kernel<T, kBwd>;
+  int rc = cuda_status(
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamSmem),
+      "cudaFuncSetAttribute(ce_stream_kernel)");
+  if (rc != FLCE_OK) return rc;
+  const int64_t g = static_cast<int64_t>(sm_count()) * kStreamCtasPerSm;
+  const int grid = static_cast<int>(a.N < g ? a.N : g);
+  kern<<<grid, kStreamThreads, kStreamSmem, s>>>(a);
+  return launch_status(kBwd ? "ce_stream_kernel<bwd> launch" : "ce_stream_kernel<fwd> launch");
+}
+
+// The bulk-copy path needs 16-byte aligned row starts and lengths.
+static bool streamable(const void* p, int64_t ld, int64_t V, size_t es) {
+  return aligned(p, 16) && (ld * static_cast<int64_t>(es)) % 16 == 0 &&
+         (V * static_cast<int64_t>(es)) % 16 == 0;
+}
+
 // ------------------------------------------------------------------ host side
 
 static thread_local char g_last_error[320] = "no CUDA error recorded";
@@ -309,7 +535,22 @@ extern "C" int ce_logits_fwd(const void* logits, int dt, int64_t N, int64_t V, i
     rows = static_cast<float*>(ws);
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (N > 0) {
+  if (N > 0 && streamable(logits, ld, V, dtype_size(dt))) {
+    StreamArgs a{};
+    a.logits = logits;
+    a.N = N;
+    a.V = V;
+    a.ld = ld;
+    a.labels = labels;
+    a.ignore_index = ignore_index;
+    a.lse_out = lse;
+    a.loss_rows = rows;
+    a.label_logit = label_logit;
+    a.status = status;
+    rc = dt == FLCE_BF16 ? launch_stream<__nv_bfloat16, false>(a, s)
+                         : launch_stream<float, false>(a, s);
+    if (rc != FLCE_OK) return rc;
+  } else if (N > 0) {
     const int grid = row_grid(N);
     if (dt == FLCE_BF16) {
       ce_fwd_rows_kernel<__nv_bfloat16, 512><<<grid, 512, 0, s>>>(
@@ -399,6 +640,25 @@ extern "C" int ce_logits_bwd(const void* logits, int dt, int64_t N, int64_t V, i
     return FLCE_EINVAL;  // out-of-place buffers must not overlap
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (streamable(logits, ld, V, es) && streamable(grad_logits, ld_grad, V, es)) {
+    StreamArgs a{};
+    a.logits = logits;
+    a.N = N;
+    a.V = V;
+    a.ld = ld;
+    a.labels = labels;
+    a.ignore_index = ignore_index;
+    a.reduction = reduction;
+    a.num_label_tokens = num_label_tokens;
+    a.lse_in = lse;
+    a.n_valid = n_valid;
+    a.grad_loss = grad_loss;
+    a.grad = grad_logits;
+    a.ldg = ld_grad;
+    a.status = status;
+    return dt == FLCE_BF16 ? launch_stream<__nv_bfloat16, true>(a, s)
+                           : launch_stream<float, true>(a, s);
+  }
   const int grid = row_grid(N);
   if (dt == FLCE_BF16) {
     ce_bwd_rows_kernel<__nv_bfloat16, 512><<<grid, 512, 0, s>>>(
