@@ -54,7 +54,8 @@ struct EpiLse {
     float* zlab;       // [M] label logit (written by the tile holding the label)
   };
   template <int BN>
-  __device__ static void tile(const Params& p, int mt, int nt, int row_in_tile, uint32_t taddr) {
+  __device__ static void tile(const Params& p, int mt, int nt, int row_in_tile, uint32_t taddr,
+                              EpiCtx&) {
     const int row = mt * kBM + row_in_tile;
     const bool row_ok = row < p.M;
     const int64_t y = row_ok ? p.labels[row] : -1;
@@ -86,7 +87,8 @@ struct EpiLse {
   }
 };
 
-// Backward step 1: dZ of one recomputed logits tile, stored as T.
+// Backward step 1: dZ of one recomputed logits tile, stored as T through TMA
+// (the output tensor map covers the chunk's [M, V] dZ buffer).
 template <typename T>
 struct EpiDlogits {
   struct Params {
@@ -99,11 +101,12 @@ struct EpiDlogits {
     const int64_t* n_valid;
     const float* grad_loss;
     int M, V;               // M = rows in this chunk
-    T* dz;                  // [M, ldd]
-    int64_t ldd;
   };
   template <int BN>
-  __device__ static void tile(const Params& p, int mt, int nt, int row_in_tile, uint32_t taddr) {
+  __device__ static void tile(const Params& p, int mt, int nt, int row_in_tile, uint32_t taddr,
+                              EpiCtx& ctx) {
+    constexpr int CPS = 128 / static_cast<int>(sizeof(T));  // columns per 128-byte row slab
+    constexpr int EPV = Elem<T>::kPerVec;
     const int row = mt * kBM + row_in_tile;
     const bool row_ok = row < p.M;
     const int64_t y = row_ok ? p.labels[row] : p.ignore_index;
@@ -113,81 +116,71 @@ struct EpiDlogits {
     const float lse2 = row_ok ? p.lse[row] * kLog2e : 0.0f;
     const int col_base = nt * BN;
     const int64_t ylocal = y - col_base;
-    T* out = p.dz + static_cast<int64_t>(row) * p.ldd;
+    const int r0 = mt * kBM + (row_in_tile & ~31);
 #pragma unroll 1
-    for (int cc = 0; cc < BN / 32; ++cc) {
-      const int col0 = col_base + cc * 32;
-      if (col0 >= p.V) break;
-      float v[32];
-      tmem_ld32(taddr + cc * 32, v);
+    for (int g = 0; g < BN / CPS; ++g) {
+      const int col0 = col_base + g * CPS;
+      if (col0 >= p.V) break;  // uniform across the warp
+      uint4 packed[8];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float x = v[j];
-        if (p.bias != nullptr && col0 + j < p.V) x += load_elem<T>(p.bias, col0 + j);
-        v[j] = (ex2(fmaf(x, kLog2e, -lse2)) - (cc * 32 + j == ylocal ? 1.0f : 0.0f)) * c;
-      }
-      if (!row_ok) continue;
-      constexpr int EPV = Elem<T>::kPerVec;
-      if (col0 + 32 <= p.V) {
-        uint4* q = reinterpret_cast<uint4*>(out + col0);
+      for (int h = 0; h < CPS / 32; ++h) {
+        float v[32];
+        tmem_ld32(taddr + g * CPS + h * 32, v);
+        const int cl = g * CPS + h * 32;  // column within the tile
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          float x = v[j];
+          if (p.bias != nullptr && col_base + cl + j < p.V)
+            x += load_elem<T>(p.bias, col_base + cl + j);
+          v[j] = (ex2(fmaf(x, kLog2e, -lse2)) - (cl + j == ylocal ? 1.0f : 0.0f)) * c;
+        }
 #pragma unroll
         for (int k = 0; k < 32 / EPV; ++k) {
           float x[EPV];
 #pragma unroll
           for (int e = 0; e < EPV; ++e) x[e] = v[k * EPV + e];
-          q[k] = Elem<T>::pack(x);
+          packed[h * (32 / EPV) + k] = Elem<T>::pack(x);
         }
-      } else {
-        for (int j = 0; j < 32 && col0 + j < p.V; ++j) Elem<T>::store(out + col0 + j, v[j]);
       }
+      ctx.store_slab(packed, col0, r0, false);
     }
   }
 };
 
-// Store the accumulator as OutT (grad_H), or add it into an fp32 matrix (grad_W).
+// Stores the accumulator as OutT through TMA (grad_H), or, with kAccumulate and
+// beta = 1, adds it into the existing fp32 output with a TMA reduce-add
+// (grad_W): the read-modify-write happens in L2, not on the SM.
 template <typename OutT, bool kAccumulate>
 struct EpiStore {
   struct Params {
-    OutT* out;
-    int64_t ldo;
     int M, N;
-    int beta;  // fp32 accumulate variant: 1 adds to the existing contents
+    int beta;  // accumulate variant: 1 adds to the existing contents
   };
   template <int BN>
-  __device__ static void tile(const Params& p, int mt, int nt, int row_in_tile, uint32_t taddr) {
-    const int row = mt * kBM + row_in_tile;
-    const bool row_ok = row < p.M;
-    OutT* out = p.out + static_cast<int64_t>(row) * p.ldo;
+  __device__ static void tile(const Params& p, int mt, int nt, int row_in_tile, uint32_t taddr,
+                              EpiCtx& ctx) {
+    constexpr int CPS = 128 / static_cast<int>(sizeof(OutT));
+    constexpr int EPV = Elem<OutT>::kPerVec;
+    const int r0 = mt * kBM + (row_in_tile & ~31);
+    const bool reduce = kAccumulate && p.beta != 0;
 #pragma unroll 1
-    for (int cc = 0; cc < BN / 32; ++cc) {
-      const int col0 = nt * BN + cc * 32;
+    for (int g = 0; g < BN / CPS; ++g) {
+      const int col0 = nt * BN + g * CPS;
       if (col0 >= p.N) break;
-      float v[32];
-      tmem_ld32(taddr + cc * 32, v);
-      if (!row_ok) continue;
-      constexpr int EPV = Elem<OutT>::kPerVec;
-      if (col0 + 32 <= p.N) {
-        uint4* q = reinterpret_cast<uint4*>(out + col0);
+      uint4 packed[8];
+#pragma unroll
+      for (int h = 0; h < CPS / 32; ++h) {
+        float v[32];
+        tmem_ld32(taddr + g * CPS + h * 32, v);
 #pragma unroll
         for (int k = 0; k < 32 / EPV; ++k) {
           float x[EPV];
-          if (kAccumulate && p.beta) {
-            Elem<OutT>::unpack(q[k], x);
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) x[e] += v[k * EPV + e];
-          } else {
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) x[e] = v[k * EPV + e];
-          }
-          q[k] = Elem<OutT>::pack(x);
-        }
-      } else {
-        for (int j = 0; j < 32 && col0 + j < p.N; ++j) {
-          float x = v[j];
-          if (kAccumulate && p.beta) x += Elem<OutT>::load(out + col0 + j);
-          Elem<OutT>::store(out + col0 + j, x);
+          for (int e = 0; e < EPV; ++e) x[e] = v[k * EPV + e];
+          packed[h * (32 / EPV) + k] = Elem<OutT>::pack(x);
         }
       }
+      ctx.store_slab(packed, col0, r0, reduce);
     }
   }
 };
@@ -355,16 +348,31 @@ static int make_operand_map(CUtensorMap* m, const Operand& op, int dt, int tile_
   return make_map(m, op.ptr, dt, op.rows, op.k, op.ld, ek);
 }
 
+// Output of an epilogue that stores through TMA: row-major [rows, cols] with
+// row stride ld (elements), written in boxes of 32 rows x 128 bytes.
+struct OutDesc {
+  void* ptr;
+  int dt;
+  int64_t rows, cols, ld;
+};
+
 template <typename T, int BN, bool A_MN, bool B_MN, class Epi>
-static int launch_gemm(const Operand& a, const Operand& b, int M, int N, int K, int group_m,
-                       const typename Epi::Params& ep, int32_t* status, cudaStream_t s) {
+static int launch_gemm(const Operand& a, const Operand& b, const OutDesc* out, int M, int N,
+                       int K, int group_m, const typename Epi::Params& ep, int32_t* status,
+                       cudaStream_t s) {
   using G = GemmGeo<T, BN>;
   const int dt = sizeof(T) == 2 ? FLCE_BF16 : FLCE_F32;
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mc;
   int rc = make_operand_map(&ma, a, dt, kBM);
   if (rc != FLCE_OK) return rc;
   rc = make_operand_map(&mb, b, dt, BN);
   if (rc != FLCE_OK) return rc;
+  if (out != nullptr) {
+    rc = make_map(&mc, out->ptr, out->dt, out->cols, out->rows, out->ld, 32);
+    if (rc != FLCE_OK) return rc;
+  } else {
+    mc = ma;  // unused by epilogues that do not store through TMA
+  }
   GemmArgs ga;
   ga.M = M;
   ga.N = N;
@@ -382,7 +390,7 @@ static int launch_gemm(const Operand& a, const Operand& b, int M, int N, int K, 
       "cudaFuncSetAttribute(tc_gemm_kernel)");
   if (rc != FLCE_OK) return rc;
   const int grid = std::min(tiles, sm_count());
-  kern<<<grid, kGemmThreads, G::kSmemBytes, s>>>(ma, mb, ga, ep);
+  kern<<<grid, kGemmThreads, G::kSmemBytes, s>>>(ma, mb, mc, ga, ep);
   return launch_status("tc_gemm_kernel launch");
 }
 
@@ -412,13 +420,36 @@ struct FlcePlan {
   size_t total;
 };
 
+// Rows per backward chunk.  The dZ buffer of one chunk is C x ldV elements of
+// the input dtype, kept at or below about 1.25 GiB (and never above 4864 rows);
+// within that, C (a multiple of 128) is chosen so that the grad_H contraction,
+// whose tile count C/128 x D/256 is the smallest of the backward's, fills whole
+// waves of the GPU's SMs over all chunks of N.
 static int64_t default_chunk(int dt, int64_t N, int64_t D, int64_t V) {
-  (void)dt;
-  (void)D;
-  (void)V;
-  int64_t c = 4096;
   const int64_t n128 = (N + 127) / 128 * 128;
-  return std::max<int64_t>(128, std::min(c, n128));
+  const int64_t ldV = (V + 63) / 64 * 64;
+  const int64_t row_bytes = ldV * static_cast<int64_t>(dtype_size(dt));
+  int64_t cap = std::min<int64_t>(4864, ((5ll << 28) / row_bytes) / 128 * 128);
+  cap = std::max<int64_t>(cap, 128);
+  if (n128 <= cap) return n128;
+  const int64_t sms = sm_count();
+  const int64_t nNt = (D + 255) / 256;
+  int64_t best = cap;
+  double best_eff = -1.0;
+  for (int64_t c = cap; c >= std::max<int64_t>(128, cap / 2); c -= 128) {
+    int64_t tiles = 0, slots = 0;
+    for (int64_t r0 = 0; r0 < N; r0 += c) {
+      const int64_t t = (std::min(c, N - r0) + 127) / 128 * nNt;
+      tiles += t;
+      slots += (t + sms - 1) / sms * sms;
+    }
+    const double eff = static_cast<double>(tiles) / static_cast<double>(slots);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = c;
+    }
+  }
+  return best;
 }
 
 static FlcePlan plan(int dt, int64_t N, int64_t D, int64_t V, int64_t chunk) {
@@ -515,14 +546,14 @@ extern "C" int flce_fwd(const void* H, const void* W, const void* bias, int dt, 
     using E = EpiLse<__nv_bfloat16>;
     E::Params ep{bias, labels, ignore_index, static_cast<int>(N), static_cast<int>(V),
                  p.part_ld, part_m, part_s, zlab};
-    rc = launch_gemm<__nv_bfloat16, kBNFwd, false, false, E>(a, b, (int)N, (int)V, (int)D, group,
-                                                             ep, status, s);
+    rc = launch_gemm<__nv_bfloat16, kBNFwd, false, false, E>(a, b, nullptr, (int)N, (int)V,
+                                                             (int)D, group, ep, status, s);
   } else {
     using E = EpiLse<float>;
     E::Params ep{bias, labels, ignore_index, static_cast<int>(N), static_cast<int>(V),
                  p.part_ld, part_m, part_s, zlab};
-    rc = launch_gemm<float, kBNFwd, false, false, E>(a, b, (int)N, (int)V, (int)D, group, ep,
-                                                     status, s);
+    rc = launch_gemm<float, kBNFwd, false, false, E>(a, b, nullptr, (int)N, (int)V, (int)D, group,
+                                                     ep, status, s);
   }
   if (rc != FLCE_OK) return rc;
   lse_combine_kernel<<<static_cast<unsigned>((N + 255) / 256), 256, 0, s>>>(
@@ -562,11 +593,11 @@ static int flce_bwd_impl(const void* H, const void* W, const void* bias, int64_t
     {
       using E = EpiDlogits<T>;
       typename E::Params ep{bias, labels + r0, ignore_index, lse + r0, reduction,
-                            num_label_tokens, n_valid, grad_loss, C, static_cast<int>(V), dz,
-                            p.ldV};
+                            num_label_tokens, n_valid, grad_loss, C, static_cast<int>(V)};
       const Operand a{Ht + r0 * D, C, D, D, false};
       const Operand b{W, V, D, D, false};
-      rc = launch_gemm<T, kBNFwd, false, false, E>(a, b, C, (int)V, (int)D,
+      const OutDesc o{dz, dt, C, V, p.ldV};
+      rc = launch_gemm<T, kBNFwd, false, false, E>(a, b, &o, C, (int)V, (int)D,
                                                    group_for(D, dt, nMt), ep, status, s);
       if (rc != FLCE_OK) return rc;
     }
@@ -582,22 +613,24 @@ static int flce_bwd_impl(const void* H, const void* W, const void* bias, int64_t
     // 3. grad_H[chunk] = dZ W
     if (grad_H != nullptr) {
       using E = EpiStore<T, false>;
-      typename E::Params ep{static_cast<T*>(grad_H) + r0 * D, D, C, static_cast<int>(D), 0};
+      typename E::Params ep{C, static_cast<int>(D), 0};
       const Operand a{dz, C, V, p.ldV, false};
+      const OutDesc o{static_cast<T*>(grad_H) + r0 * D, dt, C, D, D};
       if (kTf32) {
         const Operand b{Wt, D, V, p.ldVt, false};
-        rc = launch_gemm<T, 256, false, false, E>(a, b, C, (int)D, (int)V, 8, ep, status, s);
+        rc = launch_gemm<T, 256, false, false, E>(a, b, &o, C, (int)D, (int)V, 8, ep, status, s);
       } else {
         const Operand b{W, D, V, D, true};
-        rc = launch_gemm<T, 256, false, true, E>(a, b, C, (int)D, (int)V, 8, ep, status, s);
+        rc = launch_gemm<T, 256, false, true, E>(a, b, &o, C, (int)D, (int)V, 8, ep, status, s);
       }
       if (rc != FLCE_OK) return rc;
     }
     // 4. grad_W (+)= dZ^T H[chunk]
     if (grad_W != nullptr) {
       using E = EpiStore<float, true>;
-      typename E::Params ep{grad_W, D, static_cast<int>(V), static_cast<int>(D),
+      typename E::Params ep{static_cast<int>(V), static_cast<int>(D),
                             (r0 > 0 || accumulate_grad_W) ? 1 : 0};
+      const OutDesc o{grad_W, FLCE_F32, V, D, D};
       if (kTf32) {
         transpose32(reinterpret_cast<const float*>(dz), C, (int)V, p.ldV, dzT, p.ldCt, s);
         transpose32(reinterpret_cast<const float*>(Ht + r0 * D), C, (int)D, D, HT, p.ldCt, s);
@@ -605,11 +638,11 @@ static int flce_bwd_impl(const void* H, const void* W, const void* bias, int64_t
         if (rc != FLCE_OK) return rc;
         const Operand a{dzT, V, C, p.ldCt, false};
         const Operand b{HT, D, C, p.ldCt, false};
-        rc = launch_gemm<T, 256, false, false, E>(a, b, (int)V, (int)D, C, 8, ep, status, s);
+        rc = launch_gemm<T, 256, false, false, E>(a, b, &o, (int)V, (int)D, C, 8, ep, status, s);
       } else {
         const Operand a{dz, V, C, p.ldV, true};
         const Operand b{Ht + r0 * D, D, C, D, true};
-        rc = launch_gemm<T, 256, true, true, E>(a, b, (int)V, (int)D, C, 8, ep, status, s);
+        rc = launch_gemm<T, 256, true, true, E>(a, b, &o, (int)V, (int)D, C, 8, ep, status, s);
       }
       if (rc != FLCE_OK) return rc;
     }
@@ -676,13 +709,14 @@ extern "C" int flce_gemm(int dt, int a_mn_major, int b_mn_major, int64_t M, int6
   const Operand a{A, M, K, lda, a_mn_major != 0};
   const Operand b{B, N, K, ldb, b_mn_major != 0};
   using E = EpiStore<float, true>;
-  E::Params ep{C, ldc, static_cast<int>(M), static_cast<int>(N), accumulate};
+  E::Params ep{static_cast<int>(M), static_cast<int>(N), accumulate};
+  const OutDesc o{C, FLCE_F32, M, N, ldc};
   const int code = (dt == FLCE_BF16 ? 0 : 4) | (a_mn_major ? 2 : 0) | (b_mn_major ? 1 : 0);
   switch (code) {
-    case 0: return launch_gemm<__nv_bfloat16, 256, false, false, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
-    case 1: return launch_gemm<__nv_bfloat16, 256, false, true, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
-    case 2: return launch_gemm<__nv_bfloat16, 256, true, false, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
-    case 3: return launch_gemm<__nv_bfloat16, 256, true, true, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
-    default: return launch_gemm<float, 256, false, false, E>(a, b, (int)M, (int)N, (int)K, 8, ep, status, s);
+    case 0: return launch_gemm<__nv_bfloat16, 256, false, false, E>(a, b, &o, (int)M, (int)N, (int)K, 8, ep, status, s);
+    case 1: return launch_gemm<__nv_bfloat16, 256, false, true, E>(a, b, &o, (int)M, (int)N, (int)K, 8, ep, status, s);
+    case 2: return launch_gemm<__nv_bfloat16, 256, true, false, E>(a, b, &o, (int)M, (int)N, (int)K, 8, ep, status, s);
+    case 3: return launch_gemm<__nv_bfloat16, 256, true, true, E>(a, b, &o, (int)M, (int)N, (int)K, 8, ep, status, s);
+    default: return launch_gemm<float, 256, false, false, E>(a, b, &o, (int)M, (int)N, (int)K, 8, ep, status, s);
   }
 }

@@ -57,7 +57,9 @@ struct GemmGeo {
   static constexpr int kStageBytes = kStageA + kStageB;
   static constexpr int kStages = (BN == 256) ? 4 : 6;
   static constexpr int kTmemCols = 2 * BN;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + 1024-byte alignment slack
+  static constexpr int kEpiSmem = 4 * 2 * 4096;  // 4 epilogue warps x 2 staging buffers
+  static constexpr int kSmemBytes =
+      kStages * kStageBytes + kEpiSmem + 1024;  // + 1024-byte alignment slack
   static constexpr int kMmaPerStage = 128 / (MmaTraits<T>::kUmmaK * static_cast<int>(sizeof(T)));
 };
 
@@ -109,10 +111,46 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int k) {
   }
 }
 
+// Output staging of one epilogue warp: two 4 KB buffers (32 rows x 128 B,
+// 1024-byte aligned) written with the 128-byte swizzle the output tensor map
+// uses, each then stored (or reduce-added) to global memory by one TMA
+// instruction.  Rows and columns outside the tensor are clipped by the TMA.
+struct EpiCtx {
+  const CUtensorMap* map;
+  uint8_t* buf;
+  int next;
+  int lane;
+
+  __device__ void store_slab(const uint4 (&row)[8], int c0, int r0, bool reduce) {
+    uint8_t* b = buf + next * 4096;
+    if (lane == 0) bulk_wait_read_le1();  // the buffer's previous store has read it
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<uint4*>(b + lane * 128 + ((j ^ (lane & 7)) << 4)) = row[j];
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (reduce)
+        tma_reduce_add_2d(map, b, c0, r0);
+      else
+        tma_store_2d(map, b, c0, r0);
+      bulk_commit();
+    }
+    next ^= 1;
+  }
+
+  __device__ void drain() {
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+};
+
 template <typename T, int BN, bool A_MN, bool B_MN, class Epi>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmArgs ga, const typename Epi::Params ep) {
+                   const __grid_constant__ CUtensorMap tmC, const GemmArgs ga,
+                   const typename Epi::Params ep) {
   using G = GemmGeo<T, BN>;
   constexpr int S = G::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -248,6 +286,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // -------------------------------------------------------------- epilogue
     const int quad = warp & 3;  // TMEM lanes this warp may access: 32*quad .. +31
     const int row_in_tile = quad * 32 + lane;
+    EpiCtx ctx;
+    ctx.map = &tmC;
+    ctx.buf = smem + S * G::kStageBytes + (warp - 2) * 2 * 4096;
+    ctx.next = 0;
+    ctx.lane = lane;
     int local = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
       const int buf = local & 1;
@@ -264,11 +307,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tile_coords(t, ga.nMt, ga.nNt, ga.group_m, mt, nt);
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(buf * BN);
-      Epi::template tile<BN>(ep, mt, nt, row_in_tile, taddr);
+      Epi::template tile<BN>(ep, mt, nt, row_in_tile, taddr, ctx);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acce_bar[buf]);
     }
+    ctx.drain();
   }
 
   tc_fence_before();
