@@ -32,6 +32,25 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per FLCE fwd+bwd step
+# of the default workload, from the ncu launch list summarised in
+# profiles/flce_llama3_8b_launch_list.md, valid only for the kernel sources it
+# was taken from (sha256 prefix below); any change to them reports null.
+TRAFFIC = {"flce_step_bytes": 30.21e9, "csrc_sha": "76db89267ce67470"}
+
+
+def csrc_sha():
+    import glob
+    import hashlib
+    d = os.path.join(ROOT, "lm_head_linear_fwd_gb300", "csrc")
+    files = sorted(glob.glob(os.path.join(d, "*.cu")) + glob.glob(os.path.join(d, "*.cuh")) +
+                   glob.glob(os.path.join(d, "*.h")))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
 METRIC = "tokens/s and % bf16 tensor peak for FLCE fwd+bwd; ce_logits HBM GB/s; peak extra GiB"
 
 
@@ -375,7 +394,10 @@ def run_ours(args, rank, ws, local):
             "peak": peak_t,
             "unit": "TFLOP/s",
             "frac": round(tflops / peak_t, 4),
-            "traffic": None,
+            "traffic": (TRAFFIC["flce_step_bytes"]
+                        if (args.workload == "llama3_8b_flce" and not args.tokens and
+                            csrc_sha() == TRAFFIC["csrc_sha"]) else None),
+            "traffic_unit": "bytes per step (all FLCE kernels, ncu)",
             "peak_source": f"bf16_tflops_sustained ({peak_src})",
         },
         "roofline_fwd": {
