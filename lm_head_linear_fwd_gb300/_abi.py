@@ -43,6 +43,7 @@ _SIGNATURES = {
                       _p, _sz, _p, _p]),
     "flce_bwd": (_i, [_p, _p, _p, _i, _i64, _i64, _i64, _p, _i64, _i, _i64, _p, _p, _p, _i64,
                       _p, _p, _i, _p, _p, _sz, _p, _p]),
+    "flce_gemm_set_pair": (_i, [_i]),
     "flce_gemm": (_i, [_i, _i, _i, _i64, _i64, _i64, _p, _i64, _p, _i64, _p, _i64, _i, _p, _p]),
 }
 
@@ -105,3 +106,4 @@ flce_default_chunk = _call("flce_default_chunk")
 flce_fwd = _call("flce_fwd")
 flce_bwd = _call("flce_bwd")
 flce_gemm = _call("flce_gemm")
+flce_gemm_set_pair = _call("flce_gemm_set_pair")

@@ -25,6 +25,7 @@
 #include <stdio.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/flce_gemm.h"
@@ -356,22 +357,76 @@ struct OutDesc {
   int64_t rows, cols, ld;
 };
 
+// Which bf16 contractions run on CTA pairs (tc_gemm_pair_kernel) instead of one
+// CTA per tile: a bit mask of GemmRole.
+enum GemmRole : int { kRoleFwd = 1, kRoleDz = 2, kRoleGradH = 4, kRoleGradW = 8, kRoleRaw = 16 };
+static std::atomic<int> g_pair_mask{kRoleGradW | kRoleRaw};
+
+template <int BN, bool A_MN, bool B_MN, class Epi>
+static int launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
+                            int M, int N, int K, int group_m, const typename Epi::Params& ep,
+                            int32_t* status, cudaStream_t s) {
+  using G = PairGeo<BN>;
+  GemmArgs ga;
+  ga.M = M;
+  ga.N = N;
+  ga.K = K;
+  ga.nMt = (M + 2 * kBM - 1) / (2 * kBM);
+  ga.nNt = (N + BN - 1) / BN;
+  ga.nK = (K + G::kEK - 1) / G::kEK;
+  ga.group_m = std::max(1, std::min((group_m + 1) / 2, ga.nMt));
+  ga.status = status;
+  const int tiles = ga.nMt * ga.nNt;
+  if (tiles == 0) return FLCE_OK;
+  auto kern = tc_gemm_pair_kernel<BN, A_MN, B_MN, Epi>;
+  int rc = cuda_status(
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes),
+      "cudaFuncSetAttribute(tc_gemm_pair_kernel)");
+  if (rc != FLCE_OK) return rc;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = G::kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // as many pairs as can be resident at once (SMs of a GPC pair up; an odd one idles)
+  int max_pairs = 0;
+  cfg.gridDim = dim3(2 * static_cast<unsigned>(std::min(tiles, sm_count() / 2)), 1, 1);
+  rc = cuda_status(cudaOccupancyMaxActiveClusters(&max_pairs, kern, &cfg),
+                   "cudaOccupancyMaxActiveClusters");
+  if (rc != FLCE_OK) return rc;
+  if (max_pairs < 1) return FLCE_ENOSUP;
+  cfg.gridDim = dim3(2 * static_cast<unsigned>(std::min(tiles, max_pairs)), 1, 1);
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, ga, ep),
+                     "cudaLaunchKernelEx(tc_gemm_pair_kernel)");
+}
+
 template <typename T, int BN, bool A_MN, bool B_MN, class Epi>
-static int launch_gemm(const Operand& a, const Operand& b, const OutDesc* out, int M, int N,
-                       int K, int group_m, const typename Epi::Params& ep, int32_t* status,
-                       cudaStream_t s) {
+static int launch_gemm(int role, const Operand& a, const Operand& b, const OutDesc* out, int M,
+                       int N, int K, int group_m, const typename Epi::Params& ep,
+                       int32_t* status, cudaStream_t s) {
   using G = GemmGeo<T, BN>;
   const int dt = sizeof(T) == 2 ? FLCE_BF16 : FLCE_F32;
   CUtensorMap ma, mb, mc;
+  const bool pair = sizeof(T) == 2 && BN == 256 && (g_pair_mask.load() & role) != 0;
   int rc = make_operand_map(&ma, a, dt, kBM);
   if (rc != FLCE_OK) return rc;
-  rc = make_operand_map(&mb, b, dt, BN);
+  rc = make_operand_map(&mb, b, dt, pair ? BN / 2 : BN);
   if (rc != FLCE_OK) return rc;
   if (out != nullptr) {
     rc = make_map(&mc, out->ptr, out->dt, out->cols, out->rows, out->ld, 32);
     if (rc != FLCE_OK) return rc;
   } else {
     mc = ma;  // unused by epilogues that do not store through TMA
+  }
+  if constexpr (sizeof(T) == 2 && BN == 256) {
+    if (pair) return launch_gemm_pair<BN, A_MN, B_MN, Epi>(ma, mb, mc, M, N, K, group_m, ep,
+                                                         status, s);
   }
   GemmArgs ga;
   ga.M = M;
@@ -546,13 +601,13 @@ extern "C" int flce_fwd(const void* H, const void* W, const void* bias, int dt, 
     using E = EpiLse<__nv_bfloat16>;
     E::Params ep{bias, labels, ignore_index, static_cast<int>(N), static_cast<int>(V),
                  p.part_ld, part_m, part_s, zlab};
-    rc = launch_gemm<__nv_bfloat16, kBNFwd, false, false, E>(a, b, nullptr, (int)N, (int)V,
+    rc = launch_gemm<__nv_bfloat16, kBNFwd, false, false, E>(kRoleFwd, a, b, nullptr, (int)N, (int)V,
                                                              (int)D, group, ep, status, s);
   } else {
     using E = EpiLse<float>;
     E::Params ep{bias, labels, ignore_index, static_cast<int>(N), static_cast<int>(V),
                  p.part_ld, part_m, part_s, zlab};
-    rc = launch_gemm<float, kBNFwd, false, false, E>(a, b, nullptr, (int)N, (int)V, (int)D, group,
+    rc = launch_gemm<float, kBNFwd, false, false, E>(kRoleFwd, a, b, nullptr, (int)N, (int)V, (int)D, group,
                                                      ep, status, s);
   }
   if (rc != FLCE_OK) return rc;
@@ -597,7 +652,7 @@ static int flce_bwd_impl(const void* H, const void* W, const void* bias, int64_t
       const Operand a{Ht + r0 * D, C, D, D, false};
       const Operand b{W, V, D, D, false};
       const OutDesc o{dz, dt, C, V, p.ldV};
-      rc = launch_gemm<T, kBNFwd, false, false, E>(a, b, &o, C, (int)V, (int)D,
+      rc = launch_gemm<T, kBNFwd, false, false, E>(kRoleDz, a, b, &o, C, (int)V, (int)D,
                                                    group_for(D, dt, nMt), ep, status, s);
       if (rc != FLCE_OK) return rc;
     }
@@ -618,10 +673,12 @@ static int flce_bwd_impl(const void* H, const void* W, const void* bias, int64_t
       const OutDesc o{static_cast<T*>(grad_H) + r0 * D, dt, C, D, D};
       if (kTf32) {
         const Operand b{Wt, D, V, p.ldVt, false};
-        rc = launch_gemm<T, 256, false, false, E>(a, b, &o, C, (int)D, (int)V, 8, ep, status, s);
+        rc = launch_gemm<T, 256, false, false, E>(kRoleGradH, a, b, &o, C, (int)D, (int)V, 8, ep,
+                                                  status, s);
       } else {
         const Operand b{W, D, V, D, true};
-        rc = launch_gemm<T, 256, false, true, E>(a, b, &o, C, (int)D, (int)V, 8, ep, status, s);
+        rc = launch_gemm<T, 256, false, true, E>(kRoleGradH, a, b, &o, C, (int)D, (int)V, 8, ep,
+                                                 status, s);
       }
       if (rc != FLCE_OK) return rc;
     }
@@ -638,11 +695,13 @@ static int flce_bwd_impl(const void* H, const void* W, const void* bias, int64_t
         if (rc != FLCE_OK) return rc;
         const Operand a{dzT, V, C, p.ldCt, false};
         const Operand b{HT, D, C, p.ldCt, false};
-        rc = launch_gemm<T, 256, false, false, E>(a, b, &o, (int)V, (int)D, C, 8, ep, status, s);
+        rc = launch_gemm<T, 256, false, false, E>(kRoleGradW, a, b, &o, (int)V, (int)D, C, 8, ep,
+                                                  status, s);
       } else {
         const Operand a{dz, V, C, p.ldV, true};
         const Operand b{Ht + r0 * D, D, C, D, true};
-        rc = launch_gemm<T, 256, true, true, E>(a, b, &o, (int)V, (int)D, C, 8, ep, status, s);
+        rc = launch_gemm<T, 256, true, true, E>(kRoleGradW, a, b, &o, (int)V, (int)D, C, 8, ep,
+                                                status, s);
       }
       if (rc != FLCE_OK) return rc;
     }
@@ -685,6 +744,8 @@ extern "C" int flce_bwd(const void* H, const void* W, const void* bias, int dt, 
 
 // ------------------------------------------------------ raw GEMM entry point
 
+extern "C" int flce_gemm_set_pair(int mask) { return g_pair_mask.exchange(mask & 31); }
+
 extern "C" int flce_gemm(int dt, int a_mn_major, int b_mn_major, int64_t M, int64_t N, int64_t K,
                          const void* A, int64_t lda, const void* B, int64_t ldb, float* C,
                          int64_t ldc, int accumulate, int32_t* status, flce_stream_t stream) {
@@ -713,10 +774,10 @@ extern "C" int flce_gemm(int dt, int a_mn_major, int b_mn_major, int64_t M, int6
   const OutDesc o{C, FLCE_F32, M, N, ldc};
   const int code = (dt == FLCE_BF16 ? 0 : 4) | (a_mn_major ? 2 : 0) | (b_mn_major ? 1 : 0);
   switch (code) {
-    case 0: return launch_gemm<__nv_bfloat16, 256, false, false, E>(a, b, &o, (int)M, (int)N, (int)K, 8, ep, status, s);
-    case 1: return launch_gemm<__nv_bfloat16, 256, false, true, E>(a, b, &o, (int)M, (int)N, (int)K, 8, ep, status, s);
-    case 2: return launch_gemm<__nv_bfloat16, 256, true, false, E>(a, b, &o, (int)M, (int)N, (int)K, 8, ep, status, s);
-    case 3: return launch_gemm<__nv_bfloat16, 256, true, true, E>(a, b, &o, (int)M, (int)N, (int)K, 8, ep, status, s);
-    default: return launch_gemm<float, 256, false, false, E>(a, b, &o, (int)M, (int)N, (int)K, 8, ep, status, s);
+    case 0: return launch_gemm<__nv_bfloat16, 256, false, false, E>(kRoleRaw, a, b, &o, (int)M, (int)N, (int)K, 8, ep, status, s);
+    case 1: return launch_gemm<__nv_bfloat16, 256, false, true, E>(kRoleRaw, a, b, &o, (int)M, (int)N, (int)K, 8, ep, status, s);
+    case 2: return launch_gemm<__nv_bfloat16, 256, true, false, E>(kRoleRaw, a, b, &o, (int)M, (int)N, (int)K, 8, ep, status, s);
+    case 3: return launch_gemm<__nv_bfloat16, 256, true, true, E>(kRoleRaw, a, b, &o, (int)M, (int)N, (int)K, 8, ep, status, s);
+    default: return launch_gemm<float, 256, false, false, E>(kRoleRaw, a, b, &o, (int)M, (int)N, (int)K, 8, ep, status, s);
   }
 }

@@ -324,3 +324,234 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 }  // namespace flce
+
+// =====================================================================
+// CTA-pair variant (bf16): a cluster of two CTAs on two SMs computes one
+// 256 x BN tile with tcgen05.mma.cta_group::2.  Each CTA loads its own 128 rows
+// of A and its own BN/2 rows of B (so each SM moves half of B through shared
+// memory), the leader CTA (rank 0) issues the MMAs for the pair, and each CTA's
+// TMEM holds the accumulator rows of its own half.  Stages are 32 KB, so six
+// fit beside the epilogue staging buffers.
+//
+// Synchronisation:
+//   full[s]   leader only: one arrive (expect_tx for both CTAs' bytes); both
+//             CTAs' TMA loads complete_tx on it (the peer through its
+//             shared::cluster address)
+//   empty[s]  both CTAs: the leader's MMA commit arrives on both (multicast)
+//   accf[b]   both CTAs: accumulator b ready (multicast commit)
+//   acce[b]   leader only: 8 arrivals, the epilogue warps of both CTAs
+// =====================================================================
+
+namespace flce {
+
+template <int BN>
+struct PairGeo {
+  static constexpr int kEK = 64;  // bf16 elements per 128-byte row
+  static constexpr int kHalfN = BN / 2;
+  static constexpr int kStageA = kBM * 128;
+  static constexpr int kStageB = kHalfN * 128;
+  static constexpr int kStageBytes = kStageA + kStageB;
+  static constexpr int kStages = 6;
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kEpiSmem = 4 * 2 * 4096;
+  static constexpr int kSmemBytes = kStages * kStageBytes + kEpiSmem + 1024;
+  static constexpr int kMmaPerStage = 4;
+};
+
+template <bool MN>
+__device__ __forceinline__ void load_operand_pair(uint8_t* dst, const CUtensorMap* map,
+                                                  uint32_t bar_cluster, int rows, int row0,
+                                                  int kb) {
+  constexpr int EK = 64;
+  if (!MN) {
+    tma_load_2d_pair(dst, map, bar_cluster, kb * EK, row0);
+  } else {
+    for (int s = 0; s < rows / EK; ++s)
+      tma_load_2d_pair(dst + s * EK * 128, map, bar_cluster, row0 + s * EK, kb * EK);
+  }
+}
+
+template <int BN, bool A_MN, bool B_MN, class Epi>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, const GemmArgs ga,
+                        const typename Epi::Params ep) {
+  using G = PairGeo<BN>;
+  using T = __nv_bfloat16;
+  constexpr int S = G::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full_bar[S], empty_bar[S], accf_bar[2], acce_bar[2], drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  volatile int* abort_flag = &abort_sh;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&accf_bar[i], 1);
+      mbar_init(&acce_bar[i], 8);
+    }
+    mbar_init(&drain_bar, 1);
+    abort_sh = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&tmem_base_sh, G::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // barriers of both CTAs initialised; TMEM allocated in both
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_sh;
+  const int cluster_id = static_cast<int>(blockIdx.x >> 1);
+  const int nclusters = static_cast<int>(gridDim.x >> 1);
+  const int num_tiles = ga.nMt * ga.nNt;  // nMt counts 256-row tiles
+  const uint32_t full_leader = mapa_shared(smem_u32(&full_bar[0]), 0);
+  const uint32_t acce_leader = mapa_shared(smem_u32(&acce_bar[0]), 0);
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    set_status(ga.status, FLCE_ETIMEOUT);
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int t = cluster_id; t < num_tiles && ok; t += nclusters) {
+        int mt, nt;
+        tile_coords(t, ga.nMt, ga.nNt, ga.group_m, mt, nt);
+        const int arow = mt * 2 * kBM + static_cast<int>(rank) * kBM;
+        const int brow = nt * BN + static_cast<int>(rank) * G::kHalfN;
+        for (int kb = 0; kb < ga.nK; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * G::kStageBytes);
+          uint8_t* sa = smem + stage * G::kStageBytes;
+          const uint32_t fb = full_leader + stage * 8u;
+          load_operand_pair<A_MN>(sa, &tmA, fb, kBM, arow, kb);
+          load_operand_pair<B_MN>(sa + G::kStageA, &tmB, fb, G::kHalfN, brow, kb);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        fail();
+        // copies in flight complete on the leader's barrier; give them time to land
+        const uint64_t t0 = global_ns();
+        while (global_ns() - t0 < 20000000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (leader && lane == 0) {
+      // --------------------------------------------------------- MMA (leader)
+      constexpr uint32_t idesc = make_idesc(1, 2 * kBM, BN, A_MN, B_MN);
+      uint32_t stage = 0, phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int t = cluster_id; t < num_tiles && ok; t += nclusters, ++local) {
+        const int buf = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!mbar_wait(&acce_bar[buf], acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+        for (int kb = 0; kb < ga.nK; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * G::kStageBytes);
+          const uint32_t sb = sa + G::kStageA;
+#pragma unroll
+          for (int k = 0; k < G::kMmaPerStage; ++k) {
+            mma_f16_pair(d_tmem, operand_desc<T, A_MN>(sa, k), operand_desc<T, B_MN>(sb, k),
+                         idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit_pair(&empty_bar[stage], 0x3);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair(&accf_bar[buf], 0x3);
+      }
+      if (!ok) fail();
+      mma_commit_pair(&drain_bar, 0x1);
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(smem_u32(&drain_bar), 0) && global_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int quad = warp & 3;
+    const int row_in_tile = quad * 32 + lane;
+    EpiCtx ctx;
+    ctx.map = &tmC;
+    ctx.buf = smem + S * G::kStageBytes + (warp - 2) * 2 * 4096;
+    ctx.next = 0;
+    ctx.lane = lane;
+    int local = 0;
+    for (int t = cluster_id; t < num_tiles; t += nclusters, ++local) {
+      const int buf = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&accf_bar[buf], acc_phase, abort_flag) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) fail();
+        break;
+      }
+      tc_fence_after();
+      int mt, nt;
+      tile_coords(t, ga.nMt, ga.nNt, ga.group_m, mt, nt);
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(buf * BN);
+      // this CTA's half of the 256-row tile is 128-row tile 2*mt + rank
+      Epi::template tile<BN>(ep, 2 * mt + static_cast<int>(rank), nt, row_in_tile, taddr, ctx);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader)
+          mbar_arrive(&acce_bar[buf]);
+        else
+          mbar_arrive_cluster(acce_leader + static_cast<uint32_t>(buf) * 8u);
+      }
+    }
+    ctx.drain();
+  }
+
+  tc_fence_before();
+  cluster_sync();  // both CTAs done with the pair's TMEM and shared memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, G::kTmemCols);
+  }
+}
+
+}  // namespace flce

@@ -83,12 +83,18 @@ def test_small_model_workload(lh):
     _check_all(p, out, bw)
 
 
+@pytest.mark.parametrize("pair", [31, 0], ids=["pair", "single"])
 @pytest.mark.parametrize("N,D,V,chunk,bias", [(700, 256, 3001, 256, True), (129, 64, 777, 128, False),
                                               (1000, 520, 2048, None, False)])
-def test_ragged_multi_chunk(lh, N, D, V, chunk, bias):
-    p = wl.random_flce(N, D, V, torch.bfloat16, bias=bias, seed=N, reduction="mean")
-    out, bw = _run(lh, p, chunk=chunk, g=0.5)
-    _check_all(p, out, bw, g=0.5)
+def test_ragged_multi_chunk(lh, N, D, V, chunk, bias, pair):
+    from lm_head_linear_fwd_gb300 import _abi
+    prev = _abi.flce_gemm_set_pair(pair)
+    try:
+        p = wl.random_flce(N, D, V, torch.bfloat16, bias=bias, seed=N, reduction="mean")
+        out, bw = _run(lh, p, chunk=chunk, g=0.5)
+        _check_all(p, out, bw, g=0.5)
+    finally:
+        _abi.flce_gemm_set_pair(prev)
 
 
 def test_fp32_multi_chunk_with_bias(lh):

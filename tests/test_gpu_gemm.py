@@ -21,6 +21,15 @@ def lh():
     return m
 
 
+@pytest.fixture(params=[31, 0], ids=["pair", "single"])
+def variant(request, lh):
+    """bf16 contractions on CTA pairs (cta_group::2) or on single CTAs."""
+    from lm_head_linear_fwd_gb300 import _abi
+    prev = _abi.flce_gemm_set_pair(request.param)
+    yield request.param
+    _abi.flce_gemm_set_pair(prev)
+
+
 def _ref(A, B, a_mn, b_mn):
     A64 = A.double().cpu().numpy()
     B64 = B.double().cpu().numpy()
@@ -33,8 +42,9 @@ def _ref(A, B, a_mn, b_mn):
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
 @pytest.mark.parametrize("a_mn,b_mn", [(False, False), (False, True), (True, False), (True, True)])
-@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (296, 520, 200), (1000, 264, 1032)])
-def test_gemm_layouts(lh, dtype, a_mn, b_mn, M, N, K):
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (296, 520, 200), (1000, 264, 1032),
+                                   (2048, 4096, 512)])
+def test_gemm_layouts(lh, variant, dtype, a_mn, b_mn, M, N, K):
     g = torch.Generator(device="cuda").manual_seed(M * 7 + N * 3 + K)
     A = torch.randn((K, M) if a_mn else (M, K), generator=g, device="cuda").to(dtype)
     B = torch.randn((K, N) if b_mn else (N, K), generator=g, device="cuda").to(dtype)
@@ -60,7 +70,7 @@ def test_gemm_layouts(lh, dtype, a_mn, b_mn, M, N, K):
     assert err2 < tol, err2
 
 
-def test_gemm_is_deterministic(lh):
+def test_gemm_is_deterministic(lh, variant):
     g = torch.Generator(device="cuda").manual_seed(3)
     A = torch.randn(777, 512, generator=g, device="cuda").bfloat16()
     B = torch.randn(900, 512, generator=g, device="cuda").bfloat16()
