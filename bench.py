@@ -263,6 +263,29 @@ def run_ours(args, rank, ws, local):
     n_chunks = (N + chunk - 1) // chunk
     launches_flce = 3 + n_chunks * (3 + (2 if b is not None else 0))
 
+    # ------------------------------------- fused forward + backward (6NDV path)
+    fws = torch.empty(int(_abi.flce_fwd_bwd_workspace_bytes(dt, N, D, V, chunk)),
+                      dtype=torch.uint8, device=dev)
+    del wsbuf
+    torch.cuda.empty_cache()
+    torch.cuda.synchronize()
+
+    def fused():
+        lh.flce_fwd_bwd(H, W, y, b, p.ignore_index, p.reduction, p.num_label_tokens, chunk, None,
+                        ws=fws, status=status, grad_W=gW)
+
+    fused()
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats(dev)
+    fused()
+    torch.cuda.synchronize()
+    fused_peak_extra = torch.cuda.max_memory_allocated(dev) - base_mem - outputs_bytes
+    lh.check_status(status, "flce_fwd_bwd")
+    fused_ms = max_over_ranks(sum(_events_time(fused, args.steps, stream)) / args.steps, ws)
+    del fws
+    torch.cuda.empty_cache()
+    wsbuf = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+
     # ------------------------------------------------------- e2e (host buffers)
     Hh = H.cpu().pin_memory()
     Wh = W.cpu().pin_memory()
@@ -378,6 +401,14 @@ def run_ours(args, rank, ws, local):
             "peak_extra_gib": round(peak_extra / 2**30, 4),
             "bound_one_chunk_fp32_tile_gib": round(chunk * V * 4 / 2**30, 4),
             "chunk": chunk,
+        },
+        "flce_fused_fwd_bwd": {
+            "what": "flce_fwd_bwd: gradients formed in the forward, 6NDV flops",
+            "ms": round(fused_ms, 4),
+            "tokens_per_s": round(N * ws / (fused_ms * 1e-3), 1),
+            "tflops_6NDV": round(6.0 * N * D * V / (fused_ms * 1e-3) / 1e12, 2),
+            "frac_of_peak": round(6.0 * N * D * V / (fused_ms * 1e-3) / 1e12 / peak_t, 4),
+            "peak_extra_gib": round(fused_peak_extra / 2**30, 4),
         },
         "ce_logits": {
             "ms": round(ce_ms, 4),

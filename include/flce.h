@@ -209,6 +209,38 @@ FLCE_API int flce_bwd(const void* H, const void* W, const void* bias, int dt, in
              int accumulate_grad_W, float* grad_bias, void* ws, size_t ws_bytes,
              int32_t* status, flce_stream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Fused linear cross-entropy, forward and backward in one call             */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace bytes for flce_fwd_bwd (same chunk rule as flce_workspace_bytes). */
+FLCE_API size_t flce_fwd_bwd_workspace_bytes(int dt, int64_t N, int64_t D, int64_t V,
+                                             int64_t chunk);
+
+/* Loss and gradients in one call, with the gradient formed while the logits of
+ * each chunk are at hand: the eager-gradient variant of Liger-Kernel issue
+ * #533 "Gradient checkpointing for grad_weight in LFCE" (feature pitch: the
+ * gradients are computed in the forward and only scaled in the backward).
+ * It costs 6NDV flops instead of the 8NDV of flce_fwd + flce_bwd: per chunk
+ * the forward contraction also stores the chunk's logits (as base-2 offsets
+ * from each 256-column tile's maximum, in dtype dt) into the workspace, dZ is
+ * formed from them in place once the chunk's lse is known, and grad_H, grad_W,
+ * grad_bias follow as in flce_bwd.  grad_loss ([1] f32 device) may be NULL,
+ * meaning g = 1 (scale later with flce_grad_scale).  Outputs as flce_fwd
+ * (loss, n_valid, lse, optional loss_rows) and flce_bwd (grad_H, grad_W,
+ * grad_bias, each optional).  ws: flce_fwd_bwd_workspace_bytes bytes. */
+FLCE_API int flce_fwd_bwd(const void* H, const void* W, const void* bias, int dt, int64_t N,
+                          int64_t D, int64_t V, const int64_t* labels, int64_t ignore_index,
+                          int reduction, int64_t num_label_tokens, const float* grad_loss,
+                          int64_t chunk, float* loss, int64_t* n_valid, float* lse,
+                          float* loss_rows, void* grad_H, float* grad_W, int accumulate_grad_W,
+                          float* grad_bias, void* ws, size_t ws_bytes, int32_t* status,
+                          flce_stream_t stream);
+
+/* x[0..n) *= *g for x of dtype dt (device pointers); when *g == 1 nothing is
+ * written.  Applies the incoming gradient to gradients computed with g = 1. */
+FLCE_API int flce_grad_scale(void* x, int dt, int64_t n, const float* g, flce_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -43,6 +43,10 @@ _SIGNATURES = {
                       _p, _sz, _p, _p]),
     "flce_bwd": (_i, [_p, _p, _p, _i, _i64, _i64, _i64, _p, _i64, _i, _i64, _p, _p, _p, _i64,
                       _p, _p, _i, _p, _p, _sz, _p, _p]),
+    "flce_fwd_bwd_workspace_bytes": (_sz, [_i, _i64, _i64, _i64, _i64]),
+    "flce_fwd_bwd": (_i, [_p, _p, _p, _i, _i64, _i64, _i64, _p, _i64, _i, _i64, _p, _i64, _p, _p,
+                          _p, _p, _p, _p, _i, _p, _p, _sz, _p, _p]),
+    "flce_grad_scale": (_i, [_p, _i, _i64, _p, _p]),
     "flce_gemm_set_pair": (_i, [_i]),
     "flce_gemm": (_i, [_i, _i, _i, _i64, _i64, _i64, _p, _i64, _p, _i64, _p, _i64, _i, _p, _p]),
 }
@@ -106,4 +110,7 @@ flce_default_chunk = _call("flce_default_chunk")
 flce_fwd = _call("flce_fwd")
 flce_bwd = _call("flce_bwd")
 flce_gemm = _call("flce_gemm")
+flce_fwd_bwd_workspace_bytes = _call("flce_fwd_bwd_workspace_bytes")
+flce_fwd_bwd = _call("flce_fwd_bwd")
+flce_grad_scale = _call("flce_grad_scale")
 flce_gemm_set_pair = _call("flce_gemm_set_pair")

@@ -6,12 +6,12 @@ C ABI (``_abi``).  There is no CPU or eager-PyTorch fallback: a missing
 library or a non-CUDA tensor raises.
 
 Low-level calls (same names as the C entry points):
-    ce_logits_fwd, ce_logits_bwd, flce_fwd, flce_bwd, flce_gemm
+    ce_logits_fwd, ce_logits_bwd, flce_fwd, flce_bwd, flce_fwd_bwd, flce_gemm
 Autograd front ends:
     ce_logits(logits, labels, *, ignore_index, reduction, num_label_tokens,
               inplace_grad=False, mask=None)
     flce(H, W, labels, bias=None, *, ignore_index, reduction, num_label_tokens,
-         chunk=None, mask=None)
+         chunk=None, mask=None, eager=False)
 """
 from __future__ import annotations
 
@@ -286,6 +286,81 @@ def flce_bwd(H, W, labels, lse, n_valid, grad_loss, bias=None, ignore_index=-100
     return BackwardOut(grad_H, grad_W, grad_bias)
 
 
+def flce_fwd_bwd(H, W, labels, bias=None, ignore_index=-100, reduction="sum",
+                 num_label_tokens=None, chunk=None, grad_loss=None, *, want_grad_H=True,
+                 want_grad_W=True, want_grad_bias=None, want_rows=False, grad_W=None,
+                 accumulate_grad_W=False, ws=None, status=None):
+    """Loss and gradients in one call (6NDV flops).  Returns (ForwardOut, BackwardOut).
+    grad_loss None means g = 1."""
+    N, D, V = _flce_inputs(H, W, bias)
+    labels = _labels(labels, N)
+    dev = H.device
+    dt = _dtype_code(H)
+    ch = 0 if chunk is None else int(chunk)
+    if want_grad_bias is None:
+        want_grad_bias = bias is not None
+    out = ForwardOut(loss=torch.empty(1, dtype=torch.float32, device=dev),
+                     n_valid=torch.empty(1, dtype=torch.int64, device=dev),
+                     lse=torch.empty(N, dtype=torch.float32, device=dev),
+                     loss_rows=torch.empty(N, dtype=torch.float32, device=dev) if want_rows else None,
+                     label_logit=None,
+                     status=status if status is not None else new_status(dev))
+    gH = torch.empty((N, D), dtype=H.dtype, device=dev) if want_grad_H else None
+    if want_grad_W and grad_W is None:
+        grad_W = torch.empty((V, D), dtype=torch.float32, device=dev)
+    gW = grad_W if want_grad_W else None
+    gb = torch.empty(V, dtype=torch.float32, device=dev) if want_grad_bias else None
+    if ws is None:
+        ws = torch.empty(int(_abi.flce_fwd_bwd_workspace_bytes(dt, N, D, V, ch)),
+                         dtype=torch.uint8, device=dev)
+    g = None
+    if grad_loss is not None:
+        g = grad_loss.to(device=dev, dtype=torch.float32).reshape(1).contiguous()
+    rc = _abi.flce_fwd_bwd(_ptr(H), _ptr(W), _ptr(bias), dt, N, D, V, _ptr(labels),
+                           int(ignore_index), _red_code(reduction), _nlt(num_label_tokens), _ptr(g),
+                           ch, _ptr(out.loss), _ptr(out.n_valid), _ptr(out.lse),
+                           _ptr(out.loss_rows), _ptr(gH), _ptr(gW),
+                           1 if accumulate_grad_W else 0, _ptr(gb), _ptr(ws), ws.numel(),
+                           _ptr(out.status), _stream(dev))
+    _abi.check(rc, "flce_fwd_bwd")
+    return out, BackwardOut(gH, gW, gb)
+
+
+def grad_scale_(x: torch.Tensor, g: torch.Tensor) -> torch.Tensor:
+    """x *= g in place on the device (no work when g == 1)."""
+    _cuda(x, "x")
+    g = g.to(device=x.device, dtype=torch.float32).reshape(1).contiguous()
+    rc = _abi.flce_grad_scale(_ptr(x), _dtype_code(x), x.numel(), _ptr(g), _stream(x.device))
+    _abi.check(rc, "flce_grad_scale")
+    return x
+
+
+class _FLCEEager(torch.autograd.Function):
+    """Gradients formed during the forward (flce_fwd_bwd with g = 1), scaled by
+    the incoming gradient in the backward."""
+
+    @staticmethod
+    def forward(ctx, H, W, labels, bias, ignore_index, reduction, num_label_tokens, chunk):
+        out, bw = flce_fwd_bwd(H, W, labels, bias, ignore_index, reduction, num_label_tokens,
+                               chunk, want_grad_H=H.requires_grad, want_grad_W=W.requires_grad,
+                               want_grad_bias=bias is not None and bias.requires_grad)
+        ctx.grads = (bw.grad_H, bw.grad_W, bw.grad_bias)
+        return out.loss.reshape(())
+
+    @staticmethod
+    @once_differentiable
+    def backward(ctx, g):
+        gH, gW, gb = ctx.grads
+        ctx.grads = (None, None, None)
+        if gH is None and gW is None and gb is None:
+            raise RuntimeError("flce(eager=True): the gradients were already handed out; "
+                               "a second backward is not possible")
+        for t in (gH, gW, gb):
+            if t is not None:
+                grad_scale_(t, g)
+        return gH, gW, None, gb, None, None, None, None
+
+
 class _FLCE(torch.autograd.Function):
     @staticmethod
     def forward(ctx, H, W, labels, bias, ignore_index, reduction, num_label_tokens, chunk):
@@ -310,14 +385,17 @@ class _FLCE(torch.autograd.Function):
 
 
 def flce(H, W, labels, bias=None, *, ignore_index=-100, reduction="mean", num_label_tokens=None,
-         chunk=None, mask=None):
+         chunk=None, mask=None, eager=False):
     """Fused linear cross-entropy: loss of logits = H @ W.T (+ bias), never materialised.
 
     H: [N, D], W: [V, D] (tied-embedding layout), bias: [V] or None, labels:
-    [N] int64.  The backward recomputes the logits chunk by chunk (``chunk``
-    rows at a time; None picks the library default)."""
+    [N] int64.  Default: the backward recomputes the logits chunk by chunk
+    (``chunk`` rows at a time; None picks the library default), 8NDV flops in
+    all.  ``eager=True`` forms the gradients during the forward (6NDV flops)
+    and keeps them, fp32 grad_W included, until the backward scales them."""
     labels = _fold_mask(labels, mask, ignore_index)
-    return _FLCE.apply(H, W, labels, bias, int(ignore_index), reduction, num_label_tokens, chunk)
+    fn = _FLCEEager if eager else _FLCE
+    return fn.apply(H, W, labels, bias, int(ignore_index), reduction, num_label_tokens, chunk)
 
 
 # ------------------------------------------------------------------- raw GEMM

@@ -50,6 +50,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // Scale applied to every gradient: g * (1 / divisor), 0 when the divisor is 0.
+// A null grad_loss means g = 1.
 __device__ __forceinline__ float grad_coef(int reduction, int64_t num_label_tokens,
                                            const int64_t* n_valid, const float* grad_loss) {
   int64_t div;
@@ -61,7 +62,8 @@ __device__ __forceinline__ float grad_coef(int reduction, int64_t num_label_toke
     div = *n_valid;
   }
   if (div == 0) return 0.0f;
-  return (float)((double)(*grad_loss) / (double)div);
+  const double g = grad_loss != nullptr ? static_cast<double>(*grad_loss) : 1.0;
+  return static_cast<float>(g / static_cast<double>(div));
 }
 
 // Element access for the two supported storage types (16-byte vectors).

@@ -88,6 +88,79 @@ struct EpiLse {
   }
 };
 
+// Fused forward + backward, step 1: what EpiLse computes, and the tile's
+// logits stored through TMA as u = z*log2(e) - m_tile (<= 0, in the input
+// dtype) into the chunk buffer, so that the softmax can later be formed
+// without recomputing the logits.  Storing the offset from the tile's own
+// maximum keeps the rounding error of u small exactly where the softmax is
+// large.  Two passes over the TMEM columns: the maximum first, then u and
+// the sum of 2^u.
+template <typename T>
+struct EpiLseStore {
+  using Params = typename EpiLse<T>::Params;
+  template <int BN>
+  __device__ static void tile(const Params& p, int mt, int nt, int row_in_tile, uint32_t taddr,
+                              EpiCtx& ctx) {
+    constexpr int CPS = 128 / static_cast<int>(sizeof(T));
+    constexpr int EPV = Elem<T>::kPerVec;
+    const int row = mt * kBM + row_in_tile;
+    const bool row_ok = row < p.M;
+    const int64_t y = row_ok ? p.labels[row] : -1;
+    const int col_base = nt * BN;
+    const int64_t ylocal = y - col_base;
+    const int r0 = mt * kBM + (row_in_tile & ~31);
+    float m = -INFINITY, zy = 0.0f;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int col0 = col_base + c * 32;
+      if (col0 >= p.V) break;
+      float v[32];
+      tmem_ld32(taddr + c * 32, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float x = v[j];
+        if (p.bias != nullptr && col0 + j < p.V) x += load_elem<T>(p.bias, col0 + j);
+        if (c * 32 + j == ylocal) zy = x;
+        if (col0 + j < p.V) m = fmaxf(m, x * kLog2e);
+      }
+    }
+    float s = 0.0f;
+#pragma unroll 1
+    for (int g = 0; g < BN / CPS; ++g) {
+      const int col0 = col_base + g * CPS;
+      if (col0 >= p.V) break;
+      uint4 packed[8];
+#pragma unroll
+      for (int h = 0; h < CPS / 32; ++h) {
+        float v[32];
+        tmem_ld32(taddr + g * CPS + h * 32, v);
+        const int cb = col0 + h * 32;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          float x = v[j];
+          if (p.bias != nullptr && cb + j < p.V) x += load_elem<T>(p.bias, cb + j);
+          const float u = fmaf(x, kLog2e, -m);
+          if (cb + j < p.V) s += ex2(u);
+          v[j] = u;
+        }
+#pragma unroll
+        for (int k = 0; k < 32 / EPV; ++k) {
+          float x[EPV];
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) x[e] = v[k * EPV + e];
+          packed[h * (32 / EPV) + k] = Elem<T>::pack(x);
+        }
+      }
+      ctx.store_slab(packed, col0, r0, false);
+    }
+    if (row_ok) {
+      p.part_m[nt * p.part_ld + row] = m;
+      p.part_s[nt * p.part_ld + row] = s;
+      if (ylocal >= 0 && ylocal < BN) p.zlab[row] = zy;
+    }
+  }
+};
+
 // Backward step 1: dZ of one recomputed logits tile, stored as T through TMA
 // (the output tensor map covers the chunk's [M, V] dZ buffer).
 template <typename T>
@@ -266,6 +339,86 @@ static void transpose32(const float* in, int R, int Cc, int64_t ld_in, float* ou
                         int64_t ld_out, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>((Cc + 31) / 32), static_cast<unsigned>((R + 31) / 32));
   transpose32_kernel<<<grid, 256, 0, s>>>(in, R, Cc, ld_in, out, ld_out);
+}
+
+// Fused forward + backward, step 3: in place over the chunk buffer,
+// dZ = (2^(u + m_tile - lse*log2(e)) - [j == y]) * coef, one CTA per row
+// (grid-stride); the row's per-tile maxima are staged in shared memory first.
+constexpr int kMaxTilesPerRow = 8192;  // V < 2^21 with 256-wide tiles
+
+template <typename T>
+__global__ void __launch_bounds__(256) dz_from_u_kernel(
+    T* buf, int C, int V, int64_t ldd, const float* __restrict__ part_m, int nparts,
+    int64_t part_ld, const float* __restrict__ lse, const int64_t* __restrict__ labels,
+    int64_t ignore_index, int reduction, int64_t num_label_tokens, const int64_t* n_valid,
+    const float* grad_loss) {
+  constexpr int EPV = Elem<T>::kPerVec;
+  extern __shared__ float mrow[];
+  const float coef = grad_coef(reduction, num_label_tokens, n_valid, grad_loss);
+  const int nvec = V / EPV;
+  for (int row = blockIdx.x; row < C; row += gridDim.x) {
+    const int64_t y = labels[row];
+    const bool valid = (y != ignore_index) && label_ok(y, V);
+    const float c = valid ? coef : 0.0f;
+    const float lse2 = lse[row] * kLog2e;
+    __syncthreads();  // mrow of the previous row fully used
+    for (int t = threadIdx.x; t < nparts; t += blockDim.x)
+      mrow[t] = part_m[static_cast<int64_t>(t) * part_ld + row] - lse2;
+    __syncthreads();
+    T* r = buf + static_cast<int64_t>(row) * ldd;
+    uint4* rv = reinterpret_cast<uint4*>(r);
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+      float x[EPV];
+      const int j0 = v * EPV;
+      if (c == 0.0f) {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) x[e] = 0.0f;
+      } else {
+        Elem<T>::unpack(rv[v], x);
+        const float off = mrow[j0 >> 8];  // all EPV columns lie in one 256-wide tile
+#pragma unroll
+        for (int e = 0; e < EPV; ++e)
+          x[e] = (ex2(x[e] + off) - (j0 + e == y ? 1.0f : 0.0f)) * c;
+      }
+      rv[v] = Elem<T>::pack(x);
+    }
+    for (int j = nvec * EPV + threadIdx.x; j < V; j += blockDim.x) {
+      float d = 0.0f;
+      if (c != 0.0f)
+        d = (ex2(Elem<T>::load(r + j) + mrow[j >> 8]) - (j == y ? 1.0f : 0.0f)) * c;
+      Elem<T>::store(r + j, d);
+    }
+  }
+}
+
+// n_valid = number of labels that are not ignore_index and lie in [0, V).
+__global__ void __launch_bounds__(1024) count_valid_kernel(const int64_t* __restrict__ labels,
+                                                           int64_t N, int64_t V,
+                                                           int64_t ignore_index,
+                                                           int64_t* __restrict__ n_valid) {
+  __shared__ long long sc[1024];
+  long long cnt = 0;
+  for (int64_t i = threadIdx.x; i < N; i += 1024) {
+    const int64_t y = labels[i];
+    cnt += (y != ignore_index && label_ok(y, V)) ? 1 : 0;
+  }
+  sc[threadIdx.x] = cnt;
+  __syncthreads();
+  for (int w = 512; w > 0; w >>= 1) {
+    if (threadIdx.x < w) sc[threadIdx.x] += sc[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *n_valid = sc[0];
+}
+
+// x *= g (one float read per thread; nothing is written when g == 1).
+template <typename T>
+__global__ void __launch_bounds__(256) scale_kernel(T* x, int64_t n, const float* g) {
+  const float s = *g;
+  if (s == 1.0f) return;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    Elem<T>::store(x + i, Elem<T>::load(x + i) * s);
 }
 
 // --------------------------------------------------------------- host: TMA
@@ -472,6 +625,9 @@ struct FlcePlan {
   // fp32 only: K-major copies of the operands the tf32 MMA cannot read MN-major
   int64_t ldVt, ldCt;
   size_t off_Wt, off_dzT, off_HT;
+  // fused forward + backward: chunk-sized partials after the backward buffers
+  int64_t fpart_ld;
+  size_t off_fpart_m, off_fpart_s, off_fzlab, off_frows, fused_bytes;
   size_t total;
 };
 
@@ -542,6 +698,16 @@ static FlcePlan plan(int dt, int64_t N, int64_t D, int64_t V, int64_t chunk) {
   }
   p.bwd_bytes = o;
   p.total = std::max(p.fwd_bytes, p.bwd_bytes);
+  p.fpart_ld = (std::min<int64_t>(p.chunk, N) + 63) / 64 * 64;
+  p.off_fpart_m = o;
+  o += round_up(static_cast<size_t>(p.nparts) * p.fpart_ld * 4, 256);
+  p.off_fpart_s = o;
+  o += round_up(static_cast<size_t>(p.nparts) * p.fpart_ld * 4, 256);
+  p.off_fzlab = o;
+  o += round_up(static_cast<size_t>(N) * 4, 256);
+  p.off_frows = o;
+  o += round_up(static_cast<size_t>(N) * 4, 256);
+  p.fused_bytes = o;
   return p;
 }
 
@@ -620,6 +786,81 @@ extern "C" int flce_fwd(const void* H, const void* W, const void* bias, int dt, 
                          n_valid, s);
 }
 
+// Steps 2-4 of a backward chunk, shared by flce_bwd and flce_fwd_bwd: bias
+// column sums, grad_H of the chunk, grad_W accumulation, from the chunk's dZ.
+template <typename T>
+static int bwd_tail(const void* W, const T* Hc, int64_t D, int64_t V, int C, bool first_chunk,
+                    const FlcePlan& p, char* w, void* grad_H_chunk, float* grad_W,
+                    int accumulate_grad_W, float* grad_bias, int32_t* status, cudaStream_t s) {
+  const int dt = sizeof(T) == 2 ? FLCE_BF16 : FLCE_F32;
+  constexpr bool kTf32 = sizeof(T) == 4;
+  T* dz = reinterpret_cast<T*>(w + p.off_dz);
+  float* colsum = reinterpret_cast<float*>(w + p.off_colsum);
+  float* Wt = reinterpret_cast<float*>(w + p.off_Wt);    // [D, ldVt]  (fp32 only)
+  float* dzT = reinterpret_cast<float*>(w + p.off_dzT);  // [V, ldCt]  (fp32 only)
+  float* HT = reinterpret_cast<float*>(w + p.off_HT);    // [D, ldCt]  (fp32 only)
+  int rc = FLCE_OK;
+  // 2. bias gradient
+  if (grad_bias != nullptr) {
+    dim3 g1(static_cast<unsigned>((V + 255) / 256), kColSplits);
+    colsum_partial_kernel<T><<<g1, 256, 0, s>>>(dz, C, p.ldV, (int)V, colsum);
+    colsum_final_kernel<<<static_cast<unsigned>((V + 255) / 256), 256, 0, s>>>(
+        colsum, (int)V, grad_bias, first_chunk ? 0 : 1);
+    rc = launch_status("colsum kernels launch");
+    if (rc != FLCE_OK) return rc;
+  }
+  // 3. grad_H[chunk] = dZ W
+  if (grad_H_chunk != nullptr) {
+    using E = EpiStore<T, false>;
+    typename E::Params ep{C, static_cast<int>(D), 0};
+    const Operand a{dz, C, V, p.ldV, false};
+    const OutDesc o{grad_H_chunk, dt, C, D, D};
+    if (kTf32) {
+      const Operand b{Wt, D, V, p.ldVt, false};
+      rc = launch_gemm<T, 256, false, false, E>(kRoleGradH, a, b, &o, C, (int)D, (int)V, 8, ep,
+                                                status, s);
+    } else {
+      const Operand b{W, D, V, D, true};
+      rc = launch_gemm<T, 256, false, true, E>(kRoleGradH, a, b, &o, C, (int)D, (int)V, 8, ep,
+                                               status, s);
+    }
+    if (rc != FLCE_OK) return rc;
+  }
+  // 4. grad_W (+)= dZ^T H[chunk]
+  if (grad_W != nullptr) {
+    using E = EpiStore<float, true>;
+    typename E::Params ep{static_cast<int>(V), static_cast<int>(D),
+                          (!first_chunk || accumulate_grad_W) ? 1 : 0};
+    const OutDesc o{grad_W, FLCE_F32, V, D, D};
+    if (kTf32) {
+      transpose32(reinterpret_cast<const float*>(dz), C, (int)V, p.ldV, dzT, p.ldCt, s);
+      transpose32(reinterpret_cast<const float*>(Hc), C, (int)D, D, HT, p.ldCt, s);
+      rc = launch_status("transpose32(dZ, H) launch");
+      if (rc != FLCE_OK) return rc;
+      const Operand a{dzT, V, C, p.ldCt, false};
+      const Operand b{HT, D, C, p.ldCt, false};
+      rc = launch_gemm<T, 256, false, false, E>(kRoleGradW, a, b, &o, (int)V, (int)D, C, 8, ep,
+                                                status, s);
+    } else {
+      const Operand a{dz, V, C, p.ldV, true};
+      const Operand b{Hc, D, C, D, true};
+      rc = launch_gemm<T, 256, true, true, E>(kRoleGradW, a, b, &o, (int)V, (int)D, C, 8, ep,
+                                              status, s);
+    }
+    if (rc != FLCE_OK) return rc;
+  }
+  return rc;
+}
+
+template <typename T>
+static int transpose_W_if_needed(const void* W, int64_t D, int64_t V, const FlcePlan& p, char* w,
+                                 void* grad_H, cudaStream_t s) {
+  if (sizeof(T) != 4 || grad_H == nullptr) return FLCE_OK;
+  transpose32(static_cast<const float*>(W), (int)V, (int)D, D,
+              reinterpret_cast<float*>(w + p.off_Wt), p.ldVt, s);
+  return launch_status("transpose32(W) launch");
+}
+
 template <typename T>
 static int flce_bwd_impl(const void* H, const void* W, const void* bias, int64_t N, int64_t D,
                          int64_t V, const int64_t* labels, int64_t ignore_index, int reduction,
@@ -629,84 +870,87 @@ static int flce_bwd_impl(const void* H, const void* W, const void* bias, int64_t
                          int32_t* status, cudaStream_t s) {
   const int dt = sizeof(T) == 2 ? FLCE_BF16 : FLCE_F32;
   T* dz = reinterpret_cast<T*>(w + p.off_dz);
-  float* colsum = reinterpret_cast<float*>(w + p.off_colsum);
   const T* Ht = static_cast<const T*>(H);
-  constexpr bool kTf32 = sizeof(T) == 4;
-  float* Wt = reinterpret_cast<float*>(w + p.off_Wt);    // [D, ldVt]  (fp32 only)
-  float* dzT = reinterpret_cast<float*>(w + p.off_dzT);  // [V, ldCt]  (fp32 only)
-  float* HT = reinterpret_cast<float*>(w + p.off_HT);    // [D, ldCt]  (fp32 only)
-  int rc = FLCE_OK;
-  if (kTf32 && grad_H != nullptr) {
-    transpose32(static_cast<const float*>(W), (int)V, (int)D, D, Wt, p.ldVt, s);
-    rc = launch_status("transpose32(W) launch");
-    if (rc != FLCE_OK) return rc;
-  }
+  int rc = transpose_W_if_needed<T>(W, D, V, p, w, grad_H, s);
+  if (rc != FLCE_OK) return rc;
   for (int64_t r0 = 0; r0 < N; r0 += p.chunk) {
     const int C = static_cast<int>(std::min<int64_t>(p.chunk, N - r0));
     const int nMt = (C + kBM - 1) / kBM;
     // 1. recompute logits, form dZ
+    using E = EpiDlogits<T>;
+    typename E::Params ep{bias, labels + r0, ignore_index, lse + r0, reduction,
+                          num_label_tokens, n_valid, grad_loss, C, static_cast<int>(V)};
+    const Operand a{Ht + r0 * D, C, D, D, false};
+    const Operand b{W, V, D, D, false};
+    const OutDesc o{dz, dt, C, V, p.ldV};
+    rc = launch_gemm<T, kBNFwd, false, false, E>(kRoleDz, a, b, &o, C, (int)V, (int)D,
+                                                 group_for(D, dt, nMt), ep, status, s);
+    if (rc != FLCE_OK) return rc;
+    rc = bwd_tail<T>(W, Ht + r0 * D, D, V, C, r0 == 0, p, w,
+                     grad_H != nullptr ? static_cast<T*>(grad_H) + r0 * D : nullptr, grad_W,
+                     accumulate_grad_W, grad_bias, status, s);
+    if (rc != FLCE_OK) return rc;
+  }
+  return rc;
+}
+
+// Fused forward + backward: per chunk, the forward GEMM also stores the
+// chunk's logits (as offsets u from each tile's maximum), the chunk's lse is
+// combined, dZ is formed in place from u, then steps 2-4 as in flce_bwd.
+template <typename T>
+static int flce_fused_impl(const void* H, const void* W, const void* bias, int64_t N, int64_t D,
+                           int64_t V, const int64_t* labels, int64_t ignore_index,
+                           int reduction, int64_t num_label_tokens, const float* grad_loss,
+                           const FlcePlan& p, float* loss, int64_t* n_valid, float* lse,
+                           float* loss_rows, void* grad_H, float* grad_W, int accumulate_grad_W,
+                           float* grad_bias, char* w, int32_t* status, cudaStream_t s) {
+  const int dt = sizeof(T) == 2 ? FLCE_BF16 : FLCE_F32;
+  T* dz = reinterpret_cast<T*>(w + p.off_dz);
+  float* part_m = reinterpret_cast<float*>(w + p.off_fpart_m);
+  float* part_s = reinterpret_cast<float*>(w + p.off_fpart_s);
+  float* zlab = reinterpret_cast<float*>(w + p.off_fzlab);
+  float* rows = loss_rows != nullptr ? loss_rows : reinterpret_cast<float*>(w + p.off_frows);
+  const T* Ht = static_cast<const T*>(H);
+  count_valid_kernel<<<1, 1024, 0, s>>>(labels, N, V, ignore_index, n_valid);
+  int rc = launch_status("count_valid_kernel launch");
+  if (rc != FLCE_OK) return rc;
+  rc = transpose_W_if_needed<T>(W, D, V, p, w, grad_H, s);
+  if (rc != FLCE_OK) return rc;
+  for (int64_t r0 = 0; r0 < N; r0 += p.chunk) {
+    const int C = static_cast<int>(std::min<int64_t>(p.chunk, N - r0));
+    const int nMt = (C + kBM - 1) / kBM;
+    // 1. logits of the chunk: lse partials and u into the chunk buffer
     {
-      using E = EpiDlogits<T>;
-      typename E::Params ep{bias, labels + r0, ignore_index, lse + r0, reduction,
-                            num_label_tokens, n_valid, grad_loss, C, static_cast<int>(V)};
+      using E = EpiLseStore<T>;
+      typename E::Params ep{bias, labels + r0, ignore_index, C, static_cast<int>(V),
+                            p.fpart_ld, part_m, part_s, zlab + r0};
       const Operand a{Ht + r0 * D, C, D, D, false};
       const Operand b{W, V, D, D, false};
       const OutDesc o{dz, dt, C, V, p.ldV};
-      rc = launch_gemm<T, kBNFwd, false, false, E>(kRoleDz, a, b, &o, C, (int)V, (int)D,
+      rc = launch_gemm<T, kBNFwd, false, false, E>(kRoleFwd, a, b, &o, C, (int)V, (int)D,
                                                    group_for(D, dt, nMt), ep, status, s);
       if (rc != FLCE_OK) return rc;
     }
-    // 2. bias gradient
-    if (grad_bias != nullptr) {
-      dim3 g1(static_cast<unsigned>((V + 255) / 256), kColSplits);
-      colsum_partial_kernel<T><<<g1, 256, 0, s>>>(dz, C, p.ldV, (int)V, colsum);
-      colsum_final_kernel<<<static_cast<unsigned>((V + 255) / 256), 256, 0, s>>>(
-          colsum, (int)V, grad_bias, r0 > 0 ? 1 : 0);
-      rc = launch_status("colsum kernels launch");
-      if (rc != FLCE_OK) return rc;
+    // 2. lse and per-row loss of the chunk
+    lse_combine_kernel<<<static_cast<unsigned>((C + 255) / 256), 256, 0, s>>>(
+        part_m, part_s, p.nparts, p.fpart_ld, zlab + r0, labels + r0, C, V, ignore_index,
+        lse + r0, rows + r0, nullptr, status);
+    // 3. dZ in place
+    {
+      const int grid = std::min(C, sm_count() * 8);
+      dz_from_u_kernel<T><<<grid, 256, p.nparts * sizeof(float), s>>>(
+          dz, C, (int)V, p.ldV, part_m, p.nparts, p.fpart_ld, lse + r0, labels + r0,
+          ignore_index, reduction, num_label_tokens, n_valid, grad_loss);
     }
-    // 3. grad_H[chunk] = dZ W
-    if (grad_H != nullptr) {
-      using E = EpiStore<T, false>;
-      typename E::Params ep{C, static_cast<int>(D), 0};
-      const Operand a{dz, C, V, p.ldV, false};
-      const OutDesc o{static_cast<T*>(grad_H) + r0 * D, dt, C, D, D};
-      if (kTf32) {
-        const Operand b{Wt, D, V, p.ldVt, false};
-        rc = launch_gemm<T, 256, false, false, E>(kRoleGradH, a, b, &o, C, (int)D, (int)V, 8, ep,
-                                                  status, s);
-      } else {
-        const Operand b{W, D, V, D, true};
-        rc = launch_gemm<T, 256, false, true, E>(kRoleGradH, a, b, &o, C, (int)D, (int)V, 8, ep,
-                                                 status, s);
-      }
-      if (rc != FLCE_OK) return rc;
-    }
-    // 4. grad_W (+)= dZ^T H[chunk]
-    if (grad_W != nullptr) {
-      using E = EpiStore<float, true>;
-      typename E::Params ep{static_cast<int>(V), static_cast<int>(D),
-                            (r0 > 0 || accumulate_grad_W) ? 1 : 0};
-      const OutDesc o{grad_W, FLCE_F32, V, D, D};
-      if (kTf32) {
-        transpose32(reinterpret_cast<const float*>(dz), C, (int)V, p.ldV, dzT, p.ldCt, s);
-        transpose32(reinterpret_cast<const float*>(Ht + r0 * D), C, (int)D, D, HT, p.ldCt, s);
-        rc = launch_status("transpose32(dZ, H) launch");
-        if (rc != FLCE_OK) return rc;
-        const Operand a{dzT, V, C, p.ldCt, false};
-        const Operand b{HT, D, C, p.ldCt, false};
-        rc = launch_gemm<T, 256, false, false, E>(kRoleGradW, a, b, &o, (int)V, (int)D, C, 8, ep,
-                                                  status, s);
-      } else {
-        const Operand a{dz, V, C, p.ldV, true};
-        const Operand b{Ht + r0 * D, D, C, D, true};
-        rc = launch_gemm<T, 256, true, true, E>(kRoleGradW, a, b, &o, (int)V, (int)D, C, 8, ep,
-                                                status, s);
-      }
-      if (rc != FLCE_OK) return rc;
-    }
+    rc = launch_status("lse_combine / dz_from_u launch");
+    if (rc != FLCE_OK) return rc;
+    rc = bwd_tail<T>(W, Ht + r0 * D, D, V, C, r0 == 0, p, w,
+                     grad_H != nullptr ? static_cast<T*>(grad_H) + r0 * D : nullptr, grad_W,
+                     accumulate_grad_W, grad_bias, status, s);
+    if (rc != FLCE_OK) return rc;
   }
-  return rc;
+  return launch_finalize(rows, labels, N, V, ignore_index, reduction, num_label_tokens, loss,
+                         n_valid, s);
 }
 
 extern "C" int flce_bwd(const void* H, const void* W, const void* bias, int dt, int64_t N,
@@ -740,6 +984,62 @@ extern "C" int flce_bwd(const void* H, const void* W, const void* bias, int dt, 
   return flce_bwd_impl<float>(H, W, bias, N, D, V, labels, ignore_index, reduction,
                               num_label_tokens, lse, n_valid, grad_loss, p, grad_H, grad_W,
                               accumulate_grad_W, grad_bias, w, status, s);
+}
+
+extern "C" size_t flce_fwd_bwd_workspace_bytes(int dt, int64_t N, int64_t D, int64_t V,
+                                               int64_t chunk) {
+  if (!valid_dtype(dt) || N < 1 || V < 1) return 0;
+  return plan(dt, N, D, V, chunk).fused_bytes;
+}
+
+extern "C" int flce_fwd_bwd(const void* H, const void* W, const void* bias, int dt, int64_t N,
+                            int64_t D, int64_t V, const int64_t* labels, int64_t ignore_index,
+                            int reduction, int64_t num_label_tokens, const float* grad_loss,
+                            int64_t chunk, float* loss, int64_t* n_valid, float* lse,
+                            float* loss_rows, void* grad_H, float* grad_W, int accumulate_grad_W,
+                            float* grad_bias, void* ws, size_t ws_bytes, int32_t* status,
+                            flce_stream_t stream) {
+  int rc = flce_checks(H, W, dt, N, D, V, labels, reduction);
+  if (rc != FLCE_OK) return rc;
+  if (loss == nullptr || n_valid == nullptr || lse == nullptr || status == nullptr)
+    return FLCE_EINVAL;
+  if (accumulate_grad_W != 0 && accumulate_grad_W != 1) return FLCE_EINVAL;
+  if (chunk > 0 && chunk % kBM != 0 && chunk < N) return FLCE_ESHAPE;
+  if (bias != nullptr && !aligned(bias, dtype_size(dt))) return FLCE_EALIGN;
+  if (grad_H != nullptr && !aligned(grad_H, 16)) return FLCE_EALIGN;
+  if (grad_W != nullptr && !aligned(grad_W, 16)) return FLCE_EALIGN;
+  if (grad_bias != nullptr && !aligned(grad_bias, 4)) return FLCE_EALIGN;
+  const FlcePlan p = plan(dt, N, D, V, chunk);
+  if (p.nparts > kMaxTilesPerRow) return FLCE_ESHAPE;
+  if (ws == nullptr || ws_bytes < p.fused_bytes) return FLCE_EWORKSPACE;
+  if (!aligned(ws, 256)) return FLCE_EALIGN;
+  rc = bind_context();
+  if (rc != FLCE_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  if (dt == FLCE_BF16)
+    return flce_fused_impl<__nv_bfloat16>(H, W, bias, N, D, V, labels, ignore_index, reduction,
+                                          num_label_tokens, grad_loss, p, loss, n_valid, lse,
+                                          loss_rows, grad_H, grad_W, accumulate_grad_W,
+                                          grad_bias, w, status, s);
+  return flce_fused_impl<float>(H, W, bias, N, D, V, labels, ignore_index, reduction,
+                                num_label_tokens, grad_loss, p, loss, n_valid, lse, loss_rows,
+                                grad_H, grad_W, accumulate_grad_W, grad_bias, w, status, s);
+}
+
+extern "C" int flce_grad_scale(void* x, int dt, int64_t n, const float* g, flce_stream_t stream) {
+  if (!valid_dtype(dt)) return FLCE_EDTYPE;
+  if (n < 0) return FLCE_ESHAPE;
+  if (n == 0) return FLCE_OK;
+  if (x == nullptr || g == nullptr) return FLCE_EINVAL;
+  if (!aligned(x, dtype_size(dt))) return FLCE_EALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int grid = static_cast<int>(std::min<int64_t>((n + 255) / 256, sm_count() * 8));
+  if (dt == FLCE_BF16)
+    scale_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<__nv_bfloat16*>(x), n, g);
+  else
+    scale_kernel<float><<<grid, 256, 0, s>>>(static_cast<float*>(x), n, g);
+  return launch_status("scale_kernel launch");
 }
 
 // ------------------------------------------------------ raw GEMM entry point
