@@ -237,6 +237,13 @@ FLCE_API int flce_fwd_bwd(const void* H, const void* W, const void* bias, int dt
                           float* grad_bias, void* ws, size_t ws_bytes, int32_t* status,
                           flce_stream_t stream);
 
+/* *n_valid = number of labels[0..N) that are not ignore_index and lie in
+ * [0, V) (device pointers).  Data-parallel training sums it over ranks and
+ * passes the total as num_label_tokens, so that the per-rank losses and
+ * gradients add up to those of the global mean. */
+FLCE_API int flce_count_valid(const int64_t* labels, int64_t N, int64_t V, int64_t ignore_index,
+                              int64_t* n_valid, flce_stream_t stream);
+
 /* x[0..n) *= *g for x of dtype dt (device pointers); when *g == 1 nothing is
  * written.  Applies the incoming gradient to gradients computed with g = 1. */
 FLCE_API int flce_grad_scale(void* x, int dt, int64_t n, const float* g, flce_stream_t stream);

@@ -1027,6 +1027,16 @@ extern "C" int flce_fwd_bwd(const void* H, const void* W, const void* bias, int 
                                 grad_H, grad_W, accumulate_grad_W, grad_bias, w, status, s);
 }
 
+extern "C" int flce_count_valid(const int64_t* labels, int64_t N, int64_t V, int64_t ignore_index,
+                                int64_t* n_valid, flce_stream_t stream) {
+  if (N < 0 || V < 1) return FLCE_ESHAPE;
+  if (n_valid == nullptr || (N > 0 && labels == nullptr)) return FLCE_EINVAL;
+  if (!aligned(labels, 8) || !aligned(n_valid, 8)) return FLCE_EALIGN;
+  count_valid_kernel<<<1, 1024, 0, reinterpret_cast<cudaStream_t>(stream)>>>(labels, N, V,
+                                                                          ignore_index, n_valid);
+  return launch_status("count_valid_kernel launch");
+}
+
 extern "C" int flce_grad_scale(void* x, int dt, int64_t n, const float* g, flce_stream_t stream) {
   if (!valid_dtype(dt)) return FLCE_EDTYPE;
   if (n < 0) return FLCE_ESHAPE;
