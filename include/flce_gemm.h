@@ -46,6 +46,10 @@ FLCE_API int flce_gemm(int dt, int a_mn_major, int b_mn_major, int64_t M, int64_
  * not change it while calls run. */
 FLCE_API int flce_gemm_set_pair(int mask);
 
+/* How many CTA pairs of the pair-tiled contraction can be resident at once on
+ * the current device (SMs pair up within a GPC), or -1 on error. */
+FLCE_API int flce_gemm_pair_slots(void);
+
 #ifdef __cplusplus
 }
 #endif

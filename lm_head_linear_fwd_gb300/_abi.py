@@ -49,6 +49,7 @@ _SIGNATURES = {
     "flce_grad_scale": (_i, [_p, _i, _i64, _p, _p]),
     "flce_count_valid": (_i, [_p, _i64, _i64, _i64, _p, _p]),
     "flce_gemm_set_pair": (_i, [_i]),
+    "flce_gemm_pair_slots": (_i, []),
     "flce_gemm": (_i, [_i, _i, _i, _i64, _i64, _i64, _p, _i64, _p, _i64, _p, _i64, _i, _p, _p]),
 }
 
@@ -116,3 +117,4 @@ flce_fwd_bwd = _call("flce_fwd_bwd")
 flce_grad_scale = _call("flce_grad_scale")
 flce_count_valid = _call("flce_count_valid")
 flce_gemm_set_pair = _call("flce_gemm_set_pair")
+flce_gemm_pair_slots = _call("flce_gemm_pair_slots")

@@ -356,7 +356,43 @@ __global__ void __launch_bounds__(kStreamThreads) ce_stream_kernel(const StreamA
         const int nvec = static_cast<int>(
             min(static_cast<int64_t>(kSegBytes), row_bytes - static_cast<int64_t>(sg) * kSegBytes) / 16);
         const uint4* sv = reinterpret_cast<const uint4*>(ring + stage * kSegBytes);
-        if (!kBwd) {
+        if (!kBwd && sizeof(T) == 2) {
+          // bf16: the batch maximum on packed pairs (exact), then one FFMA,
+          // one ex2 and one add per element
+          uint4 u[kVecPerThread];
+          __nv_bfloat162 mx = __float2bfloat162_rn(-INFINITY);
+#pragma unroll
+          for (int k = 0; k < kVecPerThread; ++k) {
+            const int v = tid + k * kConsumers;
+            if (v < nvec) {
+              u[k] = sv[v];
+              mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&u[k].x));
+              mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&u[k].y));
+              mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&u[k].z));
+              mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&u[k].w));
+            }
+          }
+          const float bm =
+              fmaxf(__low2float(mx), __high2float(mx)) * kLog2e;  // monotone: max of x*log2e
+          if (bm > st.m) {
+            st.s *= ex2(st.m - bm);
+            st.m = bm;
+          }
+          if (st.m != -INFINITY) {
+            float acc = 0.0f;
+#pragma unroll
+            for (int k = 0; k < kVecPerThread; ++k) {
+              const int v = tid + k * kConsumers;
+              if (v < nvec) {
+                float x[EPV];
+                Elem<T>::unpack(u[k], x);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) acc += ex2(fmaf(x[e], kLog2e, -st.m));
+              }
+            }
+            st.s += acc;
+          }
+        } else if (!kBwd) {
           float t[kVecPerThread * EPV];
 #pragma unroll
           for (int k = 0; k < kVecPerThread; ++k) {
@@ -381,11 +417,18 @@ __global__ void __launch_bounds__(kStreamThreads) ce_stream_kernel(const StreamA
               float x[EPV];
               Elem<T>::unpack(sv[v], x);
               const int64_t j0 = static_cast<int64_t>(v) * EPV;
+              if (c == 0.0f) {
 #pragma unroll
-              for (int e = 0; e < EPV; ++e)
-                x[e] = (c == 0.0f) ? 0.0f
-                                   : (ex2(fmaf(x[e], kLog2e, -lse2)) -
-                                      (j0 + e == ylocal ? 1.0f : 0.0f)) * c;
+                for (int e = 0; e < EPV; ++e) x[e] = 0.0f;
+              } else {
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) x[e] = ex2(fmaf(x[e], kLog2e, -lse2)) * c;
+                if (static_cast<uint64_t>(ylocal - j0) < static_cast<uint64_t>(EPV)) {
+#pragma unroll
+                  for (int e = 0; e < EPV; ++e)
+                    if (j0 + e == ylocal) x[e] -= c;  // the one-hot label term
+                }
+              }
               __stcs(reinterpret_cast<uint4*>(out + e0) + v, Elem<T>::pack(x));
             }
           }

@@ -547,7 +547,7 @@ static int launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const 
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // as many pairs as can be resident at once (SMs of a GPC pair up; an odd one idles)
+  // as many pairs as can be resident at once (on GB300 all 152 SMs pair up: 76)
   int max_pairs = 0;
   cfg.gridDim = dim3(2 * static_cast<unsigned>(std::min(tiles, sm_count() / 2)), 1, 1);
   rc = cuda_status(cudaOccupancyMaxActiveClusters(&max_pairs, kern, &cfg),
@@ -1055,6 +1055,30 @@ extern "C" int flce_grad_scale(void* x, int dt, int64_t n, const float* g, flce_
 // ------------------------------------------------------ raw GEMM entry point
 
 extern "C" int flce_gemm_set_pair(int mask) { return g_pair_mask.exchange(mask & 31); }
+
+extern "C" int flce_gemm_pair_slots(void) {
+  using E = EpiStore<float, true>;
+  auto kern = tc_gemm_pair_kernel<256, false, false, E>;
+  using G = PairGeo<256>;
+  if (bind_context() != FLCE_OK) return -1;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes) !=
+      cudaSuccess)
+    return -1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = G::kSmemBytes;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return -1;
+  return n;
+}
 
 extern "C" int flce_gemm(int dt, int a_mn_major, int b_mn_major, int64_t M, int64_t N, int64_t K,
                          const void* A, int64_t lda, const void* B, int64_t ldb, float* C,
