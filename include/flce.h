@@ -121,6 +121,16 @@ FLCE_API int ce_logits_fwd(const void* logits, int dt, int64_t N, int64_t V, int
                   float* loss_rows, float* label_logit, void* ws, size_t ws_bytes,
                   int32_t* status, flce_stream_t stream);
 
+/* Label masking for packed sequences: labels and doc_ids are [B, T] int64
+ * (device, row-major); doc_ids holds 1, 2, ... for the packed documents of a
+ * row and 0 for padding (the indexed packing mask of Automodel PR #2996,
+ * "fix(models): preserve indexed packing masks").  In place, labels[b, t]
+ * becomes ignore_index where doc_ids[b, t] == 0 or where position t is the
+ * last of its document (the next token belongs to another document, or the
+ * row ends); other labels are left as they are. */
+FLCE_API int flce_mask_packed_labels(int64_t* labels, const int64_t* doc_ids, int64_t B,
+                                     int64_t T, int64_t ignore_index, flce_stream_t stream);
+
 /* Largest N ce_logits_fwd_noalloc accepts. */
 #define CE_LOGITS_NOALLOC_MAX_ROWS (1 << 20)
 

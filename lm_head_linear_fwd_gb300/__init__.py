@@ -12,6 +12,6 @@ _abi.load()
 from .api import (  # noqa: E402,F401
     BackwardOut, ForwardOut, ce_logits, ce_logits_bwd, ce_logits_fwd,
     ce_logits_workspace_bytes, check_status, flce, flce_bwd, flce_default_chunk, flce_fwd,
-    flce_fwd_bwd, flce_gemm, flce_workspace_bytes, grad_scale_, new_status,
+    flce_fwd_bwd, flce_gemm, flce_workspace_bytes, grad_scale_, mask_packed_labels, new_status,
 )
 from ._abi import FlceError  # noqa: E402,F401

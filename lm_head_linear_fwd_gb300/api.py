@@ -192,6 +192,25 @@ def ce_logits(logits, labels, *, ignore_index=-100, reduction="sum", num_label_t
                            bool(inplace_grad))
 
 
+def mask_packed_labels(labels: torch.Tensor, doc_ids: torch.Tensor, ignore_index: int = -100):
+    """In place: labels [B, T] become ignore_index on padding (doc id 0) and on
+    the last token of every packed document (see flce_mask_packed_labels)."""
+    _cuda(labels, "labels")
+    _cuda(doc_ids, "doc_ids")
+    if labels.shape != doc_ids.shape or labels.dim() != 2:
+        raise ValueError("labels and doc_ids must both be [B, T]")
+    if labels.dtype != torch.int64 or doc_ids.dtype != torch.int64:
+        raise TypeError("labels and doc_ids must be int64")
+    if not labels.is_contiguous():
+        raise ValueError("labels must be contiguous (it is written in place)")
+    doc_ids = doc_ids.contiguous()
+    B, T = labels.shape
+    rc = _abi.flce_mask_packed_labels(_ptr(labels), _ptr(doc_ids), B, T, int(ignore_index),
+                                      _stream(labels.device))
+    _abi.check(rc, "flce_mask_packed_labels")
+    return labels
+
+
 # ---------------------------------------------------------- fused linear CE
 
 def flce_workspace_bytes(dt_code: int, N: int, D: int, V: int, chunk: int = 0) -> int:

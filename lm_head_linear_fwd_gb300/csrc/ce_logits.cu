@@ -18,6 +18,7 @@
 #include <math.h>
 #include <stdio.h>
 
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -609,6 +610,38 @@ extern "C" int ce_logits_fwd(const void* logits, int dt, int64_t N, int64_t V, i
   }
   return launch_finalize(rows, labels, N, V, ignore_index, reduction, num_label_tokens, loss,
                          n_valid, s);
+}
+
+// ------------------------------------------------- packed-document labels
+
+// labels[b, t] = ignore_index where doc[b, t] == 0 (padding) or where the next
+// position belongs to another document (doc[b, t+1] != doc[b, t]) or the row
+// ends; doc holds 1, 2, ... per packed document and 0 for padding.
+__global__ void __launch_bounds__(256) packed_labels_kernel(int64_t* __restrict__ labels,
+                                                            const int64_t* __restrict__ doc,
+                                                            int64_t B, int64_t T,
+                                                            int64_t ignore_index) {
+  const int64_t n = B * T;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = i % T;
+    const int64_t d = doc[i];
+    const bool last = (t == T - 1) || (doc[i + 1] != d);
+    if (d == 0 || last) labels[i] = ignore_index;
+  }
+}
+
+extern "C" int flce_mask_packed_labels(int64_t* labels, const int64_t* doc_ids, int64_t B,
+                                       int64_t T, int64_t ignore_index, flce_stream_t stream) {
+  if (B < 0 || T < 0) return FLCE_ESHAPE;
+  if (B == 0 || T == 0) return FLCE_OK;
+  if (labels == nullptr || doc_ids == nullptr) return FLCE_EINVAL;
+  if (!aligned(labels, 8) || !aligned(doc_ids, 8)) return FLCE_EALIGN;
+  const int64_t n = B * T;
+  const int grid = static_cast<int>(std::min<int64_t>((n + 255) / 256, sm_count() * 8));
+  packed_labels_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      labels, doc_ids, B, T, ignore_index);
+  return launch_status("packed_labels_kernel launch");
 }
 
 // ------------------------------------------------- allocation-free forward

@@ -39,3 +39,27 @@ def test_shards_add_up_to_the_global_mean():
     torch.cuda.synchronize()
     assert abs(loss - full_o.loss.item()) <= 1e-5 * abs(full_o.loss.item())
     assert oracle.normwise_err(gW.cpu(), full_b.grad_W.cpu().double().numpy()) <= 1e-5
+
+
+def test_mask_packed_labels_matches_the_workload_recipe():
+    """The kernel reproduces the long packed workload's masking: padding tail
+    and last token of each document ignored."""
+    import lm_head_linear_fwd_gb300 as lh
+    B, T, V = 4, 4096, 151936
+    doc = torch.zeros(B, T, dtype=torch.int64)
+    rng = torch.Generator().manual_seed(7)
+    pad = 327
+    ref = torch.randint(0, V, (B, T), generator=rng)
+    labels = ref.clone()
+    for r in range(B):
+        cuts = sorted((torch.randperm(T - pad - 2, generator=rng)[:3] + 1).tolist())
+        ends = cuts + [T - pad]
+        start = 0
+        for k, e in enumerate(ends):
+            doc[r, start:e] = k + 1
+            ref[r, e - 1] = -100
+            start = e
+        ref[r, T - pad:] = -100
+    out = lh.mask_packed_labels(labels.cuda(), doc.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu(), ref)
