@@ -220,6 +220,56 @@ FLCE_API int flce_bwd(const void* H, const void* W, const void* bias, int dt, in
              int32_t* status, flce_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Vocabulary-parallel fused linear cross-entropy                           */
+/* ------------------------------------------------------------------------ */
+/* "Loss Parallel" of torchtitan PR #996 (review: TP with Loss Parallel): each
+ * rank holds rows [vocab_offset, vocab_offset + V_shard) of W (and of the
+ * bias) and all of H and the labels (global ids in [0, V_total)).  A forward
+ * step is:
+ *   1. flce_fwd_shard     per row: m, s = base-2 max and sum of 2^(z*log2e - m)
+ *                         over the shard's columns; zy = the label logit if the
+ *                         label lies in the shard, else 0
+ *   2. all-reduce MAX of m over the ranks                     -> m_global
+ *   3. flce_shard_rescale s_scaled = s * 2^(m - m_global)
+ *   4. all-reduce SUM of s_scaled and of zy                   -> s_global, zy_global
+ *   5. flce_shard_finish  lse = (m_global + log2 s_global) ln 2, loss rows,
+ *                         reduction (identical on every rank)
+ * and the backward is flce_bwd_shard with the global lse (the shard's columns
+ * of dZ), followed by an all-reduce SUM of the grad_H partials; grad_W and
+ * grad_bias stay with their shard.  Workspaces: flce_workspace_bytes(dt, N, D,
+ * V_shard, chunk).  The collectives are the caller's (e.g. NCCL). */
+FLCE_API int flce_fwd_shard(const void* H, const void* W_shard, const void* bias_shard, int dt,
+                            int64_t N, int64_t D, int64_t V_shard, int64_t vocab_offset,
+                            int64_t V_total, const int64_t* labels, int64_t ignore_index,
+                            float* m_local, float* s_local, float* zy_local, void* ws,
+                            size_t ws_bytes, int32_t* status, flce_stream_t stream);
+
+/* s_scaled[i] = s_local[i] * 2^(m_local[i] - m_global[i]) (0 when m_local[i] is -inf). */
+FLCE_API int flce_shard_rescale(const float* m_local, const float* s_local,
+                                const float* m_global, int64_t N, float* s_scaled,
+                                flce_stream_t stream);
+
+/* lse, per-row loss (loss_rows may be NULL: ws then needs 4N bytes rounded up
+ * to 256) and the reduced loss and n_valid from the reduced m, s and zy. */
+FLCE_API int flce_shard_finish(const float* m_global, const float* s_global,
+                               const float* zy_global, const int64_t* labels, int64_t N,
+                               int64_t V_total, int64_t ignore_index, int reduction,
+                               int64_t num_label_tokens, float* lse, float* loss_rows,
+                               float* loss, int64_t* n_valid, void* ws, size_t ws_bytes,
+                               int32_t* status, flce_stream_t stream);
+
+/* Backward of one shard: as flce_bwd over the shard's columns, with the
+ * global lse and n_valid; grad_H_partial is this shard's term of grad_H. */
+FLCE_API int flce_bwd_shard(const void* H, const void* W_shard, const void* bias_shard, int dt,
+                            int64_t N, int64_t D, int64_t V_shard, int64_t vocab_offset,
+                            int64_t V_total, const int64_t* labels, int64_t ignore_index,
+                            int reduction, int64_t num_label_tokens, const float* lse,
+                            const int64_t* n_valid, const float* grad_loss, int64_t chunk,
+                            void* grad_H_partial, float* grad_W_shard, int accumulate_grad_W,
+                            float* grad_bias_shard, void* ws, size_t ws_bytes, int32_t* status,
+                            flce_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Fused linear cross-entropy, forward and backward in one call             */
 /* ------------------------------------------------------------------------ */
 

@@ -43,6 +43,13 @@ _SIGNATURES = {
                       _p, _sz, _p, _p]),
     "flce_bwd": (_i, [_p, _p, _p, _i, _i64, _i64, _i64, _p, _i64, _i, _i64, _p, _p, _p, _i64,
                       _p, _p, _i, _p, _p, _sz, _p, _p]),
+    "flce_fwd_shard": (_i, [_p, _p, _p, _i, _i64, _i64, _i64, _i64, _i64, _p, _i64, _p, _p, _p,
+                            _p, _sz, _p, _p]),
+    "flce_shard_rescale": (_i, [_p, _p, _p, _i64, _p, _p]),
+    "flce_shard_finish": (_i, [_p, _p, _p, _p, _i64, _i64, _i64, _i, _i64, _p, _p, _p, _p, _p,
+                               _sz, _p, _p]),
+    "flce_bwd_shard": (_i, [_p, _p, _p, _i, _i64, _i64, _i64, _i64, _i64, _p, _i64, _i, _i64, _p,
+                            _p, _p, _i64, _p, _p, _i, _p, _p, _sz, _p, _p]),
     "flce_fwd_bwd_workspace_bytes": (_sz, [_i, _i64, _i64, _i64, _i64]),
     "flce_fwd_bwd": (_i, [_p, _p, _p, _i, _i64, _i64, _i64, _p, _i64, _i, _i64, _p, _i64, _p, _p,
                           _p, _p, _p, _p, _i, _p, _p, _sz, _p, _p]),
@@ -114,6 +121,10 @@ flce_fwd = _call("flce_fwd")
 flce_bwd = _call("flce_bwd")
 flce_gemm = _call("flce_gemm")
 flce_fwd_bwd_workspace_bytes = _call("flce_fwd_bwd_workspace_bytes")
+flce_fwd_shard = _call("flce_fwd_shard")
+flce_shard_rescale = _call("flce_shard_rescale")
+flce_shard_finish = _call("flce_shard_finish")
+flce_bwd_shard = _call("flce_bwd_shard")
 flce_fwd_bwd = _call("flce_fwd_bwd")
 flce_grad_scale = _call("flce_grad_scale")
 flce_count_valid = _call("flce_count_valid")

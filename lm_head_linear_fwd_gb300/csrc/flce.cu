@@ -48,11 +48,12 @@ struct EpiLse {
     const void* bias;  // [V] of T or null
     const int64_t* labels;
     int64_t ignore_index;
-    int M, V;
+    int M, V;          // V: columns of this (shard of the) vocabulary
     int64_t part_ld;   // row stride of part_m / part_s (>= M)
     float* part_m;     // [nNt, part_ld], base-2 max
     float* part_s;     // [nNt, part_ld], sum of 2^(t - max)
     float* zlab;       // [M] label logit (written by the tile holding the label)
+    int64_t v0;        // vocabulary id of this shard's column 0 (0 unsharded)
   };
   template <int BN>
   __device__ static void tile(const Params& p, int mt, int nt, int row_in_tile, uint32_t taddr,
@@ -61,7 +62,7 @@ struct EpiLse {
     const bool row_ok = row < p.M;
     const int64_t y = row_ok ? p.labels[row] : -1;
     const int col_base = nt * BN;
-    const int64_t ylocal = y - col_base;
+    const int64_t ylocal = (y < 0) ? -1 : (y - p.v0) - col_base;
     Lse2 st;
     float zy = 0.0f;
 #pragma unroll 1
@@ -107,7 +108,7 @@ struct EpiLseStore {
     const bool row_ok = row < p.M;
     const int64_t y = row_ok ? p.labels[row] : -1;
     const int col_base = nt * BN;
-    const int64_t ylocal = y - col_base;
+    const int64_t ylocal = (y < 0) ? -1 : (y - p.v0) - col_base;
     const int r0 = mt * kBM + (row_in_tile & ~31);
     float m = -INFINITY, zy = 0.0f;
 #pragma unroll 1
@@ -174,7 +175,9 @@ struct EpiDlogits {
     int64_t num_label_tokens;
     const int64_t* n_valid;
     const float* grad_loss;
-    int M, V;               // M = rows in this chunk
+    int M, V;               // M = rows in this chunk; V = columns of this shard
+    int64_t v0;             // vocabulary id of this shard's column 0
+    int64_t V_total;        // vocabulary size (labels are checked against it)
   };
   template <int BN>
   __device__ static void tile(const Params& p, int mt, int nt, int row_in_tile, uint32_t taddr,
@@ -184,12 +187,12 @@ struct EpiDlogits {
     const int row = mt * kBM + row_in_tile;
     const bool row_ok = row < p.M;
     const int64_t y = row_ok ? p.labels[row] : p.ignore_index;
-    const bool valid = row_ok && y != p.ignore_index && label_ok(y, p.V);
+    const bool valid = row_ok && y != p.ignore_index && label_ok(y, p.V_total);
     const float c = valid ? grad_coef(p.reduction, p.num_label_tokens, p.n_valid, p.grad_loss)
                           : 0.0f;
     const float lse2 = row_ok ? p.lse[row] * kLog2e : 0.0f;
     const int col_base = nt * BN;
-    const int64_t ylocal = y - col_base;
+    const int64_t ylocal = valid ? (y - p.v0) - col_base : -1;
     const int r0 = mt * kBM + (row_in_tile & ~31);
 #pragma unroll 1
     for (int g = 0; g < BN / CPS; ++g) {
@@ -285,6 +288,57 @@ __global__ void __launch_bounds__(256) lse_combine_kernel(
   }
   loss_rows[row] = li;
   if (label_logit != nullptr) label_logit[row] = zy;
+}
+
+// Vocabulary-parallel forward: merges this shard's tile partials of each row
+// into (m, s) (base-2 max and sum over the shard's columns) and the label logit
+// when the label lies in the shard (0 otherwise).
+__global__ void __launch_bounds__(256) shard_combine_kernel(
+    const float* __restrict__ part_m, const float* __restrict__ part_s, int nparts,
+    int64_t part_ld, const float* __restrict__ zlab, const int64_t* __restrict__ labels,
+    int64_t N, int64_t V_shard, int64_t v0, int64_t ignore_index, float* __restrict__ m_out,
+    float* __restrict__ s_out, float* __restrict__ zy_out) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (row >= N) return;
+  Lse2 st;
+  for (int p = 0; p < nparts; ++p) st.merge(part_m[p * part_ld + row], part_s[p * part_ld + row]);
+  m_out[row] = st.m;
+  s_out[row] = st.s;
+  const int64_t y = labels[row];
+  const bool in_shard = y != ignore_index && y >= v0 && y < v0 + V_shard;
+  zy_out[row] = in_shard ? zlab[row] : 0.0f;
+}
+
+// s_scaled = s * 2^(m - m_global): a shard's sum expressed relative to the
+// maximum over all shards (0 when the shard's maximum is -inf).
+__global__ void __launch_bounds__(256) shard_rescale_kernel(const float* __restrict__ m,
+                                                            const float* __restrict__ s,
+                                                            const float* __restrict__ m_global,
+                                                            int64_t N, float* __restrict__ out) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= N) return;
+  out[i] = (m[i] == -INFINITY) ? 0.0f : s[i] * ex2(m[i] - m_global[i]);
+}
+
+// lse = (M + log2 S) ln 2 from the global (M, S); loss_i = valid (lse - z_y).
+__global__ void __launch_bounds__(256) shard_finish_kernel(
+    const float* __restrict__ m_global, const float* __restrict__ s_global,
+    const float* __restrict__ zy_global, const int64_t* __restrict__ labels, int64_t N,
+    int64_t V_total, int64_t ignore_index, float* __restrict__ lse_out,
+    float* __restrict__ loss_rows, int32_t* status) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= N) return;
+  const float lse = m_global[i] * kLn2 + logf(s_global[i]);
+  lse_out[i] = lse;
+  const int64_t y = labels[i];
+  float li = 0.0f;
+  if (y != ignore_index) {
+    if (label_ok(y, V_total))
+      li = lse - zy_global[i];
+    else
+      set_status(status, FLCE_ELABEL);
+  }
+  loss_rows[i] = li;
 }
 
 constexpr int kColSplits = 16;
@@ -738,6 +792,33 @@ extern "C" size_t flce_workspace_bytes(int dt, int64_t N, int64_t D, int64_t V, 
   return plan(dt, N, D, V, chunk).total;
 }
 
+// Forward contraction of one (shard of the) vocabulary: per (row, 256-column
+// tile) partials and the label logit into the workspace.  v0 is the vocabulary
+// id of W's row 0 (0 unsharded).
+static int fwd_gemm(const void* H, const void* W, const void* bias, int dt, int64_t N, int64_t D,
+                    int64_t V, int64_t v0, const int64_t* labels, int64_t ignore_index,
+                    const FlcePlan& p, char* w, int32_t* status, cudaStream_t s) {
+  float* part_m = reinterpret_cast<float*>(w + p.off_part_m);
+  float* part_s = reinterpret_cast<float*>(w + p.off_part_s);
+  float* zlab = reinterpret_cast<float*>(w + p.off_zlab);
+  const Operand a{H, N, D, D, false};
+  const Operand b{W, V, D, D, false};
+  const int group = group_for(D, dt, static_cast<int>((N + kBM - 1) / kBM));
+  if (dt == FLCE_BF16) {
+    using E = EpiLse<__nv_bfloat16>;
+    E::Params ep{bias, labels, ignore_index, static_cast<int>(N), static_cast<int>(V),
+                 p.part_ld, part_m, part_s, zlab, v0};
+    return launch_gemm<__nv_bfloat16, kBNFwd, false, false, E>(kRoleFwd, a, b, nullptr, (int)N,
+                                                               (int)V, (int)D, group, ep, status,
+                                                               s);
+  }
+  using E = EpiLse<float>;
+  E::Params ep{bias, labels, ignore_index, static_cast<int>(N), static_cast<int>(V), p.part_ld,
+               part_m, part_s, zlab, v0};
+  return launch_gemm<float, kBNFwd, false, false, E>(kRoleFwd, a, b, nullptr, (int)N, (int)V,
+                                                     (int)D, group, ep, status, s);
+}
+
 extern "C" int flce_fwd(const void* H, const void* W, const void* bias, int dt, int64_t N,
                         int64_t D, int64_t V, const int64_t* labels, int64_t ignore_index,
                         int reduction, int64_t num_label_tokens, float* loss, int64_t* n_valid,
@@ -754,36 +835,86 @@ extern "C" int flce_fwd(const void* H, const void* W, const void* bias, int dt, 
   rc = bind_context();
   if (rc != FLCE_OK) return rc;
   char* w = static_cast<char*>(ws);
-  float* part_m = reinterpret_cast<float*>(w + p.off_part_m);
-  float* part_s = reinterpret_cast<float*>(w + p.off_part_s);
-  float* zlab = reinterpret_cast<float*>(w + p.off_zlab);
   float* rows = loss_rows != nullptr ? loss_rows : reinterpret_cast<float*>(w + p.off_rows);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-
-  const Operand a{H, N, D, D, false};
-  const Operand b{W, V, D, D, false};
-  const int group = group_for(D, dt, static_cast<int>((N + kBM - 1) / kBM));
-  if (dt == FLCE_BF16) {
-    using E = EpiLse<__nv_bfloat16>;
-    E::Params ep{bias, labels, ignore_index, static_cast<int>(N), static_cast<int>(V),
-                 p.part_ld, part_m, part_s, zlab};
-    rc = launch_gemm<__nv_bfloat16, kBNFwd, false, false, E>(kRoleFwd, a, b, nullptr, (int)N, (int)V,
-                                                             (int)D, group, ep, status, s);
-  } else {
-    using E = EpiLse<float>;
-    E::Params ep{bias, labels, ignore_index, static_cast<int>(N), static_cast<int>(V),
-                 p.part_ld, part_m, part_s, zlab};
-    rc = launch_gemm<float, kBNFwd, false, false, E>(kRoleFwd, a, b, nullptr, (int)N, (int)V, (int)D, group,
-                                                     ep, status, s);
-  }
+  rc = fwd_gemm(H, W, bias, dt, N, D, V, 0, labels, ignore_index, p, w, status, s);
   if (rc != FLCE_OK) return rc;
   lse_combine_kernel<<<static_cast<unsigned>((N + 255) / 256), 256, 0, s>>>(
-      part_m, part_s, p.nparts, p.part_ld, zlab, labels, N, V, ignore_index, lse, rows,
-      label_logit, status);
+      reinterpret_cast<float*>(w + p.off_part_m), reinterpret_cast<float*>(w + p.off_part_s),
+      p.nparts, p.part_ld, reinterpret_cast<float*>(w + p.off_zlab), labels, N, V, ignore_index,
+      lse, rows, label_logit, status);
   rc = launch_status("lse_combine_kernel launch");
   if (rc != FLCE_OK) return rc;
   return launch_finalize(rows, labels, N, V, ignore_index, reduction, num_label_tokens, loss,
                          n_valid, s);
+}
+
+extern "C" int flce_fwd_shard(const void* H, const void* W_shard, const void* bias_shard, int dt,
+                              int64_t N, int64_t D, int64_t V_shard, int64_t vocab_offset,
+                              int64_t V_total, const int64_t* labels, int64_t ignore_index,
+                              float* m_local, float* s_local, float* zy_local, void* ws,
+                              size_t ws_bytes, int32_t* status, flce_stream_t stream) {
+  int rc = flce_checks(H, W_shard, dt, N, D, V_shard, labels, FLCE_SUM);
+  if (rc != FLCE_OK) return rc;
+  if (vocab_offset < 0 || V_total < vocab_offset + V_shard || V_total >= (int64_t(1) << 31))
+    return FLCE_ESHAPE;
+  if (m_local == nullptr || s_local == nullptr || zy_local == nullptr || status == nullptr)
+    return FLCE_EINVAL;
+  if (bias_shard != nullptr && !aligned(bias_shard, dtype_size(dt))) return FLCE_EALIGN;
+  const FlcePlan p = plan(dt, N, D, V_shard, 0);
+  if (ws == nullptr || ws_bytes < p.fwd_bytes) return FLCE_EWORKSPACE;
+  if (!aligned(ws, 256)) return FLCE_EALIGN;
+  rc = bind_context();
+  if (rc != FLCE_OK) return rc;
+  char* w = static_cast<char*>(ws);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  rc = fwd_gemm(H, W_shard, bias_shard, dt, N, D, V_shard, vocab_offset, labels, ignore_index, p,
+                w, status, s);
+  if (rc != FLCE_OK) return rc;
+  shard_combine_kernel<<<static_cast<unsigned>((N + 255) / 256), 256, 0, s>>>(
+      reinterpret_cast<float*>(w + p.off_part_m), reinterpret_cast<float*>(w + p.off_part_s),
+      p.nparts, p.part_ld, reinterpret_cast<float*>(w + p.off_zlab), labels, N, V_shard,
+      vocab_offset, ignore_index, m_local, s_local, zy_local);
+  return launch_status("shard_combine_kernel launch");
+}
+
+extern "C" int flce_shard_rescale(const float* m_local, const float* s_local,
+                                  const float* m_global, int64_t N, float* s_scaled,
+                                  flce_stream_t stream) {
+  if (N < 0) return FLCE_ESHAPE;
+  if (N == 0) return FLCE_OK;
+  if (m_local == nullptr || s_local == nullptr || m_global == nullptr || s_scaled == nullptr)
+    return FLCE_EINVAL;
+  shard_rescale_kernel<<<static_cast<unsigned>((N + 255) / 256), 256, 0,
+                         reinterpret_cast<cudaStream_t>(stream)>>>(m_local, s_local, m_global, N,
+                                                                   s_scaled);
+  return launch_status("shard_rescale_kernel launch");
+}
+
+extern "C" int flce_shard_finish(const float* m_global, const float* s_global,
+                                 const float* zy_global, const int64_t* labels, int64_t N,
+                                 int64_t V_total, int64_t ignore_index, int reduction,
+                                 int64_t num_label_tokens, float* lse, float* loss_rows,
+                                 float* loss, int64_t* n_valid, void* ws, size_t ws_bytes,
+                                 int32_t* status, flce_stream_t stream) {
+  if (!valid_reduction(reduction)) return FLCE_EINVAL;
+  if (N < 1 || V_total < 1 || V_total >= (int64_t(1) << 31)) return FLCE_ESHAPE;
+  if (m_global == nullptr || s_global == nullptr || zy_global == nullptr || labels == nullptr ||
+      lse == nullptr || loss == nullptr || n_valid == nullptr || status == nullptr)
+    return FLCE_EINVAL;
+  float* rows = loss_rows;
+  if (rows == nullptr) {
+    if (ws == nullptr || ws_bytes < round_up(static_cast<size_t>(N) * 4, 256))
+      return FLCE_EWORKSPACE;
+    rows = static_cast<float*>(ws);
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  shard_finish_kernel<<<static_cast<unsigned>((N + 255) / 256), 256, 0, s>>>(
+      m_global, s_global, zy_global, labels, N, V_total, ignore_index, lse, rows, status);
+  int rc = launch_status("shard_finish_kernel launch");
+  if (rc != FLCE_OK) return rc;
+  return launch_finalize(rows, labels, N, V_total, ignore_index, reduction, num_label_tokens,
+                         loss, n_valid, s);
 }
 
 // Steps 2-4 of a backward chunk, shared by flce_bwd and flce_fwd_bwd: bias
@@ -863,7 +994,8 @@ static int transpose_W_if_needed(const void* W, int64_t D, int64_t V, const Flce
 
 template <typename T>
 static int flce_bwd_impl(const void* H, const void* W, const void* bias, int64_t N, int64_t D,
-                         int64_t V, const int64_t* labels, int64_t ignore_index, int reduction,
+                         int64_t V, int64_t v0, int64_t V_total, const int64_t* labels,
+                         int64_t ignore_index, int reduction,
                          int64_t num_label_tokens, const float* lse, const int64_t* n_valid,
                          const float* grad_loss, const FlcePlan& p, void* grad_H,
                          float* grad_W, int accumulate_grad_W, float* grad_bias, char* w,
@@ -879,7 +1011,8 @@ static int flce_bwd_impl(const void* H, const void* W, const void* bias, int64_t
     // 1. recompute logits, form dZ
     using E = EpiDlogits<T>;
     typename E::Params ep{bias, labels + r0, ignore_index, lse + r0, reduction,
-                          num_label_tokens, n_valid, grad_loss, C, static_cast<int>(V)};
+                          num_label_tokens, n_valid, grad_loss, C, static_cast<int>(V), v0,
+                          V_total};
     const Operand a{Ht + r0 * D, C, D, D, false};
     const Operand b{W, V, D, D, false};
     const OutDesc o{dz, dt, C, V, p.ldV};
@@ -953,14 +1086,16 @@ static int flce_fused_impl(const void* H, const void* W, const void* bias, int64
                          n_valid, s);
 }
 
-extern "C" int flce_bwd(const void* H, const void* W, const void* bias, int dt, int64_t N,
-                        int64_t D, int64_t V, const int64_t* labels, int64_t ignore_index,
-                        int reduction, int64_t num_label_tokens, const float* lse,
-                        const int64_t* n_valid, const float* grad_loss, int64_t chunk,
-                        void* grad_H, float* grad_W, int accumulate_grad_W, float* grad_bias,
-                        void* ws, size_t ws_bytes, int32_t* status, flce_stream_t stream) {
+static int flce_bwd_entry(const void* H, const void* W, const void* bias, int dt, int64_t N,
+                          int64_t D, int64_t V, int64_t v0, int64_t V_total,
+                          const int64_t* labels, int64_t ignore_index, int reduction,
+                          int64_t num_label_tokens, const float* lse, const int64_t* n_valid,
+                          const float* grad_loss, int64_t chunk, void* grad_H, float* grad_W,
+                          int accumulate_grad_W, float* grad_bias, void* ws, size_t ws_bytes,
+                          int32_t* status, flce_stream_t stream) {
   int rc = flce_checks(H, W, dt, N, D, V, labels, reduction);
   if (rc != FLCE_OK) return rc;
+  if (v0 < 0 || V_total < v0 + V || V_total >= (int64_t(1) << 31)) return FLCE_ESHAPE;
   if (lse == nullptr || n_valid == nullptr || grad_loss == nullptr || status == nullptr)
     return FLCE_EINVAL;
   if (accumulate_grad_W != 0 && accumulate_grad_W != 1) return FLCE_EINVAL;
@@ -978,12 +1113,38 @@ extern "C" int flce_bwd(const void* H, const void* W, const void* bias, int dt, 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
   if (dt == FLCE_BF16)
-    return flce_bwd_impl<__nv_bfloat16>(H, W, bias, N, D, V, labels, ignore_index, reduction,
-                                        num_label_tokens, lse, n_valid, grad_loss, p, grad_H,
-                                        grad_W, accumulate_grad_W, grad_bias, w, status, s);
-  return flce_bwd_impl<float>(H, W, bias, N, D, V, labels, ignore_index, reduction,
+    return flce_bwd_impl<__nv_bfloat16>(H, W, bias, N, D, V, v0, V_total, labels, ignore_index,
+                                        reduction, num_label_tokens, lse, n_valid, grad_loss, p,
+                                        grad_H, grad_W, accumulate_grad_W, grad_bias, w, status,
+                                        s);
+  return flce_bwd_impl<float>(H, W, bias, N, D, V, v0, V_total, labels, ignore_index, reduction,
                               num_label_tokens, lse, n_valid, grad_loss, p, grad_H, grad_W,
                               accumulate_grad_W, grad_bias, w, status, s);
+}
+
+extern "C" int flce_bwd(const void* H, const void* W, const void* bias, int dt, int64_t N,
+                        int64_t D, int64_t V, const int64_t* labels, int64_t ignore_index,
+                        int reduction, int64_t num_label_tokens, const float* lse,
+                        const int64_t* n_valid, const float* grad_loss, int64_t chunk,
+                        void* grad_H, float* grad_W, int accumulate_grad_W, float* grad_bias,
+                        void* ws, size_t ws_bytes, int32_t* status, flce_stream_t stream) {
+  return flce_bwd_entry(H, W, bias, dt, N, D, V, 0, V, labels, ignore_index, reduction,
+                        num_label_tokens, lse, n_valid, grad_loss, chunk, grad_H, grad_W,
+                        accumulate_grad_W, grad_bias, ws, ws_bytes, status, stream);
+}
+
+extern "C" int flce_bwd_shard(const void* H, const void* W_shard, const void* bias_shard,
+                              int dt, int64_t N, int64_t D, int64_t V_shard,
+                              int64_t vocab_offset, int64_t V_total, const int64_t* labels,
+                              int64_t ignore_index, int reduction, int64_t num_label_tokens,
+                              const float* lse, const int64_t* n_valid, const float* grad_loss,
+                              int64_t chunk, void* grad_H_partial, float* grad_W_shard,
+                              int accumulate_grad_W, float* grad_bias_shard, void* ws,
+                              size_t ws_bytes, int32_t* status, flce_stream_t stream) {
+  return flce_bwd_entry(H, W_shard, bias_shard, dt, N, D, V_shard, vocab_offset, V_total, labels,
+                        ignore_index, reduction, num_label_tokens, lse, n_valid, grad_loss,
+                        chunk, grad_H_partial, grad_W_shard, accumulate_grad_W, grad_bias_shard,
+                        ws, ws_bytes, status, stream);
 }
 
 extern "C" size_t flce_fwd_bwd_workspace_bytes(int dt, int64_t N, int64_t D, int64_t V,
