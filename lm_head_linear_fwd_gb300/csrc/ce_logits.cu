@@ -19,6 +19,7 @@
 #include <stdio.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -479,10 +480,18 @@ __global__ void __launch_bounds__(kStreamThreads) ce_stream_kernel(const StreamA
 template <typename T, bool kBwd>
 static int launch_stream(const StreamArgs& a, cudaStream_t s) {
   auto kern = ce_stream_kernel<T, kBwd>;
-  int rc = cuda_status(
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamSmem),
-      "cudaFuncSetAttribute(ce_stream_kernel)");
-  if (rc != FLCE_OK) return rc;
+  static std::atomic<uint64_t> done{0};  // devices whose smem limit is raised
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  const uint64_t bit = 1ull << (dev & 63);
+  int rc = FLCE_OK;
+  if (!(done.load() & bit)) {
+    rc = cuda_status(
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamSmem),
+        "cudaFuncSetAttribute(ce_stream_kernel)");
+    if (rc != FLCE_OK) return rc;
+    done.fetch_or(bit);
+  }
   const int64_t g = static_cast<int64_t>(sm_count()) * kStreamCtasPerSm;
   const int grid = static_cast<int>(a.N < g ? a.N : g);
   kern<<<grid, kStreamThreads, kStreamSmem, s>>>(a);

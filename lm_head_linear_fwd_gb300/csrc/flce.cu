@@ -27,6 +27,8 @@
 #include <algorithm>
 #include <atomic>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "../../include/flce_gemm.h"
 #include "host.h"
@@ -498,9 +500,31 @@ static EncodeTiledFn encode_fn() {
 
 // cuTensorMapEncodeTiled is a driver call and needs a current context on the
 // calling thread.  A thread that has only launched kernels through a runtime
-// may have none bound yet (e.g. an autograd worker thread), so bind the
-// current device's primary context explicitly.
+// may have none bound yet (e.g. an autograd worker thread): then bind the
+// current device's primary context.  A thread that has one is left alone (so
+// nothing but a query runs while a stream is being captured).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+static CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
 static int bind_context() {
+  CtxGetCurrentFn get = ctx_get_current_fn();
+  if (get != nullptr) {
+    CUcontext ctx = nullptr;
+    if (get(&ctx) == CUDA_SUCCESS && ctx != nullptr) return FLCE_OK;
+  }
   int dev = 0;
   int rc = cuda_status(cudaGetDevice(&dev), "cudaGetDevice");
   if (rc != FLCE_OK) return rc;
@@ -556,6 +580,27 @@ static int make_operand_map(CUtensorMap* m, const Operand& op, int dt, int tile_
   return make_map(m, op.ptr, dt, op.rows, op.k, op.ld, ek);
 }
 
+// Per-device, per-kernel host state: whether the dynamic shared-memory limit
+// has been raised, and the number of resident CTA pairs.  Filled on the first
+// launch of each kernel on each device (ids < 64), so that later launches -
+// including launches inside a stream capture - only enqueue work.
+static std::mutex g_attr_mutex;
+static std::vector<std::pair<const void*, int>> g_attr_done;  // (kernel, device)
+
+template <typename Kern>
+static int raise_smem_once(Kern kern, int bytes, const char* what) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  const void* key = reinterpret_cast<const void*>(kern);
+  std::lock_guard<std::mutex> lock(g_attr_mutex);
+  for (const auto& e : g_attr_done)
+    if (e.first == key && e.second == dev) return FLCE_OK;
+  const int rc = cuda_status(
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes), what);
+  if (rc == FLCE_OK) g_attr_done.emplace_back(key, dev);
+  return rc;
+}
+
 // Output of an epilogue that stores through TMA: row-major [rows, cols] with
 // row stride ld (elements), written in boxes of 32 rows x 128 bytes.
 struct OutDesc {
@@ -586,9 +631,7 @@ static int launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const 
   const int tiles = ga.nMt * ga.nNt;
   if (tiles == 0) return FLCE_OK;
   auto kern = tc_gemm_pair_kernel<BN, A_MN, B_MN, Epi>;
-  int rc = cuda_status(
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes),
-      "cudaFuncSetAttribute(tc_gemm_pair_kernel)");
+  int rc = raise_smem_once(kern, G::kSmemBytes, "cudaFuncSetAttribute(tc_gemm_pair_kernel)");
   if (rc != FLCE_OK) return rc;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -602,12 +645,18 @@ static int launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   // as many pairs as can be resident at once (on GB300 all 152 SMs pair up: 76)
-  int max_pairs = 0;
-  cfg.gridDim = dim3(2 * static_cast<unsigned>(std::min(tiles, sm_count() / 2)), 1, 1);
-  rc = cuda_status(cudaOccupancyMaxActiveClusters(&max_pairs, kern, &cfg),
-                   "cudaOccupancyMaxActiveClusters");
-  if (rc != FLCE_OK) return rc;
-  if (max_pairs < 1) return FLCE_ENOSUP;
+  static std::atomic<int> pairs_cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  int max_pairs = pairs_cache[dev & 63].load();
+  if (max_pairs <= 0) {
+    cfg.gridDim = dim3(2 * static_cast<unsigned>(std::min(tiles, sm_count() / 2)), 1, 1);
+    rc = cuda_status(cudaOccupancyMaxActiveClusters(&max_pairs, kern, &cfg),
+                     "cudaOccupancyMaxActiveClusters");
+    if (rc != FLCE_OK) return rc;
+    if (max_pairs < 1) return FLCE_ENOSUP;
+    pairs_cache[dev & 63].store(max_pairs);
+  }
   cfg.gridDim = dim3(2 * static_cast<unsigned>(std::min(tiles, max_pairs)), 1, 1);
   return cuda_status(cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, ga, ep),
                      "cudaLaunchKernelEx(tc_gemm_pair_kernel)");
@@ -647,9 +696,7 @@ static int launch_gemm(int role, const Operand& a, const Operand& b, const OutDe
   const int tiles = ga.nMt * ga.nNt;
   if (tiles == 0) return FLCE_OK;
   auto kern = tc_gemm_kernel<T, BN, A_MN, B_MN, Epi>;
-  rc = cuda_status(
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes),
-      "cudaFuncSetAttribute(tc_gemm_kernel)");
+  rc = raise_smem_once(kern, G::kSmemBytes, "cudaFuncSetAttribute(tc_gemm_kernel)");
   if (rc != FLCE_OK) return rc;
   const int grid = std::min(tiles, sm_count());
   kern<<<grid, kGemmThreads, G::kSmemBytes, s>>>(ma, mb, mc, ga, ep);

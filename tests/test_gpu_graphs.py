@@ -1,0 +1,55 @@
+"""Both operations captured in a CUDA graph: replays give the eager results
+bit for bit (the library only enqueues work on the caller's stream once each
+kernel has run once on the device)."""
+import pytest
+import torch
+
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def test_flce_and_ce_in_a_cuda_graph():
+    import lm_head_linear_fwd_gb300 as lh
+    p = wl.random_flce(1000, 256, 5000, torch.bfloat16, bias=True, seed=31, reduction="mean")
+    H, W, b, y = p.H.cuda(), p.W.cuda(), p.bias.cuda(), p.labels.cuda()
+    c = wl.random_ce(512, 7000, torch.bfloat16, seed=32)
+    logits0 = c.logits.cuda().contiguous()
+    logits = logits0.clone()
+    yl = c.labels.cuda()
+    N, D, V = p.N, p.D, p.V
+    ws = torch.empty(lh.flce_workspace_bytes(0, N, D, V, 256), dtype=torch.uint8, device="cuda")
+    st = lh.new_status("cuda")
+    one = torch.ones(1, device="cuda")
+    gH = torch.empty_like(H)
+    gW = torch.empty(V, D, device="cuda")
+    gb = torch.empty(V, device="cuda")
+    fo = lh.flce_fwd(H, W, y, b, -100, "mean", ws=ws, status=st)
+    co = lh.ce_logits_fwd(logits, yl, status=st)
+
+    def step():
+        lh.flce_fwd(H, W, y, b, -100, "mean", ws=ws, status=st, out=fo)
+        lh.flce_bwd(H, W, y, fo.lse, fo.n_valid, one, b, -100, "mean", None, 256, grad_H=gH,
+                    grad_W=gW, grad_bias=gb, ws=ws, status=st)
+        logits.copy_(logits0)
+        lh.ce_logits_fwd(logits, yl, status=st, out=co)
+        lh.ce_logits_bwd(logits, yl, co.lse, co.n_valid, one, inplace_grad=True, status=st)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()   # eager, on the capture stream: every kernel has run once
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in (fo.loss, fo.lse, gH, gW, gb, co.loss, logits)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(2):
+        for t in (gH, gW, gb):
+            t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        lh.check_status(st)
+        for a, e in zip((fo.loss, fo.lse, gH, gW, gb, co.loss, logits), eager):
+            assert torch.equal(a, e)
