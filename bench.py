@@ -367,6 +367,9 @@ def run_ours(args, rank, ws, local):
     del pristine, logits, c, cws, co
     torch.cuda.empty_cache()
 
+    # ------------------------------------------------- latency-bound workloads
+    small = latency_configs(dev, stream, args.steps)
+
     # ------------------------------------------------------------ CPU baseline
     cpu = cpu_baseline(args) if (rank == 0 and not args.no_cpu_baseline) else None
 
@@ -410,6 +413,7 @@ def run_ours(args, rank, ws, local):
             "frac_of_peak": round(6.0 * N * D * V / (fused_ms * 1e-3) / 1e12 / peak_t, 4),
             "peak_extra_gib": round(fused_peak_extra / 2**30, 4),
         },
+        "latency_workloads": small,
         "ce_logits": {
             "ms": round(ce_ms, 4),
             "gb_s": round(ce_gbs, 1),
@@ -497,6 +501,52 @@ def run_ce_only(args, rank, ws, local, dev, stream, peaks, peak_src):
                           "config": {"workload": f"CE on logits only [{c.N},{c.V}] bf16"},
                           "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
                           "note": "profiling run: given-logits part only"}))
+
+
+def latency_configs(dev, stream, steps):
+    """fwd+bwd of the two small FLCE workloads (tiny fp32; the small bf16 model
+    with bias), launched eagerly and replayed from a CUDA graph."""
+    import torch
+    import workloads as wl
+    import lm_head_linear_fwd_gb300 as lh
+    out = {}
+    for name, p in (("tiny_flce N=256 D=128 V=1000 fp32", wl.tiny_flce(device=dev)),
+                    ("small_flce N=2048 D=768 V=32777 bf16+bias", wl.small_flce(device=dev))):
+        H, W, b, y = p.H, p.W, p.bias, p.labels
+        N, D, V = p.N, p.D, p.V
+        dt = 0 if H.dtype == torch.bfloat16 else 1
+        ws = torch.empty(lh.flce_workspace_bytes(dt, N, D, V, 0), dtype=torch.uint8, device=dev)
+        st = lh.new_status(dev)
+        one = torch.ones(1, device=dev)
+        gH = torch.empty_like(H)
+        gW = torch.empty(V, D, device=dev)
+        gb = torch.empty(V, device=dev) if b is not None else None
+        fo = lh.flce_fwd(H, W, y, b, -100, p.reduction, p.num_label_tokens, ws=ws, status=st)
+
+        def step():
+            lh.flce_fwd(H, W, y, b, -100, p.reduction, p.num_label_tokens, ws=ws, status=st,
+                        out=fo)
+            lh.flce_bwd(H, W, y, fo.lse, fo.n_valid, one, b, -100, p.reduction,
+                        p.num_label_tokens, None, grad_H=gH, grad_W=gW, grad_bias=gb, ws=ws,
+                        status=st)
+
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                step()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize()
+        eager = sum(_events_time(step, steps, stream)) / steps
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        graph = sum(_events_time(g.replay, steps, stream)) / steps
+        lh.check_status(st)
+        out[name] = {"eager_ms": round(eager, 4), "graph_ms": round(graph, 4),
+                     "tokens_per_s_graph": round(N / (graph * 1e-3), 1),
+                     "tflops_8NDV_graph": round(8.0 * N * D * V / (graph * 1e-3) / 1e12, 2)}
+    return out
 
 
 # ------------------------------------------------------------- oracle timing
