@@ -477,6 +477,21 @@ __global__ void __launch_bounds__(256) scale_kernel(T* x, int64_t n, const float
     Elem<T>::store(x + i, Elem<T>::load(x + i) * s);
 }
 
+// out[r, d] = sum over s of part[s * split_stride + r * D + d], in split order
+// (deterministic), converted to OutT.  Closes a split-K contraction.
+template <typename OutT>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ part,
+                                                            int S, int64_t split_stride, int C,
+                                                            int D, OutT* __restrict__ out) {
+  const int64_t n = static_cast<int64_t>(C) * D;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float acc = 0.0f;
+    for (int sp = 0; sp < S; ++sp) acc += part[sp * split_stride + i];
+    Elem<OutT>::store(out + i, acc);
+  }
+}
+
 // --------------------------------------------------------------- host: TMA
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -628,6 +643,8 @@ static int launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const 
   ga.nK = (K + G::kEK - 1) / G::kEK;
   ga.group_m = std::max(1, std::min((group_m + 1) / 2, ga.nMt));
   ga.status = status;
+  ga.k_splits = 1;
+  ga.kb_per_split = ga.nK;
   const int tiles = ga.nMt * ga.nNt;
   if (tiles == 0) return FLCE_OK;
   auto kern = tc_gemm_pair_kernel<BN, A_MN, B_MN, Epi>;
@@ -665,11 +682,12 @@ static int launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const 
 template <typename T, int BN, bool A_MN, bool B_MN, class Epi>
 static int launch_gemm(int role, const Operand& a, const Operand& b, const OutDesc* out, int M,
                        int N, int K, int group_m, const typename Epi::Params& ep,
-                       int32_t* status, cudaStream_t s) {
+                       int32_t* status, cudaStream_t s, int k_splits = 1) {
   using G = GemmGeo<T, BN>;
   const int dt = sizeof(T) == 2 ? FLCE_BF16 : FLCE_F32;
   CUtensorMap ma, mb, mc;
-  const bool pair = sizeof(T) == 2 && BN == 256 && (g_pair_mask.load() & role) != 0;
+  const bool pair =
+      sizeof(T) == 2 && BN == 256 && k_splits == 1 && (g_pair_mask.load() & role) != 0;
   int rc = make_operand_map(&ma, a, dt, kBM);
   if (rc != FLCE_OK) return rc;
   rc = make_operand_map(&mb, b, dt, pair ? BN / 2 : BN);
@@ -691,9 +709,12 @@ static int launch_gemm(int role, const Operand& a, const Operand& b, const OutDe
   ga.nMt = (M + kBM - 1) / kBM;
   ga.nNt = (N + BN - 1) / BN;
   ga.nK = (K + G::kEK - 1) / G::kEK;
-  ga.group_m = std::max(1, std::min(group_m, ga.nMt));
+  ga.k_splits = std::max(1, std::min(k_splits, ga.nK));
+  ga.kb_per_split = (ga.nK + ga.k_splits - 1) / ga.k_splits;
+  ga.k_splits = (ga.nK + ga.kb_per_split - 1) / ga.kb_per_split;  // no empty split
+  ga.group_m = std::max(1, std::min(group_m, ga.nMt * ga.k_splits));
   ga.status = status;
-  const int tiles = ga.nMt * ga.nNt;
+  const int tiles = ga.nMt * ga.k_splits * ga.nNt;
   if (tiles == 0) return FLCE_OK;
   auto kern = tc_gemm_kernel<T, BN, A_MN, B_MN, Epi>;
   rc = raise_smem_once(kern, G::kSmemBytes, "cudaFuncSetAttribute(tc_gemm_kernel)");
@@ -712,6 +733,25 @@ static int group_for(int64_t K, int dt, int nMt) {
   return static_cast<int>(g);
 }
 
+// Number of K splits launch_gemm really uses for `requested` (no empty split).
+static int effective_splits(int nK, int requested) {
+  int S = std::max(1, std::min(requested, nK));
+  const int per = (nK + S - 1) / S;
+  return (nK + per - 1) / per;
+}
+
+// grad_H of a C-row chunk has only ceil(C/128) * ceil(D/256) output tiles; when
+// they cannot fill half of the SMs, its long K (= V) is split so that they do.
+static int grad_h_splits(int64_t C, int64_t D, int64_t V, int dt) {
+  const int64_t tiles = ((C + kBM - 1) / kBM) * ((D + 255) / 256);
+  const int64_t sms = sm_count();
+  if (tiles * 2 > sms) return 1;
+  const int nK = static_cast<int>((V + (128 / dtype_size(dt)) - 1) / (128 / dtype_size(dt)));
+  int64_t S = std::min<int64_t>(sms / tiles, 8);
+  S = std::min<int64_t>(S, nK / 16);
+  return effective_splits(nK, static_cast<int>(std::max<int64_t>(S, 1)));
+}
+
 // ------------------------------------------------------------ workspace plan
 
 constexpr int kBNFwd = 256;
@@ -722,7 +762,7 @@ struct FlcePlan {
   int nparts;          // vocab tiles of the forward
   int64_t part_ld;
   size_t off_part_m, off_part_s, off_zlab, off_rows, fwd_bytes;
-  size_t off_dz, off_colsum, bwd_bytes;
+  size_t off_dz, off_colsum, off_hpart, bwd_bytes;
   // fp32 only: K-major copies of the operands the tf32 MMA cannot read MN-major
   int64_t ldVt, ldCt;
   size_t off_Wt, off_dzT, off_HT;
@@ -786,6 +826,19 @@ static FlcePlan plan(int dt, int64_t N, int64_t D, int64_t V, int64_t chunk) {
   o += round_up(static_cast<size_t>(std::min<int64_t>(p.chunk, N)) * p.ldV * es, 256);
   p.off_colsum = o;
   o += round_up(static_cast<size_t>(kColSplits) * V * 4, 256);
+  {
+    // split-K partials of grad_H, for the full chunk and for the last one
+    const int64_t c1 = std::min<int64_t>(p.chunk, N);
+    const int64_t c2 = N % p.chunk == 0 ? c1 : N % p.chunk;
+    size_t need = 0;
+    for (int64_t c : {c1, c2}) {
+      const int S = grad_h_splits(c, D, V, dt);
+      if (S > 1)
+        need = std::max(need, static_cast<size_t>(S) * ((c + kBM - 1) / kBM) * kBM * D * 4);
+    }
+    p.off_hpart = o;
+    o += round_up(need, 256);
+  }
   p.ldVt = (V + 3) / 4 * 4;
   p.ldCt = (std::min<int64_t>(p.chunk, N) + 3) / 4 * 4;
   p.off_Wt = p.off_dzT = p.off_HT = 0;
@@ -988,7 +1041,32 @@ static int bwd_tail(const void* W, const T* Hc, int64_t D, int64_t V, int C, boo
     if (rc != FLCE_OK) return rc;
   }
   // 3. grad_H[chunk] = dZ W
-  if (grad_H_chunk != nullptr) {
+  const int S = grad_H_chunk != nullptr ? grad_h_splits(C, D, V, dt) : 1;
+  if (grad_H_chunk != nullptr && S > 1) {
+    // few output tiles: split K (= V), fp32 partials, fixed-order reduction
+    const int64_t rows = static_cast<int64_t>((C + kBM - 1) / kBM) * kBM;
+    float* hpart = reinterpret_cast<float*>(w + p.off_hpart);
+    using E = EpiStore<float, false>;
+    typename E::Params ep{static_cast<int>(S * rows), static_cast<int>(D), 0};
+    const Operand a{dz, C, V, p.ldV, false};
+    const OutDesc o{hpart, FLCE_F32, S * rows, D, D};
+    if (kTf32) {
+      const Operand b{reinterpret_cast<float*>(w + p.off_Wt), D, V, p.ldVt, false};
+      rc = launch_gemm<T, 256, false, false, E>(kRoleGradH, a, b, &o, C, (int)D, (int)V, 8, ep,
+                                                status, s, S);
+    } else {
+      const Operand b{W, D, V, D, true};
+      rc = launch_gemm<T, 256, false, true, E>(kRoleGradH, a, b, &o, C, (int)D, (int)V, 8, ep,
+                                               status, s, S);
+    }
+    if (rc != FLCE_OK) return rc;
+    const int64_t n = static_cast<int64_t>(C) * D;
+    const int grid = static_cast<int>(std::min<int64_t>((n + 255) / 256, sm_count() * 8));
+    splitk_reduce_kernel<T><<<grid, 256, 0, s>>>(hpart, S, rows * D, C, (int)D,
+                                                 static_cast<T*>(grad_H_chunk));
+    rc = launch_status("splitk_reduce_kernel launch");
+    if (rc != FLCE_OK) return rc;
+  } else if (grad_H_chunk != nullptr) {
     using E = EpiStore<T, false>;
     typename E::Params ep{C, static_cast<int>(D), 0};
     const Operand a{dz, C, V, p.ldV, false};

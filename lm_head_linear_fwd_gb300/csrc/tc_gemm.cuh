@@ -68,6 +68,11 @@ struct GemmArgs {
   int nMt, nNt, nK;
   int group_m;
   int32_t* status;
+  // Split-K (one-CTA kernel only): K blocks are split into k_splits ranges of
+  // kb_per_split; split s of M-tile mt is handed to the epilogue as M-tile
+  // s * nMt + mt, so each split fills its own row band of the output.
+  int k_splits;
+  int kb_per_split;
 };
 
 __device__ __forceinline__ void tile_coords(int t, int nMt, int nNt, int group_m, int& mt,
@@ -189,7 +194,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
-  const int num_tiles = ga.nMt * ga.nNt;
+  const int nMtE = ga.nMt * ga.k_splits;  // M-tiles counting every K split
+  const int num_tiles = nMtE * ga.nNt;
 
   auto fail = [&]() {
     *abort_flag = 1;
@@ -203,9 +209,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int issued = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        int mt, nt;
-        tile_coords(t, ga.nMt, ga.nNt, ga.group_m, mt, nt);
-        for (int kb = 0; kb < ga.nK; ++kb) {
+        int mte, nt;
+        tile_coords(t, nMtE, ga.nNt, ga.group_m, mte, nt);
+        const int split = mte / ga.nMt;
+        const int mt = mte - split * ga.nMt;
+        const int kb0 = split * ga.kb_per_split;
+        const int kb1 = min(ga.nK, kb0 + ga.kb_per_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
@@ -247,13 +257,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
         const int buf = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
+        int mte, nt;
+        tile_coords(t, nMtE, ga.nNt, ga.group_m, mte, nt);
+        const int kb0 = (mte / ga.nMt) * ga.kb_per_split;
+        const int kb1 = min(ga.nK, kb0 + ga.kb_per_split);
         if (!mbar_wait(&acce_bar[buf], acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-        for (int kb = 0; kb < ga.nK; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
             ok = false;
             break;
@@ -264,7 +278,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int k = 0; k < G::kMmaPerStage; ++k) {
             MmaTraits<T>::mma(d_tmem, operand_desc<T, A_MN>(sa, k), operand_desc<T, B_MN>(sb, k),
-                              idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                              idesc, (kb > kb0 || k > 0) ? 1u : 0u);
           }
           mma_commit(&empty_bar[stage]);
           if (++stage == S) {
@@ -303,11 +317,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       }
       tc_fence_after();
-      int mt, nt;
-      tile_coords(t, ga.nMt, ga.nNt, ga.group_m, mt, nt);
+      int mte, nt;
+      tile_coords(t, nMtE, ga.nNt, ga.group_m, mte, nt);
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(buf * BN);
-      Epi::template tile<BN>(ep, mt, nt, row_in_tile, taddr, ctx);
+      Epi::template tile<BN>(ep, mte, nt, row_in_tile, taddr, ctx);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acce_bar[buf]);
