@@ -43,6 +43,29 @@ __device__ __forceinline__ float load_elem(const void* p, int64_t i) {
   return Elem<T>::load(static_cast<const T*>(p) + i);
 }
 
+// v[j] += bias[col0 + j] for the columns inside the vocabulary: 16-byte loads
+// when all 32 columns are inside and aligned (the address is the same for the
+// whole warp, so each load is one broadcast), element loads otherwise.
+template <typename T>
+__device__ __forceinline__ void add_bias32(const void* bias, int col0, int V, float (&v)[32]) {
+  const T* b = static_cast<const T*>(bias) + col0;
+  if (col0 + 32 <= V && (reinterpret_cast<uintptr_t>(b) & 15u) == 0) {
+    constexpr int EPV = Elem<T>::kPerVec;
+    const uint4* bv = reinterpret_cast<const uint4*>(b);
+#pragma unroll
+    for (int k = 0; k < 32 / EPV; ++k) {
+      float x[EPV];
+      Elem<T>::unpack(__ldg(bv + k), x);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) v[k * EPV + e] += x[e];
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (col0 + j < V) v[j] += Elem<T>::load(b + j);
+  }
+}
+
 // Forward: per-row partial log-sum-exp of one logits tile + label gather.
 template <typename T>
 struct EpiLse {
@@ -73,11 +96,11 @@ struct EpiLse {
       if (col0 >= p.V) break;  // uniform across the warp
       float v[32];
       tmem_ld32(taddr + c * 32, v);
+      if (p.bias != nullptr) add_bias32<T>(p.bias, col0, p.V, v);
       float t[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        float x = v[j];
-        if (p.bias != nullptr && col0 + j < p.V) x += load_elem<T>(p.bias, col0 + j);
+        const float x = v[j];
         if (c * 32 + j == ylocal) zy = x;
         t[j] = (col0 + j < p.V) ? x * kLog2e : -INFINITY;
       }
@@ -119,10 +142,10 @@ struct EpiLseStore {
       if (col0 >= p.V) break;
       float v[32];
       tmem_ld32(taddr + c * 32, v);
+      if (p.bias != nullptr) add_bias32<T>(p.bias, col0, p.V, v);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        float x = v[j];
-        if (p.bias != nullptr && col0 + j < p.V) x += load_elem<T>(p.bias, col0 + j);
+        const float x = v[j];
         if (c * 32 + j == ylocal) zy = x;
         if (col0 + j < p.V) m = fmaxf(m, x * kLog2e);
       }
@@ -138,10 +161,10 @@ struct EpiLseStore {
         float v[32];
         tmem_ld32(taddr + g * CPS + h * 32, v);
         const int cb = col0 + h * 32;
+        if (p.bias != nullptr) add_bias32<T>(p.bias, cb, p.V, v);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          float x = v[j];
-          if (p.bias != nullptr && cb + j < p.V) x += load_elem<T>(p.bias, cb + j);
+          const float x = v[j];
           const float u = fmaf(x, kLog2e, -m);
           if (cb + j < p.V) s += ex2(u);
           v[j] = u;
@@ -206,13 +229,10 @@ struct EpiDlogits {
         float v[32];
         tmem_ld32(taddr + g * CPS + h * 32, v);
         const int cl = g * CPS + h * 32;  // column within the tile
+        if (p.bias != nullptr) add_bias32<T>(p.bias, col_base + cl, p.V, v);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          float x = v[j];
-          if (p.bias != nullptr && col_base + cl + j < p.V)
-            x += load_elem<T>(p.bias, col_base + cl + j);
-          v[j] = (ex2(fmaf(x, kLog2e, -lse2)) - (cl + j == ylocal ? 1.0f : 0.0f)) * c;
-        }
+        for (int j = 0; j < 32; ++j)
+          v[j] = (ex2(fmaf(v[j], kLog2e, -lse2)) - (cl + j == ylocal ? 1.0f : 0.0f)) * c;
 #pragma unroll
         for (int k = 0; k < 32 / EPV; ++k) {
           float x[EPV];
