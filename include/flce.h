@@ -269,6 +269,26 @@ FLCE_API int flce_bwd_shard(const void* H, const void* W_shard, const void* bias
                             float* grad_bias_shard, void* ws, size_t ws_bytes, int32_t* status,
                             flce_stream_t stream);
 
+/* CE on a vocabulary shard of given logits: logits_shard [N, ld] holds the
+ * columns [vocab_offset, vocab_offset + V_shard) of the full [N, V_total]
+ * logits; labels are global ids.  The forward writes the same per-row m_local,
+ * s_local, zy_local as flce_fwd_shard (then steps 2-5 above); the backward
+ * writes the shard's columns of dZ (in place or not, as ce_logits_bwd) from
+ * the global lse and n_valid. */
+FLCE_API int ce_logits_fwd_shard(const void* logits_shard, int dt, int64_t N, int64_t V_shard,
+                                 int64_t ld, int64_t vocab_offset, int64_t V_total,
+                                 const int64_t* labels, int64_t ignore_index, float* m_local,
+                                 float* s_local, float* zy_local, int32_t* status,
+                                 flce_stream_t stream);
+
+FLCE_API int ce_logits_bwd_shard(const void* logits_shard, int dt, int64_t N, int64_t V_shard,
+                                 int64_t ld, int64_t vocab_offset, int64_t V_total,
+                                 const int64_t* labels, int64_t ignore_index, int reduction,
+                                 int64_t num_label_tokens, const float* lse,
+                                 const int64_t* n_valid, const float* grad_loss,
+                                 int inplace_grad, void* grad_logits, int64_t ld_grad,
+                                 int32_t* status, flce_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Fused linear cross-entropy, forward and backward in one call             */
 /* ------------------------------------------------------------------------ */

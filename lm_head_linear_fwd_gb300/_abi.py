@@ -50,6 +50,10 @@ _SIGNATURES = {
                                _sz, _p, _p]),
     "flce_bwd_shard": (_i, [_p, _p, _p, _i, _i64, _i64, _i64, _i64, _i64, _p, _i64, _i, _i64, _p,
                             _p, _p, _i64, _p, _p, _i, _p, _p, _sz, _p, _p]),
+    "ce_logits_fwd_shard": (_i, [_p, _i, _i64, _i64, _i64, _i64, _i64, _p, _i64, _p, _p, _p, _p,
+                                 _p]),
+    "ce_logits_bwd_shard": (_i, [_p, _i, _i64, _i64, _i64, _i64, _i64, _p, _i64, _i, _i64, _p, _p,
+                                 _p, _i, _p, _i64, _p, _p]),
     "flce_fwd_bwd_workspace_bytes": (_sz, [_i, _i64, _i64, _i64, _i64]),
     "flce_fwd_bwd": (_i, [_p, _p, _p, _i, _i64, _i64, _i64, _p, _i64, _i, _i64, _p, _i64, _p, _p,
                           _p, _p, _p, _p, _i, _p, _p, _sz, _p, _p]),
@@ -125,6 +129,8 @@ flce_fwd_shard = _call("flce_fwd_shard")
 flce_shard_rescale = _call("flce_shard_rescale")
 flce_shard_finish = _call("flce_shard_finish")
 flce_bwd_shard = _call("flce_bwd_shard")
+ce_logits_fwd_shard = _call("ce_logits_fwd_shard")
+ce_logits_bwd_shard = _call("ce_logits_bwd_shard")
 flce_fwd_bwd = _call("flce_fwd_bwd")
 flce_grad_scale = _call("flce_grad_scale")
 flce_count_valid = _call("flce_count_valid")

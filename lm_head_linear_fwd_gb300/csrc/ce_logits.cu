@@ -28,13 +28,40 @@
 
 namespace flce {
 
+// Vocabulary-shard outputs of the forward: per row the base-2 maximum and sum
+// over the shard's columns and the label logit when the label lies in the shard
+// (0 otherwise); labels are global ids in [0, V_total).  m_out == nullptr
+// selects the ordinary (unsharded) outputs.
+struct ShardOut {
+  float* m_out;
+  float* s_out;
+  float* zy_out;
+  int64_t v0;
+  int64_t V_total;
+  template <typename T>
+  __device__ void write(int64_t row, float m, float s, int64_t y, int64_t ignore_index,
+                        int64_t V_shard, const T* p, int32_t* status) const {
+    m_out[row] = m;
+    s_out[row] = s;
+    float zy = 0.0f;
+    if (y != ignore_index) {
+      if (!label_ok(y, V_total))
+        set_status(status, FLCE_ELABEL);
+      else if (y >= v0 && y < v0 + V_shard)
+        zy = Elem<T>::load(p + (y - v0));
+    }
+    zy_out[row] = zy;
+  }
+};
+
 // ---------------------------------------------------------------- forward kernel
 
 template <typename T, int THREADS>
 __global__ void __launch_bounds__(THREADS) ce_fwd_rows_kernel(
     const T* __restrict__ logits, int64_t N, int64_t V, int64_t ld,
     const int64_t* __restrict__ labels, int64_t ignore_index, float* __restrict__ lse_out,
-    float* __restrict__ loss_rows, float* __restrict__ label_logit, int32_t* status) {
+    float* __restrict__ loss_rows, float* __restrict__ label_logit, int32_t* status,
+    ShardOut sh) {
   constexpr int EPV = Elem<T>::kPerVec;
   constexpr int UNROLL = (EPV == 8) ? 4 : 8;  // 32 elements per batch
   constexpr int NW = THREADS / 32;
@@ -90,20 +117,24 @@ __global__ void __launch_bounds__(THREADS) ce_fwd_rows_kernel(
     if (tid == 0) {
       Lse2 all;
       for (int w = 0; w < NW; ++w) all.merge(red_m[w], red_s[w]);
-      const float lse = all.m * kLn2 + logf(all.s);
-      lse_out[row] = lse;
       const int64_t y = labels[row];
-      float li = 0.0f, zy = NAN;
-      if (y != ignore_index) {
-        if (label_ok(y, V)) {
-          zy = Elem<T>::load(p + y);
-          li = lse - zy;
-        } else {
-          set_status(status, FLCE_ELABEL);
+      if (sh.m_out != nullptr) {
+        sh.write(row, all.m, all.s, y, ignore_index, V, p, status);
+      } else {
+        const float lse = all.m * kLn2 + logf(all.s);
+        lse_out[row] = lse;
+        float li = 0.0f, zy = NAN;
+        if (y != ignore_index) {
+          if (label_ok(y, V)) {
+            zy = Elem<T>::load(p + y);
+            li = lse - zy;
+          } else {
+            set_status(status, FLCE_ELABEL);
+          }
         }
+        loss_rows[row] = li;
+        if (label_logit != nullptr) label_logit[row] = zy;
       }
-      loss_rows[row] = li;
-      if (label_logit != nullptr) label_logit[row] = zy;
     }
     __syncthreads();
   }
@@ -162,7 +193,8 @@ template <typename T, int THREADS>
 __global__ void __launch_bounds__(THREADS) ce_bwd_rows_kernel(
     const T* logits, int64_t N, int64_t V, int64_t ld, const int64_t* __restrict__ labels,
     int64_t ignore_index, int reduction, int64_t num_label_tokens, const float* __restrict__ lse,
-    const int64_t* n_valid, const float* grad_loss, T* grad, int64_t ldg) {
+    const int64_t* n_valid, const float* grad_loss, T* grad, int64_t ldg, int64_t v0,
+    int64_t V_total) {
   constexpr int EPV = Elem<T>::kPerVec;
   constexpr int UNROLL = 4;
   const float coef = grad_coef(reduction, num_label_tokens, n_valid, grad_loss);
@@ -171,8 +203,9 @@ __global__ void __launch_bounds__(THREADS) ce_bwd_rows_kernel(
   for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
     const T* p = logits + row * ld;
     T* q = grad + row * ldg;
-    const int64_t y = labels[row];
-    const bool valid = (y != ignore_index) && label_ok(y, V);
+    const int64_t yg = labels[row];
+    const bool valid = (yg != ignore_index) && label_ok(yg, V_total);
+    const int64_t y = valid ? yg - v0 : -1;  // label column within this shard (or none)
     const float c = valid ? coef : 0.0f;
     const float lse2 = lse[row] * kLog2e;
     const uintptr_t pa = reinterpret_cast<uintptr_t>(p) & 15u;
@@ -261,6 +294,10 @@ struct StreamArgs {
   void* grad;
   int64_t ldg;
   int32_t* status;
+  // vocabulary shard (v0 = 0, V_total = V and sh.m_out = nullptr unsharded)
+  int64_t v0;
+  int64_t V_total;
+  ShardOut sh;
 };
 
 template <typename T, bool kBwd>
@@ -340,8 +377,9 @@ __global__ void __launch_bounds__(kStreamThreads) ce_stream_kernel(const StreamA
   if (kBwd) coef = grad_coef(a.reduction, a.num_label_tokens, a.n_valid, a.grad_loss);
   uint32_t stage = 0, phase = 0;
   for (int64_t row = blockIdx.x; row < a.N; row += gridDim.x) {
-    const int64_t y = a.labels[row];
-    const bool valid = (y != a.ignore_index) && label_ok(y, a.V);
+    const int64_t yg = a.labels[row];
+    const bool valid = (yg != a.ignore_index) && label_ok(yg, a.V_total);
+    const int64_t y = valid ? yg - a.v0 : -1;  // label column within this shard (or none)
     float c = 0.0f, lse2 = 0.0f;
     if (kBwd) {
       c = valid ? coef : 0.0f;
@@ -458,19 +496,24 @@ __global__ void __launch_bounds__(kStreamThreads) ce_stream_kernel(const StreamA
       if (tid == 0) {
         Lse2 all;
         for (int w = 0; w < kConsumerWarps; ++w) all.merge(red_m[w], red_s[w]);
-        const float lse = all.m * kLn2 + logf(all.s);
-        a.lse_out[row] = lse;
-        float li = 0.0f, zy = NAN;
-        if (y != a.ignore_index) {
-          if (valid) {
-            zy = Elem<T>::load(static_cast<const T*>(a.logits) + row * a.ld + y);
-            li = lse - zy;
-          } else {
-            set_status(a.status, FLCE_ELABEL);
+        const T* prow = static_cast<const T*>(a.logits) + row * a.ld;
+        if (a.sh.m_out != nullptr) {
+          a.sh.write(row, all.m, all.s, yg, a.ignore_index, a.V, prow, a.status);
+        } else {
+          const float lse = all.m * kLn2 + logf(all.s);
+          a.lse_out[row] = lse;
+          float li = 0.0f, zy = NAN;
+          if (yg != a.ignore_index) {
+            if (valid) {
+              zy = Elem<T>::load(prow + y);
+              li = lse - zy;
+            } else {
+              set_status(a.status, FLCE_ELABEL);
+            }
           }
+          a.loss_rows[row] = li;
+          if (a.label_logit != nullptr) a.label_logit[row] = zy;
         }
-        a.loss_rows[row] = li;
-        if (a.label_logit != nullptr) a.label_logit[row] = zy;
       }
       named_barrier(1, kConsumers);
     }
@@ -572,6 +615,45 @@ static int row_grid(int64_t N) {
   return static_cast<int>(N < g ? (N > 0 ? N : 1) : g);
 }
 
+// Launches the per-row forward kernel (bulk-copy streaming for 16-byte aligned
+// rows, register streaming otherwise).  sh.m_out != nullptr: vocabulary-shard
+// outputs instead of lse / loss rows.
+static int ce_fwd_rows(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
+                       const int64_t* labels, int64_t ignore_index, float* lse, float* rows,
+                       float* label_logit, const ShardOut& sh, int32_t* status,
+                       cudaStream_t s) {
+  if (N == 0) return FLCE_OK;
+  if (streamable(logits, ld, V, dtype_size(dt))) {
+    StreamArgs a{};
+    a.logits = logits;
+    a.N = N;
+    a.V = V;
+    a.ld = ld;
+    a.labels = labels;
+    a.ignore_index = ignore_index;
+    a.lse_out = lse;
+    a.loss_rows = rows;
+    a.label_logit = label_logit;
+    a.status = status;
+    a.v0 = sh.m_out != nullptr ? sh.v0 : 0;
+    a.V_total = sh.m_out != nullptr ? sh.V_total : V;
+    a.sh = sh;
+    return dt == FLCE_BF16 ? launch_stream<__nv_bfloat16, false>(a, s)
+                           : launch_stream<float, false>(a, s);
+  }
+  const int grid = row_grid(N);
+  if (dt == FLCE_BF16) {
+    ce_fwd_rows_kernel<__nv_bfloat16, 512><<<grid, 512, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(logits), N, V, ld, labels, ignore_index, lse, rows,
+        label_logit, status, sh);
+  } else {
+    ce_fwd_rows_kernel<float, 512><<<grid, 512, 0, s>>>(static_cast<const float*>(logits), N, V,
+                                                        ld, labels, ignore_index, lse, rows,
+                                                        label_logit, status, sh);
+  }
+  return launch_status("ce_fwd_rows_kernel launch");
+}
+
 extern "C" int ce_logits_fwd(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
                              const int64_t* labels, int64_t ignore_index, int reduction,
                              int64_t num_label_tokens, float* loss, int64_t* n_valid, float* lse,
@@ -588,37 +670,29 @@ extern "C" int ce_logits_fwd(const void* logits, int dt, int64_t N, int64_t V, i
     rows = static_cast<float*>(ws);
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (N > 0 && streamable(logits, ld, V, dtype_size(dt))) {
-    StreamArgs a{};
-    a.logits = logits;
-    a.N = N;
-    a.V = V;
-    a.ld = ld;
-    a.labels = labels;
-    a.ignore_index = ignore_index;
-    a.lse_out = lse;
-    a.loss_rows = rows;
-    a.label_logit = label_logit;
-    a.status = status;
-    rc = dt == FLCE_BF16 ? launch_stream<__nv_bfloat16, false>(a, s)
-                         : launch_stream<float, false>(a, s);
-    if (rc != FLCE_OK) return rc;
-  } else if (N > 0) {
-    const int grid = row_grid(N);
-    if (dt == FLCE_BF16) {
-      ce_fwd_rows_kernel<__nv_bfloat16, 512><<<grid, 512, 0, s>>>(
-          static_cast<const __nv_bfloat16*>(logits), N, V, ld, labels, ignore_index, lse, rows,
-          label_logit, status);
-    } else {
-      ce_fwd_rows_kernel<float, 512><<<grid, 512, 0, s>>>(static_cast<const float*>(logits), N,
-                                                          V, ld, labels, ignore_index, lse,
-                                                          rows, label_logit, status);
-    }
-    rc = launch_status("ce_fwd_rows_kernel launch");
-    if (rc != FLCE_OK) return rc;
-  }
+  ShardOut none{};
+  rc = ce_fwd_rows(logits, dt, N, V, ld, labels, ignore_index, lse, rows, label_logit, none,
+                   status, s);
+  if (rc != FLCE_OK) return rc;
   return launch_finalize(rows, labels, N, V, ignore_index, reduction, num_label_tokens, loss,
                          n_valid, s);
+}
+
+extern "C" int ce_logits_fwd_shard(const void* logits_shard, int dt, int64_t N, int64_t V_shard,
+                                   int64_t ld, int64_t vocab_offset, int64_t V_total,
+                                   const int64_t* labels, int64_t ignore_index, float* m_local,
+                                   float* s_local, float* zy_local, int32_t* status,
+                                   flce_stream_t stream) {
+  int rc = ce_common_checks(logits_shard, dt, N, V_shard, ld, labels, FLCE_SUM);
+  if (rc != FLCE_OK) return rc;
+  if (vocab_offset < 0 || V_total < vocab_offset + V_shard || V_total >= (int64_t(1) << 31))
+    return FLCE_ESHAPE;
+  if (status == nullptr) return FLCE_EINVAL;
+  if (N > 0 && (m_local == nullptr || s_local == nullptr || zy_local == nullptr))
+    return FLCE_EINVAL;
+  ShardOut sh{m_local, s_local, zy_local, vocab_offset, V_total};
+  return ce_fwd_rows(logits_shard, dt, N, V_shard, ld, labels, ignore_index, nullptr, nullptr,
+                     nullptr, sh, status, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------- packed-document labels
@@ -700,13 +774,15 @@ extern "C" int ce_logits_fwd_noalloc(const void* logits, int dt, int64_t N, int6
                        loss, n_valid, lse, rows, nullptr, nullptr, 0, status, stream);
 }
 
-extern "C" int ce_logits_bwd(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
-                             const int64_t* labels, int64_t ignore_index, int reduction,
-                             int64_t num_label_tokens, const float* lse, const int64_t* n_valid,
-                             const float* grad_loss, int inplace_grad, void* grad_logits,
-                             int64_t ld_grad, int32_t* status, flce_stream_t stream) {
+static int ce_bwd_entry(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
+                        int64_t v0, int64_t V_total, const int64_t* labels,
+                        int64_t ignore_index, int reduction, int64_t num_label_tokens,
+                        const float* lse, const int64_t* n_valid, const float* grad_loss,
+                        int inplace_grad, void* grad_logits, int64_t ld_grad, int32_t* status,
+                        flce_stream_t stream) {
   int rc = ce_common_checks(logits, dt, N, V, ld, labels, reduction);
   if (rc != FLCE_OK) return rc;
+  if (v0 < 0 || V_total < v0 + V || V_total >= (int64_t(1) << 31)) return FLCE_ESHAPE;
   if (status == nullptr) return FLCE_EINVAL;
   if (N == 0) return FLCE_OK;
   if (lse == nullptr || n_valid == nullptr || grad_loss == nullptr || grad_logits == nullptr)
@@ -741,6 +817,8 @@ extern "C" int ce_logits_bwd(const void* logits, int dt, int64_t N, int64_t V, i
     a.grad = grad_logits;
     a.ldg = ld_grad;
     a.status = status;
+    a.v0 = v0;
+    a.V_total = V_total;
     return dt == FLCE_BF16 ? launch_stream<__nv_bfloat16, true>(a, s)
                            : launch_stream<float, true>(a, s);
   }
@@ -749,11 +827,34 @@ extern "C" int ce_logits_bwd(const void* logits, int dt, int64_t N, int64_t V, i
     ce_bwd_rows_kernel<__nv_bfloat16, 512><<<grid, 512, 0, s>>>(
         static_cast<const __nv_bfloat16*>(logits), N, V, ld, labels, ignore_index, reduction,
         num_label_tokens, lse, n_valid, grad_loss, static_cast<__nv_bfloat16*>(grad_logits),
-        ld_grad);
+        ld_grad, v0, V_total);
   } else {
     ce_bwd_rows_kernel<float, 512><<<grid, 512, 0, s>>>(
         static_cast<const float*>(logits), N, V, ld, labels, ignore_index, reduction,
-        num_label_tokens, lse, n_valid, grad_loss, static_cast<float*>(grad_logits), ld_grad);
+        num_label_tokens, lse, n_valid, grad_loss, static_cast<float*>(grad_logits), ld_grad,
+        v0, V_total);
   }
   return launch_status("ce_bwd_rows_kernel launch");
+}
+
+extern "C" int ce_logits_bwd(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
+                             const int64_t* labels, int64_t ignore_index, int reduction,
+                             int64_t num_label_tokens, const float* lse, const int64_t* n_valid,
+                             const float* grad_loss, int inplace_grad, void* grad_logits,
+                             int64_t ld_grad, int32_t* status, flce_stream_t stream) {
+  return ce_bwd_entry(logits, dt, N, V, ld, 0, V, labels, ignore_index, reduction,
+                      num_label_tokens, lse, n_valid, grad_loss, inplace_grad, grad_logits,
+                      ld_grad, status, stream);
+}
+
+extern "C" int ce_logits_bwd_shard(const void* logits_shard, int dt, int64_t N, int64_t V_shard,
+                                   int64_t ld, int64_t vocab_offset, int64_t V_total,
+                                   const int64_t* labels, int64_t ignore_index, int reduction,
+                                   int64_t num_label_tokens, const float* lse,
+                                   const int64_t* n_valid, const float* grad_loss,
+                                   int inplace_grad, void* grad_logits, int64_t ld_grad,
+                                   int32_t* status, flce_stream_t stream) {
+  return ce_bwd_entry(logits_shard, dt, N, V_shard, ld, vocab_offset, V_total, labels,
+                      ignore_index, reduction, num_label_tokens, lse, n_valid, grad_loss,
+                      inplace_grad, grad_logits, ld_grad, status, stream);
 }

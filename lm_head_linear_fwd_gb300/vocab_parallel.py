@@ -117,6 +117,59 @@ class CudaShardOps:
         return gH, gW, gb
 
 
+class CudaLogitsShardOps(CudaShardOps):
+    """The per-rank steps of CE on a vocabulary shard of given logits."""
+
+    def partials(self, logits, _unused, labels, v0, V_total, _bias, ignore_index, status):
+        _cuda(logits, "logits")
+        if logits.dim() != 2 or logits.stride(1) != 1:
+            raise ValueError("logits shard must be 2-D with unit column stride")
+        N, V = logits.shape
+        dev = logits.device
+        m = torch.empty(N, dtype=torch.float32, device=dev)
+        s = torch.empty_like(m)
+        zy = torch.empty_like(m)
+        rc = _abi.ce_logits_fwd_shard(_ptr(logits), _dtype_code(logits), N, V, logits.stride(0),
+                                      int(v0), int(V_total), _ptr(labels), int(ignore_index),
+                                      _ptr(m), _ptr(s), _ptr(zy), _ptr(status), _stream(dev))
+        _abi.check(rc, "ce_logits_fwd_shard")
+        return m, s, zy
+
+    def logits_backward(self, logits, labels, v0, V_total, ignore_index, reduction,
+                        num_label_tokens, lse, n_valid, grad_loss, inplace_grad, status):
+        N, V = logits.shape
+        dev = logits.device
+        grad = logits if inplace_grad else torch.empty((N, V), dtype=logits.dtype, device=dev)
+        g = grad_loss.to(device=dev, dtype=torch.float32).reshape(1).contiguous()
+        rc = _abi.ce_logits_bwd_shard(_ptr(logits), _dtype_code(logits), N, V, logits.stride(0),
+                                      int(v0), int(V_total), _ptr(labels), int(ignore_index),
+                                      _red_code(reduction), _nlt(num_label_tokens), _ptr(lse),
+                                      _ptr(n_valid), _ptr(g), 1 if inplace_grad else 0,
+                                      _ptr(grad), grad.stride(0), _ptr(status), _stream(dev))
+        _abi.check(rc, "ce_logits_bwd_shard")
+        return grad
+
+
+def ce_forward(logits_shard, labels, vocab_offset, V_total, *, ignore_index=-100,
+               reduction="sum", num_label_tokens=None, exchange=None, ops=None,
+               status=None) -> ShardForward:
+    """CE on this rank's vocabulary shard of given logits, reduced over the ranks."""
+    ops = ops or CudaLogitsShardOps()
+    return forward(logits_shard, None, labels, vocab_offset, V_total, None,
+                   ignore_index=ignore_index, reduction=reduction,
+                   num_label_tokens=num_label_tokens, exchange=exchange, ops=ops, status=status)
+
+
+def ce_backward(logits_shard, labels, vocab_offset, V_total, fwd: ShardForward, grad_loss, *,
+                ignore_index=-100, reduction="sum", num_label_tokens=None, inplace_grad=False,
+                ops=None):
+    """dZ of this rank's columns (no exchange needed)."""
+    ops = ops or CudaLogitsShardOps()
+    return ops.logits_backward(logits_shard, labels, vocab_offset, V_total, ignore_index,
+                               reduction, num_label_tokens, fwd.lse, fwd.n_valid, grad_loss,
+                               inplace_grad, fwd.status)
+
+
 def forward(H, W_shard, labels, vocab_offset, V_total, bias_shard=None, *, ignore_index=-100,
             reduction="mean", num_label_tokens=None, exchange=None, ops=None,
             status=None) -> ShardForward:

@@ -62,3 +62,39 @@ def test_three_vocab_shards_match_the_oracle(reduction, nlt, bias, dtype):
     full = lh.flce_fwd(H, W, y, b, -100, reduction, nlt)
     torch.cuda.synchronize()
     assert torch.allclose(full.lse, lse, rtol=0, atol=2e-4)
+
+
+@pytest.mark.parametrize("bounds", [[(0, 1024), (1024, 2048), (2048, 3001)],
+                                    [(0, 1001), (1001, 3001)]])
+@pytest.mark.parametrize("inplace", [False, True])
+def test_ce_on_logit_shards_matches_the_oracle(bounds, inplace):
+    """Column shards of given logits (aligned and odd boundaries: both kernels)."""
+    import lm_head_linear_fwd_gb300 as lh
+    from lm_head_linear_fwd_gb300 import vocab_parallel as vp
+    c = wl.random_ce(600, 3001, torch.bfloat16, seed=77, reduction="mean")
+    c.labels[:3] = torch.tensor([0, 1000, 3000])
+    full = c.logits.cuda().contiguous()
+    y = c.labels.cuda()
+    V = c.V
+    ops = vp.CudaLogitsShardOps()
+    st = lh.new_status("cuda")
+    parts = [ops.partials(full[:, a:b], None, y, a, V, None, -100, st) for a, b in bounds]
+    m_g = torch.stack([q[0] for q in parts]).amax(0)
+    s_g = torch.stack([ops.rescale(q[0], q[1], m_g) for q in parts]).sum(0)
+    zy_g = torch.stack([q[2] for q in parts]).sum(0)
+    lse, loss, n_valid = ops.finish(m_g, s_g, zy_g, y, V, -100, "mean", None, st)
+    fwd = vp.ShardForward(loss, n_valid, lse, st)
+    work = full.clone()
+    grads = [vp.ce_backward(work[:, a:b], y, a, V, fwd, torch.tensor([0.5], device="cuda"),
+                            reduction="mean", inplace_grad=inplace) for a, b in bounds]
+    dz = torch.cat([g for g in grads], dim=1)
+    torch.cuda.synchronize()
+    lh.check_status(st)
+    ref = oracle.ce_forward(c.logits, c.labels, -100, "mean")
+    assert int(n_valid.item()) == ref["n_valid"]
+    assert abs(loss.item() - ref["loss"]) <= 1e-3 * abs(ref["loss"])
+    got = lse.cpu().double().numpy()
+    assert np.all(np.abs(got - ref["lse"]) <= 5e-5 * (1 + np.abs(ref["lse"])))
+    _grad_ok(dz, oracle.ce_backward(c.logits, c.labels, -100, "mean", grad_loss=0.5), "dZ")
+    if inplace:
+        assert torch.equal(work, dz)
