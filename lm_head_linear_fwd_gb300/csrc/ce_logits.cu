@@ -264,17 +264,29 @@ __global__ void __launch_bounds__(THREADS) ce_bwd_rows_kernel(
 // ------------------------------------------------ bulk-copy (TMA) row streaming
 
 // Rows whose start and length are 16-byte multiples are streamed through a
-// shared-memory ring instead: one producer thread copies 16 KB row segments
-// with cp.async.bulk (a 4-stage mbarrier ring, so up to 64 KB per CTA is in
-// flight without holding registers), and 8 consumer warps reduce (forward) or
-// transform and store (backward) each segment from shared memory.
-constexpr int kSegBytes = 16384;
-constexpr int kRingStages = 4;
+// shared-memory ring instead: one producer thread copies 32 KB row segments
+// with cp.async.bulk (a 2-stage mbarrier ring, so up to 64 KB per CTA is in
+// flight without holding registers; 3 CTAs per SM), and 8 consumer warps
+// reduce (forward) or transform and store (backward) each segment from shared
+// memory.  The segment size, stage count and CTAs per SM were chosen by a
+// sweep on GB300 (16-32 KB segments, 2-8 stages, 2-4 CTAs per SM).
+#ifndef FLCE_CE_SEG_BYTES
+#define FLCE_CE_SEG_BYTES 32768
+#endif
+#ifndef FLCE_CE_STAGES
+#define FLCE_CE_STAGES 2
+#endif
+#ifndef FLCE_CE_CTAS_PER_SM
+#define FLCE_CE_CTAS_PER_SM 3
+#endif
+constexpr int kSegBytes = FLCE_CE_SEG_BYTES;
+constexpr int kRingStages = FLCE_CE_STAGES;
 constexpr int kConsumers = 256;
 constexpr int kConsumerWarps = kConsumers / 32;
 constexpr int kStreamThreads = kConsumers + 32;
 constexpr int kStreamSmem = kRingStages * kSegBytes + 128;
-constexpr int kStreamCtasPerSm = 3;
+constexpr int kStreamCtasPerSm = FLCE_CE_CTAS_PER_SM;
+static_assert(kSegBytes % (16 * kConsumers) == 0, "whole 16-byte vectors per consumer");
 
 struct StreamArgs {
   const void* logits;
