@@ -20,7 +20,16 @@
 //      the addmm with beta = 1 of the same page, chunk after chunk.
 // The tf32 tensor-core path (fp32 inputs) reads K-major operands only, so for
 // fp32 the MN-major operands of steps 3 and 4 are first transposed into the
-// workspace (W once per call, dZ and H[chunk] once per chunk).
+// workspace (W once per call, dZ and H[chunk] once per chunk).  When a chunk
+// has too few grad_H tiles to fill the GPU, step 3 splits its long K (= V)
+// and reduces the fp32 partials in a fixed order.  grad_W runs on CTA pairs
+// (tc_gemm_pair_kernel) by default; flce_gemm_set_pair selects per contraction.
+//
+// Also here: the fused forward + backward (flce_fwd_bwd: the forward epilogue
+// keeps the chunk's logits as offsets from each tile's maximum, dZ is formed
+// from them in place, 6NDV flops in all), the vocabulary-parallel entry points
+// (flce_fwd_shard / flce_bwd_shard and the rescale / finish kernels of the
+// cross-rank merge) and the raw contraction flce_gemm.
 #include <math.h>
 #include <stdio.h>
 
@@ -37,11 +46,6 @@
 namespace flce {
 
 // ----------------------------------------------------------------- epilogues
-
-template <typename T>
-__device__ __forceinline__ float load_elem(const void* p, int64_t i) {
-  return Elem<T>::load(static_cast<const T*>(p) + i);
-}
 
 // v[j] += bias[col0 + j] for the columns inside the vocabulary: 16-byte loads
 // when all 32 columns are inside and aligned (the address is the same for the

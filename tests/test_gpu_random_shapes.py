@@ -1,0 +1,82 @@
+"""Seeded random shapes for both paths (recomputing and fused FLCE, CE on
+logits) against the fp64 oracle: sizes drawn across tile, chunk and vector
+boundaries, random dtype, bias, reduction and chunk.  Tolerances as in
+tests/test_gpu_flce.py and tests/test_gpu_ce_logits.py."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+CASES = []
+_rng = np.random.default_rng(2026)
+for i in range(12):
+    CASES.append(dict(
+        N=int(_rng.integers(1, 1500)),
+        D=int(_rng.integers(1, 80)) * 8,
+        V=int(_rng.integers(2, 9000)),
+        dtype=torch.bfloat16 if _rng.random() < 0.75 else torch.float32,
+        bias=bool(_rng.random() < 0.5),
+        reduction=str(_rng.choice(["sum", "mean"])),
+        nlt=None if _rng.random() < 0.7 else int(_rng.integers(0, 2000)),
+        chunk=None if _rng.random() < 0.5 else int(_rng.integers(1, 8)) * 128,
+        seed=1000 + i))
+
+
+def _grad_ok(got, want, name):
+    mr = oracle.max_rel_err(got.float().cpu(), want)
+    nw = oracle.normwise_err(got.float().cpu(), want)
+    assert mr <= 2e-2 and nw <= 5e-3, (name, mr, nw)
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"{c['N']}x{c['D']}x{c['V']}" for c in CASES])
+def test_flce_random_shape(case):
+    import lm_head_linear_fwd_gb300 as lh
+    p = wl.random_flce(case["N"], case["D"], case["V"], case["dtype"], bias=case["bias"],
+                       seed=case["seed"], reduction=case["reduction"],
+                       num_label_tokens=case["nlt"], w_std=0.05)
+    H, W, y = p.H.cuda(), p.W.cuda(), p.labels.cuda()
+    b = p.bias.cuda() if p.bias is not None else None
+    ref = oracle.flce_forward(p.H, p.W, p.bias, p.labels, -100, p.reduction, p.num_label_tokens)
+    gr = oracle.flce_backward(p.H, p.W, p.bias, p.labels, -100, p.reduction, p.num_label_tokens)
+    out = lh.flce_fwd(H, W, y, b, -100, p.reduction, p.num_label_tokens)
+    bw = lh.flce_bwd(H, W, y, out.lse, out.n_valid, torch.ones(1, device="cuda"), b, -100,
+                     p.reduction, p.num_label_tokens, case["chunk"])
+    fo, fb = lh.flce_fwd_bwd(H, W, y, b, -100, p.reduction, p.num_label_tokens, case["chunk"])
+    torch.cuda.synchronize()
+    lh.check_status(out.status)
+    lh.check_status(fo.status)
+    for o in (out, fo):
+        assert int(o.n_valid.item()) == ref["n_valid"]
+        assert abs(o.loss.item() - ref["loss"]) <= 1e-3 * abs(ref["loss"]) + 1e-6
+    if ref["loss"] == 0.0:
+        return
+    for g in (bw, fb):
+        _grad_ok(g.grad_H, gr["grad_H"], "grad_H")
+        _grad_ok(g.grad_W, gr["grad_W"], "grad_W")
+        if b is not None:
+            _grad_ok(g.grad_bias, gr["grad_b"], "grad_b")
+
+
+@pytest.mark.parametrize("case", CASES[:8], ids=[f"{c['N']}x{c['V']}" for c in CASES[:8]])
+def test_ce_random_shape(case):
+    import lm_head_linear_fwd_gb300 as lh
+    ld = case["V"] + (0 if case["seed"] % 2 else int(case["seed"] % 13))
+    c = wl.random_ce(case["N"], case["V"], case["dtype"], seed=case["seed"], ld=ld,
+                     reduction=case["reduction"], num_label_tokens=case["nlt"])
+    logits, y = c.logits.cuda(), c.labels.cuda()
+    out = lh.ce_logits_fwd(logits, y, -100, c.reduction, c.num_label_tokens)
+    grad = lh.ce_logits_bwd(logits, y, out.lse, out.n_valid, torch.ones(1, device="cuda"), -100,
+                            c.reduction, c.num_label_tokens)
+    torch.cuda.synchronize()
+    ref = oracle.ce_forward(c.logits, c.labels, -100, c.reduction, c.num_label_tokens)
+    assert int(out.n_valid.item()) == ref["n_valid"]
+    assert abs(out.loss.item() - ref["loss"]) <= 1e-3 * abs(ref["loss"]) + 1e-6
+    lse = out.lse.cpu().double().numpy()
+    assert np.all(np.abs(lse - ref["lse"]) <= 5e-5 * (1 + np.abs(ref["lse"])))
+    if ref["loss"] != 0.0:
+        _grad_ok(grad, oracle.ce_backward(c.logits, c.labels, -100, c.reduction,
+                                          c.num_label_tokens), "dZ")
