@@ -33,11 +33,13 @@ sys.path.insert(0, ROOT)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per FLCE fwd+bwd step
-# of the default workload, from the ncu launch list summarised in
-# profiles/flce_llama3_8b_launch_list.md, valid only for the kernel sources it
-# was taken from (sha256 prefix below); any change to them reports null.
-TRAFFIC = {"flce_step_bytes": 30.21e9, "csrc_sha": "76db89267ce67470"}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per step of the
+# default workloads (FLCE fwd+bwd; CE fwd + in-place bwd), from the ncu launch
+# lists summarised in profiles/flce_llama3_8b_launch_list.md and
+# profiles/ce_logits_16384x128256_launch_list_and_full_set.md, valid only for
+# the kernel sources they were taken from (sha256 prefix below); any change to
+# them reports null.
+TRAFFIC = {"flce_step_bytes": 30.00e9, "ce_step_bytes": 12.56e9, "csrc_sha": "c05270e0c8272300"}
 
 
 def csrc_sha():
@@ -529,7 +531,10 @@ def run_ours(args, rank, ws, local):
             "peak": peaks["hbm_gbs"],
             "unit": "GB/s",
             "frac": round(ce_gbs / peaks["hbm_gbs"], 4),
-            "traffic": None,
+            "traffic": (TRAFFIC["ce_step_bytes"]
+                        if (args.ce_rows == 16384 and csrc_sha() == TRAFFIC["csrc_sha"])
+                        else None),
+            "traffic_unit": "bytes per step (CE fwd + bwd kernels, ncu)",
             "peak_source": f"hbm_gbs ({peak_src})",
         },
         "e2e": {
