@@ -444,7 +444,37 @@ def run_ours(args, rank, ws, local):
     ce_bytes = 3.0 * c.N * c.V * 2  # fwd read + bwd read + bwd write of the bf16 logits
     ce_N = c.N
     ce_gbs = ce_bytes / (ce_ms * 1e-3) / 1e9
-    del pristine, logits, c, cws, co
+
+    # the backward alone, with the saved lse and without it (out of place)
+    restore()
+    gbuf = torch.empty_like(logits)
+    n_valid_rows = int((labels != c.ignore_index).sum().item())
+
+    def bwd(lse):
+        return lambda: lh.ce_logits_bwd(logits, labels, lse, co.n_valid, one, c.ignore_index,
+                                        c.reduction, c.num_label_tokens, grad_logits=gbuf,
+                                        status=cst)
+    bwd_ms = {}
+    for name, fn in (("saved_lse", bwd(co.lse)), ("no_lse", bwd(None))):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        t = _events_time(fn, args.steps, stream)
+        bwd_ms[name] = max_over_ranks(sum(t) / len(t), ws)
+    lh.check_status(cst, "ce_logits_bwd")
+    # the saved-lse kernel reads every row; the no-lse kernel skips ignored rows
+    row_b = c.V * 2
+    bwd_bytes = {"saved_lse": 2.0 * c.N * row_b,
+                 "no_lse": (n_valid_rows + c.N) * float(row_b)}
+    ce_bwd_line = {
+        name: {"ms": round(bwd_ms[name], 4),
+               "gb_s": round(bwd_bytes[name] / (bwd_ms[name] * 1e-3) / 1e9, 1),
+               "frac_of_hbm": round(bwd_bytes[name] / (bwd_ms[name] * 1e-3) / 1e9 /
+                                    peaks["hbm_gbs"], 4)}
+        for name in bwd_ms}
+    ce_bwd_line["bytes"] = ("saved_lse: read + write of every row; no_lse: read of the "
+                            f"{n_valid_rows} non-ignored rows + write of all {c.N} rows "
+                            "(a row cluster holds each row in shared memory: one read)")
+    del pristine, logits, c, cws, co, gbuf
     torch.cuda.empty_cache()
 
     # ------------------------------------------------- latency-bound workloads
@@ -501,6 +531,7 @@ def run_ours(args, rank, ws, local):
             "frac_of_8tbs": round(ce_gbs / 8000.0, 4),
             "peak_extra_gib": round(ce_peak_extra / 2**30, 6),
             "tokens_per_s": round(ce_N * ws / (ce_ms * 1e-3), 1),
+            "bwd_only": ce_bwd_line,
         },
         "roofline": {
             "bound": "tensor",

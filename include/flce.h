@@ -121,6 +121,13 @@ FLCE_API int ce_logits_fwd(const void* logits, int dt, int64_t N, int64_t V, int
                   float* loss_rows, float* label_logit, void* ws, size_t ws_bytes,
                   int32_t* status, flce_stream_t stream);
 
+/* Self-test of the failure path: launches one warp that waits, with the same
+ * bounded mbarrier wait every kernel of this library uses, on a barrier that
+ * nothing arrives on.  After limit_ns (at most 2 s) the wait gives up and
+ * FLCE_ETIMEOUT is written to *status; the kernel returns normally and the
+ * context stays usable.  The source pages have no counterpart. */
+FLCE_API int flce_wait_selftest(int32_t* status, uint64_t limit_ns, flce_stream_t stream);
+
 /* Label masking for packed sequences: labels and doc_ids are [B, T] int64
  * (device, row-major); doc_ids holds 1, 2, ... for the packed documents of a
  * row and 0 for padding (the indexed packing mask of Automodel PR #2996,
@@ -169,7 +176,17 @@ FLCE_API int ce_logits_fwd_noalloc(const void* logits, int dt, int64_t N, int64_
  * grad_logits [N, ld_grad] of dtype dt (first V columns of each row).
  * inplace_grad != 0: grad_logits must equal logits and ld_grad == ld; the
  * logits are overwritten by their gradient (Automodel PR #2996, inplace_grad).
- * inplace_grad == 0: grad_logits must not overlap the logits. */
+ * inplace_grad == 0: grad_logits must not overlap the logits.
+ *
+ * lse may be NULL: the backward that keeps only the logits and the labels
+ * from the forward (Automodel PR #2996, the memory bullet: nothing but the
+ * inputs is saved).  Each row's lse is then formed again inside the kernel.
+ * Rows whose start, stride and length are 16-byte multiples and whose
+ * length is at most 8 x 64 KiB (V <= 262144 bf16, 131072 f32) are split over a
+ * thread-block cluster that holds the row in shared memory, so the logits are
+ * still read once; longer rows, and rows that are not 16-byte aligned, are
+ * read twice.  The result equals the saved-lse backward up to the rounding of
+ * the recomputed lse (fp32, a few ulp). */
 FLCE_API int ce_logits_bwd(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
                   const int64_t* labels, int64_t ignore_index, int reduction,
                   int64_t num_label_tokens, const float* lse, const int64_t* n_valid,

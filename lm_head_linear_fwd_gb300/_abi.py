@@ -59,6 +59,7 @@ _SIGNATURES = {
                           _p, _p, _p, _p, _i, _p, _p, _sz, _p, _p]),
     "flce_grad_scale": (_i, [_p, _i, _i64, _p, _p]),
     "flce_count_valid": (_i, [_p, _i64, _i64, _i64, _p, _p]),
+    "flce_wait_selftest": (_i, [_p, ctypes.c_uint64, _p]),
     "flce_mask_packed_labels": (_i, [_p, _p, _i64, _i64, _i64, _p]),
     "flce_gemm_set_pair": (_i, [_i]),
     "flce_gemm_pair_slots": (_i, []),
@@ -134,6 +135,7 @@ ce_logits_bwd_shard = _call("ce_logits_bwd_shard")
 flce_fwd_bwd = _call("flce_fwd_bwd")
 flce_grad_scale = _call("flce_grad_scale")
 flce_count_valid = _call("flce_count_valid")
+flce_wait_selftest = _call("flce_wait_selftest")
 flce_mask_packed_labels = _call("flce_mask_packed_labels")
 flce_gemm_set_pair = _call("flce_gemm_set_pair")
 flce_gemm_pair_slots = _call("flce_gemm_pair_slots")

@@ -129,6 +129,8 @@ def ce_logits_fwd(logits, labels, ignore_index=-100, reduction="sum", num_label_
 def ce_logits_bwd(logits, labels, lse, n_valid, grad_loss, ignore_index=-100, reduction="sum",
                   num_label_tokens=None, inplace_grad=False, grad_logits=None,
                   status=None) -> torch.Tensor:
+    """Gradient of the loss with respect to the logits.  ``lse=None``: no saved
+    lse, each row's lse is formed again from the logits in the kernel."""
     _cuda(logits, "logits")
     N, V = logits.shape
     labels = _labels(labels, N)
@@ -152,9 +154,14 @@ def ce_logits_bwd(logits, labels, lse, n_valid, grad_loss, ignore_index=-100, re
 
 class _CELogits(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, logits, labels, ignore_index, reduction, num_label_tokens, inplace_grad):
+    def forward(ctx, logits, labels, ignore_index, reduction, num_label_tokens, inplace_grad,
+                save_lse=True):
         out = ce_logits_fwd(logits, labels, ignore_index, reduction, num_label_tokens)
-        ctx.save_for_backward(logits, labels, out.lse, out.n_valid)
+        ctx.save_lse = save_lse
+        if save_lse:
+            ctx.save_for_backward(logits, labels, out.lse, out.n_valid)
+        else:  # the backward forms the lse again from the logits
+            ctx.save_for_backward(logits, labels, out.n_valid)
         ctx.args = (ignore_index, reduction, num_label_tokens, inplace_grad)
         ctx.status = out.status
         ctx.consumed = False
@@ -163,7 +170,10 @@ class _CELogits(torch.autograd.Function):
     @staticmethod
     @once_differentiable
     def backward(ctx, g):
-        logits, labels, lse, n_valid = ctx.saved_tensors
+        if ctx.save_lse:
+            logits, labels, lse, n_valid = ctx.saved_tensors
+        else:
+            (logits, labels, n_valid), lse = ctx.saved_tensors, None
         ignore_index, reduction, nlt, inplace = ctx.args
         if inplace and ctx.consumed:
             raise RuntimeError("ce_logits(inplace_grad=True): the logits were already overwritten "
@@ -171,7 +181,7 @@ class _CELogits(torch.autograd.Function):
         ctx.consumed = True
         grad = ce_logits_bwd(logits, labels, lse, n_valid, g, ignore_index, reduction, nlt,
                              inplace_grad=inplace, status=ctx.status)
-        return grad, None, None, None, None, None
+        return grad, None, None, None, None, None, None
 
 
 def _fold_mask(labels, mask, ignore_index):
@@ -181,15 +191,17 @@ def _fold_mask(labels, mask, ignore_index):
 
 
 def ce_logits(logits, labels, *, ignore_index=-100, reduction="sum", num_label_tokens=None,
-              inplace_grad=False, mask=None):
+              inplace_grad=False, mask=None, save_lse=True):
     """Masked cross-entropy on given logits [N, V] (bf16 or fp32).
 
     ``inplace_grad=True`` writes the gradient into the logits storage during
     backward (the logits are destroyed); it is keyword-only and off by default.
-    ``mask`` (same shape as labels) marks rows to ignore with 0."""
+    ``mask`` (same shape as labels) marks rows to ignore with 0.
+    ``save_lse=False`` keeps only the logits and labels (and the valid-row
+    count) for the backward, which then forms each row's lse again."""
     labels = _fold_mask(labels, mask, ignore_index)
     return _CELogits.apply(logits, labels, int(ignore_index), reduction, num_label_tokens,
-                           bool(inplace_grad))
+                           bool(inplace_grad), bool(save_lse))
 
 
 def mask_packed_labels(labels: torch.Tensor, doc_ids: torch.Tensor, ignore_index: int = -100):

@@ -56,67 +56,78 @@ struct ShardOut {
 
 // ---------------------------------------------------------------- forward kernel
 
+// Base-2 log-sum-exp state of one row p[0..V) over the block: every thread
+// reduces a strided share (16-byte vector loads; a scalar head and tail when
+// the row start is not 16-byte aligned), warps merge by shuffles, and each
+// thread then merges the warp states in the same order, so all threads return
+// the same state.  red_m/red_s hold THREADS/32 entries and are free again on
+// return.
+template <typename T, int THREADS>
+__device__ Lse2 block_row_lse2(const T* p, int64_t V, float* red_m, float* red_s) {
+  constexpr int EPV = Elem<T>::kPerVec;
+  constexpr int UNROLL = (EPV == 8) ? 4 : 8;  // 32 elements per batch
+  constexpr int NW = THREADS / 32;
+  const int tid = threadIdx.x;
+  Lse2 st;
+  int64_t head = static_cast<int64_t>(((16u - (reinterpret_cast<uintptr_t>(p) & 15u)) & 15u) /
+                                      sizeof(T));
+  if (head > V) head = V;
+  for (int64_t j = tid; j < head; j += THREADS) st.add1(Elem<T>::load(p + j) * kLog2e);
+  const uint4* vp = reinterpret_cast<const uint4*>(p + head);
+  const int64_t nvec = (V - head) / EPV;
+  int64_t v = tid;
+  for (; v + (UNROLL - 1) * THREADS < nvec; v += UNROLL * THREADS) {
+    uint4 u[UNROLL];
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) u[k] = __ldcs(vp + v + k * THREADS);
+    float t[UNROLL * EPV];
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) {
+      float x[EPV];
+      Elem<T>::unpack(u[k], x);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) t[k * EPV + e] = x[e] * kLog2e;
+    }
+    st.addk(t);
+  }
+  for (; v < nvec; v += THREADS) {
+    float x[EPV];
+    Elem<T>::unpack(__ldcs(vp + v), x);
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) x[e] *= kLog2e;
+    st.addk(x);
+  }
+  for (int64_t j = head + nvec * EPV + tid; j < V; j += THREADS)
+    st.add1(Elem<T>::load(p + j) * kLog2e);
+
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, st.m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, st.s, o);
+    st.merge(m2, s2);
+  }
+  if ((tid & 31) == 0) {
+    red_m[tid >> 5] = st.m;
+    red_s[tid >> 5] = st.s;
+  }
+  __syncthreads();
+  Lse2 all;
+  for (int w = 0; w < NW; ++w) all.merge(red_m[w], red_s[w]);
+  __syncthreads();
+  return all;
+}
+
 template <typename T, int THREADS>
 __global__ void __launch_bounds__(THREADS) ce_fwd_rows_kernel(
     const T* __restrict__ logits, int64_t N, int64_t V, int64_t ld,
     const int64_t* __restrict__ labels, int64_t ignore_index, float* __restrict__ lse_out,
     float* __restrict__ loss_rows, float* __restrict__ label_logit, int32_t* status,
     ShardOut sh) {
-  constexpr int EPV = Elem<T>::kPerVec;
-  constexpr int UNROLL = (EPV == 8) ? 4 : 8;  // 32 elements per batch
-  constexpr int NW = THREADS / 32;
-  __shared__ float red_m[NW], red_s[NW];
-  const int tid = threadIdx.x;
-
+  __shared__ float red_m[THREADS / 32], red_s[THREADS / 32];
   for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
     const T* p = logits + row * ld;
-    Lse2 st;
-    int64_t head = static_cast<int64_t>(((16u - (reinterpret_cast<uintptr_t>(p) & 15u)) & 15u) /
-                                        sizeof(T));
-    if (head > V) head = V;
-    for (int64_t j = tid; j < head; j += THREADS) st.add1(Elem<T>::load(p + j) * kLog2e);
-    const uint4* vp = reinterpret_cast<const uint4*>(p + head);
-    const int64_t nvec = (V - head) / EPV;
-    int64_t v = tid;
-    for (; v + (UNROLL - 1) * THREADS < nvec; v += UNROLL * THREADS) {
-      uint4 u[UNROLL];
-#pragma unroll
-      for (int k = 0; k < UNROLL; ++k) u[k] = __ldcs(vp + v + k * THREADS);
-      float t[UNROLL * EPV];
-#pragma unroll
-      for (int k = 0; k < UNROLL; ++k) {
-        float x[EPV];
-        Elem<T>::unpack(u[k], x);
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) t[k * EPV + e] = x[e] * kLog2e;
-      }
-      st.addk(t);
-    }
-    for (; v < nvec; v += THREADS) {
-      float x[EPV];
-      Elem<T>::unpack(__ldcs(vp + v), x);
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) x[e] *= kLog2e;
-      st.addk(x);
-    }
-    for (int64_t j = head + nvec * EPV + tid; j < V; j += THREADS)
-      st.add1(Elem<T>::load(p + j) * kLog2e);
-
-    // warp merge, then across warps
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, st.m, o);
-      const float s2 = __shfl_xor_sync(0xffffffffu, st.s, o);
-      st.merge(m2, s2);
-    }
-    if ((tid & 31) == 0) {
-      red_m[tid >> 5] = st.m;
-      red_s[tid >> 5] = st.s;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      Lse2 all;
-      for (int w = 0; w < NW; ++w) all.merge(red_m[w], red_s[w]);
+    const Lse2 all = block_row_lse2<T, THREADS>(p, V, red_m, red_s);
+    if (threadIdx.x == 0) {
       const int64_t y = labels[row];
       if (sh.m_out != nullptr) {
         sh.write(row, all.m, all.s, y, ignore_index, V, p, status);
@@ -136,7 +147,6 @@ __global__ void __launch_bounds__(THREADS) ce_fwd_rows_kernel(
         if (label_logit != nullptr) label_logit[row] = zy;
       }
     }
-    __syncthreads();
   }
 }
 
@@ -197,6 +207,7 @@ __global__ void __launch_bounds__(THREADS) ce_bwd_rows_kernel(
     int64_t V_total) {
   constexpr int EPV = Elem<T>::kPerVec;
   constexpr int UNROLL = 4;
+  __shared__ float red_m[THREADS / 32], red_s[THREADS / 32];
   const float coef = grad_coef(reduction, num_label_tokens, n_valid, grad_loss);
   const int tid = threadIdx.x;
 
@@ -207,7 +218,15 @@ __global__ void __launch_bounds__(THREADS) ce_bwd_rows_kernel(
     const bool valid = (yg != ignore_index) && label_ok(yg, V_total);
     const int64_t y = valid ? yg - v0 : -1;  // label column within this shard (or none)
     const float c = valid ? coef : 0.0f;
-    const float lse2 = lse[row] * kLog2e;
+    float lse2;
+    if (lse != nullptr) {
+      lse2 = lse[row] * kLog2e;
+    } else if (c != 0.0f) {  // no saved lse: a reduction pass over the row first
+      const Lse2 all = block_row_lse2<T, THREADS>(p, V, red_m, red_s);
+      lse2 = all.m + log2f(all.s);
+    } else {
+      lse2 = 0.0f;  // the row's gradient is zero
+    }
     const uintptr_t pa = reinterpret_cast<uintptr_t>(p) & 15u;
     const uintptr_t qa = reinterpret_cast<uintptr_t>(q) & 15u;
     int64_t head = (pa == qa) ? static_cast<int64_t>(((16u - pa) & 15u) / sizeof(T)) : V;
@@ -288,6 +307,96 @@ constexpr int kStreamSmem = kRingStages * kSegBytes + 128;
 constexpr int kStreamCtasPerSm = FLCE_CE_CTAS_PER_SM;
 static_assert(kSegBytes % (16 * kConsumers) == 0, "whole 16-byte vectors per consumer");
 
+// Adds K vectors sv[first + k*STRIDE] (those below nvec) of a row held in
+// shared memory to a base-2 log-sum-exp state.  bf16 takes the batch maximum on
+// packed pairs (exact), then one FFMA, one ex2 and one add per element.
+template <typename T, int K, int STRIDE>
+__device__ __forceinline__ void lse_add_smem(const uint4* sv, int first, int nvec, Lse2& st) {
+  constexpr int EPV = Elem<T>::kPerVec;
+  if (sizeof(T) == 2) {
+    uint4 u[K];
+    __nv_bfloat162 mx = __float2bfloat162_rn(-INFINITY);
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int v = first + k * STRIDE;
+      if (v < nvec) {
+        u[k] = sv[v];
+        mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&u[k].x));
+        mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&u[k].y));
+        mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&u[k].z));
+        mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&u[k].w));
+      }
+    }
+    const float bm = fmaxf(__low2float(mx), __high2float(mx)) * kLog2e;  // monotone
+    if (bm > st.m) {
+      st.s *= ex2(st.m - bm);
+      st.m = bm;
+    }
+    if (st.m != -INFINITY) {
+      float acc = 0.0f;
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        const int v = first + k * STRIDE;
+        if (v < nvec) {
+          float x[EPV];
+          Elem<T>::unpack(u[k], x);
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) acc += ex2(fmaf(x[e], kLog2e, -st.m));
+        }
+      }
+      st.s += acc;
+    }
+  } else {
+    float t[K * EPV];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int v = first + k * STRIDE;
+      if (v < nvec) {
+        float x[EPV];
+        Elem<T>::unpack(sv[v], x);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) t[k * EPV + e] = x[e] * kLog2e;
+      } else {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) t[k * EPV + e] = -INFINITY;
+      }
+    }
+    st.addk(t);
+  }
+}
+
+// Writes dZ = c * (2^(x*log2e - lse2) - onehot) for K vectors sv[first +
+// k*STRIDE] (those below nvec) to out[v]; ylocal is the label's element index
+// relative to sv[0] (out of range when the label lies elsewhere).  c == 0
+// writes zeros.
+template <typename T, int K, int STRIDE>
+__device__ __forceinline__ void dz_from_smem(const uint4* sv, int first, int nvec, int64_t ylocal,
+                                             float lse2, float c, uint4* out) {
+  constexpr int EPV = Elem<T>::kPerVec;
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    const int v = first + k * STRIDE;
+    if (v < nvec) {
+      float x[EPV];
+      Elem<T>::unpack(sv[v], x);
+      const int64_t j0 = static_cast<int64_t>(v) * EPV;
+      if (c == 0.0f) {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) x[e] = 0.0f;
+      } else {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) x[e] = ex2(fmaf(x[e], kLog2e, -lse2)) * c;
+        if (static_cast<uint64_t>(ylocal - j0) < static_cast<uint64_t>(EPV)) {
+#pragma unroll
+          for (int e = 0; e < EPV; ++e)
+            if (j0 + e == ylocal) x[e] -= c;  // the one-hot label term
+        }
+      }
+      __stcs(out + v, Elem<T>::pack(x));
+    }
+  }
+}
+
 struct StreamArgs {
   const void* logits;
   int64_t N, V, ld;
@@ -312,11 +421,13 @@ struct StreamArgs {
   ShardOut sh;
 };
 
-template <typename T, bool kBwd>
-__global__ void __launch_bounds__(kStreamThreads) ce_stream_kernel(const StreamArgs a) {
+// kTwoPass (backward only): no saved lse, each row is streamed twice.
+template <typename T, bool kBwd, bool kTwoPass = false>
+__global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm)
+    ce_stream_kernel(const StreamArgs a) {
   constexpr int EPV = Elem<T>::kPerVec;
   constexpr int kVecPerSeg = kSegBytes / 16;
-  constexpr int kVecPerThread = kVecPerSeg / kConsumers;  // 4
+  constexpr int kVecPerThread = kVecPerSeg / kConsumers;  // 8 (32 KB segments)
   extern __shared__ uint8_t ring_raw[];
   __shared__ uint64_t full_bar[kRingStages], empty_bar[kRingStages];
   __shared__ int abort_sh;
@@ -345,10 +456,12 @@ __global__ void __launch_bounds__(kStreamThreads) ce_stream_kernel(const StreamA
       uint32_t stage = 0, phase = 0;
       int issued = 0;
       bool ok = true;
+      constexpr int npass = (kBwd && kTwoPass) ? 2 : 1;
       for (int64_t row = blockIdx.x; row < a.N && ok; row += gridDim.x) {
         const char* src = reinterpret_cast<const char*>(static_cast<const T*>(a.logits) +
                                                         row * a.ld);
-        for (int sg = 0; sg < nseg; ++sg) {
+        for (int it = 0; it < npass * nseg && ok; ++it) {
+          const int sg = it % nseg;
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
@@ -387,6 +500,9 @@ __global__ void __launch_bounds__(kStreamThreads) ce_stream_kernel(const StreamA
   // --------------------------------------------------------------- consumers
   float coef = 0.0f;
   if (kBwd) coef = grad_coef(a.reduction, a.num_label_tokens, a.n_valid, a.grad_loss);
+  // backward without a saved lse: every row is streamed twice, a reduction
+  // pass (as the forward) and then the transform pass
+  constexpr int npass = (kBwd && kTwoPass) ? 2 : 1;
   uint32_t stage = 0, phase = 0;
   for (int64_t row = blockIdx.x; row < a.N; row += gridDim.x) {
     const int64_t yg = a.labels[row];
@@ -395,105 +511,36 @@ __global__ void __launch_bounds__(kStreamThreads) ce_stream_kernel(const StreamA
     float c = 0.0f, lse2 = 0.0f;
     if (kBwd) {
       c = valid ? coef : 0.0f;
-      lse2 = a.lse_in[row] * kLog2e;
+      if (!kTwoPass) lse2 = a.lse_in[row] * kLog2e;
     }
     T* out = kBwd ? static_cast<T*>(a.grad) + row * a.ldg : nullptr;
-    Lse2 st;
-    for (int sg = 0; sg < nseg; ++sg) {
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait(&full_bar[stage], phase, abort_flag) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (ok) {
-        const int64_t e0 = static_cast<int64_t>(sg) * seg_elems;
-        const int nvec = static_cast<int>(
-            min(static_cast<int64_t>(kSegBytes), row_bytes - static_cast<int64_t>(sg) * kSegBytes) / 16);
-        const uint4* sv = reinterpret_cast<const uint4*>(ring + stage * kSegBytes);
-        if (!kBwd && sizeof(T) == 2) {
-          // bf16: the batch maximum on packed pairs (exact), then one FFMA,
-          // one ex2 and one add per element
-          uint4 u[kVecPerThread];
-          __nv_bfloat162 mx = __float2bfloat162_rn(-INFINITY);
-#pragma unroll
-          for (int k = 0; k < kVecPerThread; ++k) {
-            const int v = tid + k * kConsumers;
-            if (v < nvec) {
-              u[k] = sv[v];
-              mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&u[k].x));
-              mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&u[k].y));
-              mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&u[k].z));
-              mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&u[k].w));
-            }
-          }
-          const float bm =
-              fmaxf(__low2float(mx), __high2float(mx)) * kLog2e;  // monotone: max of x*log2e
-          if (bm > st.m) {
-            st.s *= ex2(st.m - bm);
-            st.m = bm;
-          }
-          if (st.m != -INFINITY) {
-            float acc = 0.0f;
-#pragma unroll
-            for (int k = 0; k < kVecPerThread; ++k) {
-              const int v = tid + k * kConsumers;
-              if (v < nvec) {
-                float x[EPV];
-                Elem<T>::unpack(u[k], x);
-#pragma unroll
-                for (int e = 0; e < EPV; ++e) acc += ex2(fmaf(x[e], kLog2e, -st.m));
-              }
-            }
-            st.s += acc;
-          }
-        } else if (!kBwd) {
-          float t[kVecPerThread * EPV];
-#pragma unroll
-          for (int k = 0; k < kVecPerThread; ++k) {
-            const int v = tid + k * kConsumers;
-            if (v < nvec) {
-              float x[EPV];
-              Elem<T>::unpack(sv[v], x);
-#pragma unroll
-              for (int e = 0; e < EPV; ++e) t[k * EPV + e] = x[e] * kLog2e;
-            } else {
-#pragma unroll
-              for (int e = 0; e < EPV; ++e) t[k * EPV + e] = -INFINITY;
-            }
-          }
-          st.addk(t);
-        } else {
-          const int64_t ylocal = y - e0;
-#pragma unroll
-          for (int k = 0; k < kVecPerThread; ++k) {
-            const int v = tid + k * kConsumers;
-            if (v < nvec) {
-              float x[EPV];
-              Elem<T>::unpack(sv[v], x);
-              const int64_t j0 = static_cast<int64_t>(v) * EPV;
-              if (c == 0.0f) {
-#pragma unroll
-                for (int e = 0; e < EPV; ++e) x[e] = 0.0f;
-              } else {
-#pragma unroll
-                for (int e = 0; e < EPV; ++e) x[e] = ex2(fmaf(x[e], kLog2e, -lse2)) * c;
-                if (static_cast<uint64_t>(ylocal - j0) < static_cast<uint64_t>(EPV)) {
-#pragma unroll
-                  for (int e = 0; e < EPV; ++e)
-                    if (j0 + e == ylocal) x[e] -= c;  // the one-hot label term
-                }
-              }
-              __stcs(reinterpret_cast<uint4*>(out + e0) + v, Elem<T>::pack(x));
-            }
-          }
+    for (int pass = 0; pass < npass; ++pass) {
+      const bool reduce_pass = !kBwd || pass + 1 < npass;
+      Lse2 st;
+      for (int sg = 0; sg < nseg; ++sg) {
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(&full_bar[stage], phase, abort_flag) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok) {
+          const int64_t e0 = static_cast<int64_t>(sg) * seg_elems;
+          const int nvec = static_cast<int>(
+              min(static_cast<int64_t>(kSegBytes), row_bytes - static_cast<int64_t>(sg) * kSegBytes) /
+              16);
+          const uint4* sv = reinterpret_cast<const uint4*>(ring + stage * kSegBytes);
+          if (reduce_pass)
+            lse_add_smem<T, kVecPerThread, kConsumers>(sv, tid, nvec, st);
+          else
+            dz_from_smem<T, kVecPerThread, kConsumers>(sv, tid, nvec, y - e0, lse2, c,
+                                                       reinterpret_cast<uint4*>(out + e0));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[stage]);
+        if (++stage == kRingStages) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[stage]);
-      if (++stage == kRingStages) {
-        stage = 0;
-        phase ^= 1u;
-      }
-    }
-    if (!kBwd) {
+      if (!reduce_pass) continue;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float m2 = __shfl_xor_sync(0xffffffffu, st.m, o);
@@ -505,7 +552,12 @@ __global__ void __launch_bounds__(kStreamThreads) ce_stream_kernel(const StreamA
         red_s[warp] = st.s;
       }
       named_barrier(1, kConsumers);
-      if (tid == 0) {
+      if (kBwd) {
+        // every consumer merges the warp states itself (same order, same lse)
+        Lse2 all;
+        for (int w = 0; w < kConsumerWarps; ++w) all.merge(red_m[w], red_s[w]);
+        lse2 = all.m + log2f(all.s);
+      } else if (tid == 0) {
         Lse2 all;
         for (int w = 0; w < kConsumerWarps; ++w) all.merge(red_m[w], red_s[w]);
         const T* prow = static_cast<const T*>(a.logits) + row * a.ld;
@@ -527,14 +579,14 @@ __global__ void __launch_bounds__(kStreamThreads) ce_stream_kernel(const StreamA
           if (a.label_logit != nullptr) a.label_logit[row] = zy;
         }
       }
-      named_barrier(1, kConsumers);
+      named_barrier(1, kConsumers);  // red_* is free for the next row
     }
   }
 }
 
-template <typename T, bool kBwd>
+template <typename T, bool kBwd, bool kTwoPass = false>
 static int launch_stream(const StreamArgs& a, cudaStream_t s) {
-  auto kern = ce_stream_kernel<T, kBwd>;
+  auto kern = ce_stream_kernel<T, kBwd, kTwoPass>;
   static std::atomic<uint64_t> done{0};  // devices whose smem limit is raised
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
@@ -551,6 +603,246 @@ static int launch_stream(const StreamArgs& a, cudaStream_t s) {
   const int grid = static_cast<int>(a.N < g ? a.N : g);
   kern<<<grid, kStreamThreads, kStreamSmem, s>>>(a);
   return launch_status(kBwd ? "ce_stream_kernel<bwd> launch" : "ce_stream_kernel<fwd> launch");
+}
+
+// ------------------------------ backward without a saved lse: resident rows
+//
+// The strict "keep only the logits and the labels" backward: the lse is not
+// saved, so it has to be formed again before the gradient.  Streaming each row
+// twice costs a second read of the logits; instead a row is split over a
+// cluster of P CTAs (P = 1, 2, 4 or 8, the fewest whose slices fit
+// kResSlice bytes of shared memory: a bf16 row of V = 128256 is 250.5 KiB,
+// four slices of 62.6 KiB).  Each CTA copies its slice into shared memory once
+// (cp.async.bulk, 8 KB per mbarrier so the reduction starts on the first
+// piece), reduces it to a base-2 (m, s) pair and publishes the pair in its
+// shared memory; after a cluster barrier every CTA reads the P pairs through
+// distributed shared memory and merges them in rank order (so all CTAs of the
+// cluster hold the same lse), then writes its slice of dZ from shared memory.
+// The logits are read from HBM once, as when the lse is saved.  Rows with a
+// zero gradient (ignored labels, or a zero coefficient) are written as zeros
+// without being read.
+#ifndef FLCE_CE_RES_SLICE
+#define FLCE_CE_RES_SLICE 65536
+#endif
+constexpr int kResThreads = 256;
+constexpr int kResWarps = kResThreads / 32;
+constexpr int kResSeg = 8192;
+constexpr int kResSegVec = kResSeg / 16;
+constexpr int kResSlice = FLCE_CE_RES_SLICE;
+constexpr int kResMaxSegs = (kResSlice + kResSeg - 1) / kResSeg;
+constexpr int kResMaxCluster = 8;
+static_assert(kResSlice % 16 == 0 && kResSegVec % kResThreads == 0, "whole vectors per thread");
+
+struct ResArgs {
+  const void* logits;
+  int64_t N, V, ld;
+  const int64_t* labels;
+  int64_t ignore_index;
+  int reduction;
+  int64_t num_label_tokens;
+  const int64_t* n_valid;
+  const float* grad_loss;
+  void* grad;
+  int64_t ldg;
+  int32_t* status;
+  int64_t slice_vec;  // 16-byte vectors per CTA slice (the last slice may be shorter)
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kResThreads) ce_bwd_resident_kernel(const ResArgs a) {
+  constexpr int EPV = Elem<T>::kPerVec;
+  extern __shared__ uint8_t res_raw[];
+  __shared__ uint64_t bar[kResMaxSegs];
+  __shared__ float part_m[2], part_s[2];  // this CTA's (m, s), by parity of the row count
+  __shared__ float red_m[kResWarps], red_s[kResWarps];
+  __shared__ float lse2_sh;
+  __shared__ int abort_sh;
+  uint4* buf = reinterpret_cast<uint4*>(
+      (reinterpret_cast<uintptr_t>(res_raw) + 127) & ~static_cast<uintptr_t>(127));
+  volatile int* abort_flag = &abort_sh;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t P = cluster_nctarank();
+  const int64_t nclusters = gridDim.x / P;
+  const int64_t nvec_row = a.V * static_cast<int64_t>(sizeof(T)) / 16;
+  const int64_t v_lo = min(nvec_row, static_cast<int64_t>(rank) * a.slice_vec);
+  const int nv = static_cast<int>(min(nvec_row, v_lo + a.slice_vec) - v_lo);
+  const int nseg = (nv + kResSegVec - 1) / kResSegVec;
+  if (tid == 0) {
+    for (int i = 0; i < kResMaxSegs; ++i) mbar_init(&bar[i], 1);
+    abort_sh = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const float coef = grad_coef(a.reduction, a.num_label_tokens, a.n_valid, a.grad_loss);
+  uint32_t phase = 0;       // parity of the segment barriers' current phase
+  uint32_t nb = 0;          // rows exchanged so far (selects part_*[nb & 1])
+  int issued_parity = -1;   // thread 0: parity of the last row it issued copies for
+
+  for (int64_t row = blockIdx.x / P; row < a.N; row += nclusters) {
+    const int64_t y = a.labels[row];
+    const bool valid = (y != a.ignore_index) && label_ok(y, a.V);
+    const float c = valid ? coef : 0.0f;
+    uint4* out = reinterpret_cast<uint4*>(static_cast<T*>(a.grad) + row * a.ldg) + v_lo;
+    if (c == 0.0f) {  // the same decision in every CTA of the cluster
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      for (int v = tid; v < nv; v += kResThreads) __stcs(out + v, z);
+      continue;
+    }
+    if (tid == 0 && !*abort_flag) {
+      const char* src = reinterpret_cast<const char*>(static_cast<const T*>(a.logits) +
+                                                      row * a.ld) +
+                        v_lo * 16;
+      for (int sg = 0; sg < nseg; ++sg) {
+        const uint32_t bytes = static_cast<uint32_t>(min(kResSegVec, nv - sg * kResSegVec)) * 16u;
+        mbar_arrive_expect_tx(&bar[sg], bytes);
+        bulk_load(buf + sg * kResSegVec, src + static_cast<int64_t>(sg) * kResSeg, bytes,
+                  &bar[sg]);
+      }
+      issued_parity = static_cast<int>(phase);
+    }
+    // reduction of the slice, piece by piece as the copies land
+    Lse2 st;
+    for (int sg = 0; sg < nseg; ++sg) {
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&bar[sg], phase, abort_flag) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0 && !*abort_flag) {
+          *abort_flag = 1;
+          set_status(a.status, FLCE_ETIMEOUT);
+        }
+        break;
+      }
+      lse_add_smem<T, kResSegVec / kResThreads, kResThreads>(
+          buf + sg * kResSegVec, tid, min(kResSegVec, nv - sg * kResSegVec), st);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, st.m, o);
+      const float s2 = __shfl_xor_sync(0xffffffffu, st.s, o);
+      st.merge(m2, s2);
+    }
+    if (lane == 0) {
+      red_m[warp] = st.m;
+      red_s[warp] = st.s;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      Lse2 all;
+      for (int w = 0; w < kResWarps; ++w) all.merge(red_m[w], red_s[w]);
+      part_m[nb & 1] = all.m;
+      part_s[nb & 1] = all.s;
+    }
+    // every CTA of the cluster runs this barrier once per row it reduces, also
+    // after a timeout, so no CTA is left waiting at it
+    cluster_sync();
+    if (warp == 0) {
+      float m = -INFINITY, sv = 0.0f;
+      if (lane < static_cast<int>(P)) {
+        m = ld_shared_cluster_f32(mapa_shared(smem_u32(&part_m[nb & 1]), lane));
+        sv = ld_shared_cluster_f32(mapa_shared(smem_u32(&part_s[nb & 1]), lane));
+      }
+      Lse2 all;
+      for (int q = 0; q < static_cast<int>(P); ++q)
+        all.merge(__shfl_sync(0xffffffffu, m, q), __shfl_sync(0xffffffffu, sv, q));
+      if (lane == 0) lse2_sh = all.m + log2f(all.s);
+    }
+    __syncthreads();
+    const float lse2 = lse2_sh;
+    ++nb;
+    phase ^= 1u;
+    if (!*abort_flag) {
+      const int64_t ylocal = y - v_lo * EPV;  // label element relative to the slice
+      for (int v0 = 0; v0 < nv; v0 += 4 * kResThreads)
+        dz_from_smem<T, 4, kResThreads>(buf, v0 + tid, nv, ylocal, lse2, c, out);
+    }
+    __syncthreads();  // the slice buffer and lse2_sh are free for the next row
+  }
+  // a peer may still read this CTA's last (m, s) pair
+  cluster_sync();
+  if (tid == 0 && *abort_flag && issued_parity >= 0) {
+    // let this CTA's copies in flight land before its shared memory is released
+    for (int sg = 0; sg < nseg; ++sg) {
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(smem_u32(&bar[sg]), static_cast<uint32_t>(issued_parity)) &&
+             global_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+  }
+}
+
+struct ResCacheEntry {
+  int dev, P, es;
+  size_t smem;
+  int clusters;
+};
+
+// Launches ce_bwd_resident_kernel.  Returns 1 (nothing launched) when a row
+// does not fit a cluster of kResMaxCluster slices or no cluster of that size
+// can be resident.
+template <typename T>
+static int launch_resident(ResArgs a, cudaStream_t s) {
+  const int64_t nvec_row = a.V * static_cast<int64_t>(sizeof(T)) / 16;
+  int P = 1;
+  while (P <= kResMaxCluster && (nvec_row + P - 1) / P * 16 > kResSlice) P *= 2;
+  if (P > kResMaxCluster) return 1;
+  a.slice_vec = (nvec_row + P - 1) / P;
+  const size_t smem = static_cast<size_t>(a.slice_vec) * 16 + 128;
+  auto kern = ce_bwd_resident_kernel<T>;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  static std::atomic<uint64_t> raised{0};
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(raised.load() & bit)) {
+    const int rc = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                    kResSlice + 128),
+                               "cudaFuncSetAttribute(ce_bwd_resident_kernel)");
+    if (rc != FLCE_OK) return rc;
+    raised.fetch_or(bit);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(P);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(P), 1, 1);
+  cfg.blockDim = dim3(kResThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = P > 1 ? 1 : 0;  // P == 1: a plain launch (each CTA is its own cluster)
+  // resident clusters for this (device, P, dtype, shared memory), cached
+  static std::mutex mu;
+  static std::vector<ResCacheEntry> cache;
+  int clusters = -1;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (const auto& e : cache)
+      if (e.dev == dev && e.P == P && e.es == static_cast<int>(sizeof(T)) && e.smem == smem)
+        clusters = e.clusters;
+  }
+  if (clusters < 0) {
+    int rc;
+    if (P > 1) {
+      rc = cuda_status(cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg),
+                       "cudaOccupancyMaxActiveClusters(ce_bwd_resident_kernel)");
+    } else {
+      int per_sm = 0;
+      rc = cuda_status(
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kResThreads, smem),
+          "cudaOccupancyMaxActiveBlocksPerMultiprocessor(ce_bwd_resident_kernel)");
+      clusters = per_sm * sm_count();
+    }
+    if (rc != FLCE_OK) return rc;
+    std::lock_guard<std::mutex> lock(mu);
+    cache.push_back({dev, P, static_cast<int>(sizeof(T)), smem, clusters});
+  }
+  if (clusters < 1) return 1;
+  const int64_t g = a.N < clusters ? a.N : clusters;
+  cfg.gridDim = dim3(static_cast<unsigned>(g * P), 1, 1);
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, a), "cudaLaunchKernelEx(ce_bwd_resident_kernel)");
 }
 
 // The bulk-copy path needs 16-byte aligned row starts and lengths.
@@ -707,6 +999,32 @@ extern "C" int ce_logits_fwd_shard(const void* logits_shard, int dt, int64_t N, 
                      nullptr, sh, status, reinterpret_cast<cudaStream_t>(stream));
 }
 
+// ------------------------------------------------- bounded-wait self-test
+
+// Waits, through the same bounded mbarrier wait every pipeline of this library
+// uses, on a barrier nothing will ever arrive on; after limit_ns the wait gives
+// up and FLCE_ETIMEOUT goes to the status word, as a failed pipeline would
+// report it.  The kernel always returns.
+__global__ void wait_selftest_kernel(int32_t* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_sh;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_sh = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0, &abort_sh, limit_ns))
+    set_status(status, FLCE_ETIMEOUT);
+}
+
+extern "C" int flce_wait_selftest(int32_t* status, uint64_t limit_ns, flce_stream_t stream) {
+  if (status == nullptr) return FLCE_EINVAL;
+  if (limit_ns > 2000000000ull) return FLCE_ESHAPE;
+  wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(status, limit_ns);
+  return launch_status("wait_selftest_kernel launch");
+}
+
 // ------------------------------------------------- packed-document labels
 
 // labels[b, t] = ignore_index where doc[b, t] == 0 (padding) or where the next
@@ -797,8 +1115,9 @@ static int ce_bwd_entry(const void* logits, int dt, int64_t N, int64_t V, int64_
   if (v0 < 0 || V_total < v0 + V || V_total >= (int64_t(1) << 31)) return FLCE_ESHAPE;
   if (status == nullptr) return FLCE_EINVAL;
   if (N == 0) return FLCE_OK;
-  if (lse == nullptr || n_valid == nullptr || grad_loss == nullptr || grad_logits == nullptr)
-    return FLCE_EINVAL;
+  if (n_valid == nullptr || grad_loss == nullptr || grad_logits == nullptr) return FLCE_EINVAL;
+  // no saved lse: only for a whole vocabulary (a shard needs the global lse)
+  if (lse == nullptr && (v0 != 0 || V_total != V)) return FLCE_EINVAL;
   if (inplace_grad != 0 && inplace_grad != 1) return FLCE_EINVAL;
   if (ld_grad < V) return FLCE_ESHAPE;
   if (!aligned(grad_logits, dtype_size(dt))) return FLCE_EALIGN;
@@ -813,7 +1132,27 @@ static int ce_bwd_entry(const void* logits, int dt, int64_t N, int64_t V, int64_
     return FLCE_EINVAL;  // out-of-place buffers must not overlap
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (streamable(logits, ld, V, es) && streamable(grad_logits, ld_grad, V, es)) {
+  const bool stream_ok = streamable(logits, ld, V, es) && streamable(grad_logits, ld_grad, V, es);
+  if (stream_ok && lse == nullptr) {
+    ResArgs r{};
+    r.logits = logits;
+    r.N = N;
+    r.V = V;
+    r.ld = ld;
+    r.labels = labels;
+    r.ignore_index = ignore_index;
+    r.reduction = reduction;
+    r.num_label_tokens = num_label_tokens;
+    r.n_valid = n_valid;
+    r.grad_loss = grad_loss;
+    r.grad = grad_logits;
+    r.ldg = ld_grad;
+    r.status = status;
+    rc = dt == FLCE_BF16 ? launch_resident<__nv_bfloat16>(r, s) : launch_resident<float>(r, s);
+    if (rc != 1) return rc;
+    // a row too long for one cluster: streamed twice below
+  }
+  if (stream_ok) {
     StreamArgs a{};
     a.logits = logits;
     a.N = N;
@@ -831,6 +1170,9 @@ static int ce_bwd_entry(const void* logits, int dt, int64_t N, int64_t V, int64_
     a.status = status;
     a.v0 = v0;
     a.V_total = V_total;
+    if (lse == nullptr)
+      return dt == FLCE_BF16 ? launch_stream<__nv_bfloat16, true, true>(a, s)
+                             : launch_stream<float, true, true>(a, s);
     return dt == FLCE_BF16 ? launch_stream<__nv_bfloat16, true>(a, s)
                            : launch_stream<float, true>(a, s);
   }

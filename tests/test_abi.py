@@ -107,8 +107,16 @@ def test_ce_bwd_rejects_bad_arguments(lib):
     assert call(12, 2) == -1            # inplace flag not 0/1
     assert call(13, FAKE + 4096) == -1  # in place but grad pointer differs
     assert call(14, 12) == -1           # in place but row strides differ
-    assert call(9, None) == -1          # lse missing
+    assert call(10, None) == -1         # n_valid missing
     assert call(1, 3) == -3
+    # lse may be NULL (formed again in the kernel), but not for a vocabulary
+    # shard, whose rows need the global lse
+    shard = [FAKE, 0, 4, 10, 10, 0, 20, FAKE, -100, 0, -1, None, FAKE, FAKE, 0, FAKE + 4096, 10,
+             FAKE, None]
+    assert _abi.ce_logits_bwd_shard(*shard) == -1
+    shard[11] = FAKE
+    shard[6] = 5  # V_total < vocab_offset + V_shard
+    assert _abi.ce_logits_bwd_shard(*shard) == -2
 
 
 @no_gpu
