@@ -447,34 +447,8 @@ def run_ours(args, rank, ws, local):
 
     # the backward alone, with the saved lse and without it (out of place)
     restore()
-    gbuf = torch.empty_like(logits)
-    n_valid_rows = int((labels != c.ignore_index).sum().item())
-
-    def bwd(lse):
-        return lambda: lh.ce_logits_bwd(logits, labels, lse, co.n_valid, one, c.ignore_index,
-                                        c.reduction, c.num_label_tokens, grad_logits=gbuf,
-                                        status=cst)
-    bwd_ms = {}
-    for name, fn in (("saved_lse", bwd(co.lse)), ("no_lse", bwd(None))):
-        for _ in range(max(3, args.warmup)):
-            fn()
-        t = _events_time(fn, args.steps, stream)
-        bwd_ms[name] = max_over_ranks(sum(t) / len(t), ws)
-    lh.check_status(cst, "ce_logits_bwd")
-    # the saved-lse kernel reads every row; the no-lse kernel skips ignored rows
-    row_b = c.V * 2
-    bwd_bytes = {"saved_lse": 2.0 * c.N * row_b,
-                 "no_lse": (n_valid_rows + c.N) * float(row_b)}
-    ce_bwd_line = {
-        name: {"ms": round(bwd_ms[name], 4),
-               "gb_s": round(bwd_bytes[name] / (bwd_ms[name] * 1e-3) / 1e9, 1),
-               "frac_of_hbm": round(bwd_bytes[name] / (bwd_ms[name] * 1e-3) / 1e9 /
-                                    peaks["hbm_gbs"], 4)}
-        for name in bwd_ms}
-    ce_bwd_line["bytes"] = ("saved_lse: read + write of every row; no_lse: read of the "
-                            f"{n_valid_rows} non-ignored rows + write of all {c.N} rows "
-                            "(a row cluster holds each row in shared memory: one read)")
-    del pristine, logits, c, cws, co, gbuf
+    ce_bwd_line = ce_bwd_compare(c, co, cst, one, stream, args, ws, peaks)
+    del pristine, logits, c, cws, co
     torch.cuda.empty_cache()
 
     # ------------------------------------------------- latency-bound workloads
@@ -589,6 +563,42 @@ def run_ours(args, rank, ws, local):
         print(json.dumps(line))
 
 
+def ce_bwd_compare(c, co, cst, one, stream, args, ws, peaks):
+    """Device time of the CE backward alone on the given-logits workload, with
+    the forward's lse and without it (the row-cluster kernel), out of place."""
+    import torch
+    import lm_head_linear_fwd_gb300 as lh
+    logits, labels = c.logits, c.labels
+    gbuf = torch.empty_like(logits)
+    n_valid_rows = int((labels != c.ignore_index).sum().item())
+
+    def bwd(lse):
+        return lambda: lh.ce_logits_bwd(logits, labels, lse, co.n_valid, one, c.ignore_index,
+                                        c.reduction, c.num_label_tokens, grad_logits=gbuf,
+                                        status=cst)
+    bwd_ms = {}
+    for name, fn in (("saved_lse", bwd(co.lse)), ("no_lse", bwd(None))):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        t = _events_time(fn, args.steps, stream)
+        bwd_ms[name] = max_over_ranks(sum(t) / len(t), ws)
+    lh.check_status(cst, "ce_logits_bwd")
+    # the saved-lse kernel reads every row; the no-lse kernel skips ignored rows
+    row_b = c.V * 2
+    bwd_bytes = {"saved_lse": 2.0 * c.N * row_b,
+                 "no_lse": (n_valid_rows + c.N) * float(row_b)}
+    line = {name: {"ms": round(bwd_ms[name], 4),
+                   "gb_s": round(bwd_bytes[name] / (bwd_ms[name] * 1e-3) / 1e9, 1),
+                   "frac_of_hbm": round(bwd_bytes[name] / (bwd_ms[name] * 1e-3) / 1e9 /
+                                        peaks["hbm_gbs"], 4)}
+            for name in bwd_ms}
+    line["bytes"] = ("saved_lse: read + write of every row; no_lse: read of the "
+                     f"{n_valid_rows} non-ignored rows + write of all {c.N} rows "
+                     "(a row cluster holds each row in shared memory: one read)")
+    del gbuf
+    return line
+
+
 def run_ce_only(args, rank, ws, local, dev, stream, peaks, peak_src):
     """Given-logits part alone (profiling runs)."""
     import torch
@@ -612,12 +622,14 @@ def run_ce_only(args, rank, ws, local, dev, stream, peaks, peak_src):
     t = _events_time(ce_step, args.steps, stream)
     ms = max_over_ranks(sum(t) / len(t), ws)
     gbs = 3.0 * c.N * c.V * 2 / (ms * 1e-3) / 1e9
+    bwd_line = ce_bwd_compare(c, co, cst, one, stream, args, ws, peaks)
     if rank == 0:
         print(json.dumps({"metric": METRIC, "value": round(gbs, 1), "unit": "GB/s",
                           "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
                           "ms_per_step": round(ms, 4),
                           "config": {"workload": f"CE on logits only [{c.N},{c.V}] bf16"},
                           "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                          "bwd_only": bwd_line,
                           "note": "profiling run: given-logits part only"}))
 
 

@@ -425,7 +425,6 @@ struct StreamArgs {
 template <typename T, bool kBwd, bool kTwoPass = false>
 __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm)
     ce_stream_kernel(const StreamArgs a) {
-  constexpr int EPV = Elem<T>::kPerVec;
   constexpr int kVecPerSeg = kSegBytes / 16;
   constexpr int kVecPerThread = kVecPerSeg / kConsumers;  // 8 (32 KB segments)
   extern __shared__ uint8_t ring_raw[];
@@ -610,28 +609,35 @@ static int launch_stream(const StreamArgs& a, cudaStream_t s) {
 // The strict "keep only the logits and the labels" backward: the lse is not
 // saved, so it has to be formed again before the gradient.  Streaming each row
 // twice costs a second read of the logits; instead a row is split over a
-// cluster of P CTAs (P = 1, 2, 4 or 8, the fewest whose slices fit
-// kResSlice bytes of shared memory: a bf16 row of V = 128256 is 250.5 KiB,
-// four slices of 62.6 KiB).  Each CTA copies its slice into shared memory once
-// (cp.async.bulk, 8 KB per mbarrier so the reduction starts on the first
-// piece), reduces it to a base-2 (m, s) pair and publishes the pair in its
-// shared memory; after a cluster barrier every CTA reads the P pairs through
-// distributed shared memory and merges them in rank order (so all CTAs of the
-// cluster hold the same lse), then writes its slice of dZ from shared memory.
+// cluster of P CTAs (P = 1, 2, 4 or 8, the fewest whose slices fit kResBuf
+// bytes: a bf16 row of V = 128256, 250.5 KiB, in four slices of 62.6 KiB) that
+// hold it in shared memory.  Each CTA copies its slice in once (cp.async.bulk,
+// 8 KB per mbarrier so the reduction starts on the first piece), reduces it to
+// a base-2 (m, s) pair and sends the pair to the other CTAs with st.async
+// (8 bytes that complete on the receiver's mbarrier: no cluster-wide barrier
+// per row); every CTA merges the P pairs in rank order (so all CTAs of the
+// cluster hold the same lse) and writes its slice of dZ from shared memory.
 // The logits are read from HBM once, as when the lse is saved.  Rows with a
 // zero gradient (ignored labels, or a zero coefficient) are written as zeros
 // without being read.
-#ifndef FLCE_CE_RES_SLICE
-#define FLCE_CE_RES_SLICE 65536
+//
+// Measured alternatives on GB300 ([16384, 128256] bf16): two slice buffers
+// per CTA (the next row copied in, or a row pipeline that lets the CTAs of a
+// cluster drift apart by a row) need twice the CTAs per row and were 15-30%
+// slower; one barrier.cluster per row instead of st.async 5% slower; streaming
+// each row twice through the ring 25% slower (about even with L2 evict_last /
+// evict_first hints at 2 CTAs per SM).
+#ifndef FLCE_CE_RES_BUF
+#define FLCE_CE_RES_BUF 65536
 #endif
 constexpr int kResThreads = 256;
 constexpr int kResWarps = kResThreads / 32;
 constexpr int kResSeg = 8192;
 constexpr int kResSegVec = kResSeg / 16;
-constexpr int kResSlice = FLCE_CE_RES_SLICE;
-constexpr int kResMaxSegs = (kResSlice + kResSeg - 1) / kResSeg;
+constexpr int kResBuf = FLCE_CE_RES_BUF;  // shared-memory bytes for a slice
+constexpr int kResMaxSegs = (kResBuf + kResSeg - 1) / kResSeg;
 constexpr int kResMaxCluster = 8;
-static_assert(kResSlice % 16 == 0 && kResSegVec % kResThreads == 0, "whole vectors per thread");
+static_assert(kResBuf % 256 == 0 && kResSegVec % kResThreads == 0, "whole vectors per thread");
 
 struct ResArgs {
   const void* logits;
@@ -653,10 +659,16 @@ __global__ void __launch_bounds__(kResThreads) ce_bwd_resident_kernel(const ResA
   constexpr int EPV = Elem<T>::kPerVec;
   extern __shared__ uint8_t res_raw[];
   __shared__ uint64_t bar[kResMaxSegs];
-  __shared__ float part_m[2], part_s[2];  // this CTA's (m, s), by parity of the row count
+  // the cluster's (m, s) pairs of a copied row, by rank; copied row k uses slot
+  // k % 2, whose barrier completes when the other P - 1 pairs have landed.  Two
+  // slots suffice: a CTA sends row k's pair only after it has all pairs of row
+  // k - 1, and every CTA reads a row's pairs before it sends the next pair.
+  __shared__ __align__(8) float2 pairs[2][kResMaxCluster];
+  __shared__ uint64_t xbar[2];
   __shared__ float red_m[kResWarps], red_s[kResWarps];
   __shared__ float lse2_sh;
   __shared__ int abort_sh;
+  __shared__ int xbroken_sh;  // set (by thread 0) when an exchange wait timed out
   uint4* buf = reinterpret_cast<uint4*>(
       (reinterpret_cast<uintptr_t>(res_raw) + 127) & ~static_cast<uintptr_t>(127));
   volatile int* abort_flag = &abort_sh;
@@ -670,25 +682,54 @@ __global__ void __launch_bounds__(kResThreads) ce_bwd_resident_kernel(const ResA
   const int nseg = (nv + kResSegVec - 1) / kResSegVec;
   if (tid == 0) {
     for (int i = 0; i < kResMaxSegs; ++i) mbar_init(&bar[i], 1);
+    mbar_init(&xbar[0], 1);
+    mbar_init(&xbar[1], 1);
     abort_sh = 0;
+    xbroken_sh = 0;
     fence_barrier_init();
   }
-  __syncthreads();
+  // the exchange barriers must be initialised in every CTA before any pair is sent
+  cluster_sync();
   const float coef = grad_coef(a.reduction, a.num_label_tokens, a.n_valid, a.grad_loss);
-  uint32_t phase = 0;       // parity of the segment barriers' current phase
-  uint32_t nb = 0;          // rows exchanged so far (selects part_*[nb & 1])
-  int issued_parity = -1;   // thread 0: parity of the last row it issued copies for
+  const int64_t first = blockIdx.x / P;
 
-  for (int64_t row = blockIdx.x / P; row < a.N; row += nclusters) {
-    const int64_t y = a.labels[row];
-    const bool valid = (y != a.ignore_index) && label_ok(y, a.V);
-    const float c = valid ? coef : 0.0f;
-    uint4* out = reinterpret_cast<uint4*>(static_cast<T*>(a.grad) + row * a.ldg) + v_lo;
-    if (c == 0.0f) {  // the same decision in every CTA of the cluster
+  // Rows of this cluster: first + i * nclusters.  Each warp reads the labels
+  // of 32 rows at a time (one per lane) and keeps a bit mask of those that need
+  // a copy (a nonzero gradient: the same answer in every thread and every CTA
+  // of the cluster); rows with a zero gradient are written as zeros when
+  // passed, without being read.
+  int64_t win = -32;   // index i of the window's first row
+  uint32_t todo = 0u;  // bit t: row win + t exists and is not handed out yet
+  uint32_t need = 0u;  // bit t: row win + t needs a copy
+  auto next_row = [&]() -> int64_t {
+    while (true) {
+      if (todo == 0u) {
+        win += 32;
+        if (first + win * nclusters >= a.N) return a.N;
+        const int64_t r = first + (win + lane) * nclusters;
+        bool nd = false;
+        if (r < a.N) {
+          const int64_t yr = __ldg(a.labels + r);
+          nd = coef != 0.0f && yr != a.ignore_index && label_ok(yr, a.V);
+        }
+        todo = __ballot_sync(0xffffffffu, r < a.N);
+        need = __ballot_sync(0xffffffffu, nd);
+      }
+      const int t = __ffs(todo) - 1;
+      todo &= todo - 1u;
+      const int64_t r = first + (win + t) * nclusters;
+      if ((need >> t) & 1u) return r;
+      uint4* out = reinterpret_cast<uint4*>(static_cast<T*>(a.grad) + r * a.ldg) + v_lo;
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
       for (int v = tid; v < nv; v += kResThreads) __stcs(out + v, z);
-      continue;
     }
+  };
+
+  uint32_t phase = 0u;  // parity of the slice barriers' current phase
+  int issued_par = -1;  // thread 0: parity of the last copies issued (drain on abort)
+  uint32_t k = 0;       // copied rows so far
+  for (int64_t row = next_row(); row < a.N; row = next_row(), ++k) {
+    const int64_t y = __ldg(a.labels + row);
     if (tid == 0 && !*abort_flag) {
       const char* src = reinterpret_cast<const char*>(static_cast<const T*>(a.logits) +
                                                       row * a.ld) +
@@ -699,7 +740,7 @@ __global__ void __launch_bounds__(kResThreads) ce_bwd_resident_kernel(const ResA
         bulk_load(buf + sg * kResSegVec, src + static_cast<int64_t>(sg) * kResSeg, bytes,
                   &bar[sg]);
       }
-      issued_parity = static_cast<int>(phase);
+      issued_par = static_cast<int>(phase);
     }
     // reduction of the slice, piece by piece as the copies land
     Lse2 st;
@@ -717,6 +758,7 @@ __global__ void __launch_bounds__(kResThreads) ce_bwd_resident_kernel(const ResA
       lse_add_smem<T, kResSegVec / kResThreads, kResThreads>(
           buf + sg * kResSegVec, tid, min(kResSegVec, nv - sg * kResSegVec), st);
     }
+    phase ^= 1u;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float m2 = __shfl_xor_sync(0xffffffffu, st.m, o);
@@ -728,44 +770,61 @@ __global__ void __launch_bounds__(kResThreads) ce_bwd_resident_kernel(const ResA
       red_s[warp] = st.s;
     }
     __syncthreads();
-    if (tid == 0) {
-      Lse2 all;
-      for (int w = 0; w < kResWarps; ++w) all.merge(red_m[w], red_s[w]);
-      part_m[nb & 1] = all.m;
-      part_s[nb & 1] = all.s;
-    }
-    // every CTA of the cluster runs this barrier once per row it reduces, also
-    // after a timeout, so no CTA is left waiting at it
-    cluster_sync();
+    // Exchange of the slices' (m, s) pairs.  After a copy timed out it goes on
+    // (with meaningless values) so that no CTA waits for a pair in vain; only
+    // an exchange that itself timed out ends the exchanges.
+    const int j = static_cast<int>(k & 1u);
     if (warp == 0) {
-      float m = -INFINITY, sv = 0.0f;
+      if (lane == 0) {
+        Lse2 all;
+        for (int w = 0; w < kResWarps; ++w) all.merge(red_m[w], red_s[w]);
+        pairs[j][rank] = make_float2(all.m, all.s);
+        if (P > 1 && !xbroken_sh) {
+          mbar_arrive_expect_tx(&xbar[j], (P - 1) * 8u);
+          const uint32_t src = smem_u32(&pairs[j][rank]);
+          const uint32_t xb = smem_u32(&xbar[j]);
+          for (uint32_t q = 0; q < P; ++q)
+            if (q != rank) st_async_f32x2(mapa_shared(src, q), all.m, all.s, mapa_shared(xb, q));
+        }
+      }
+      __syncwarp();
+      if (P > 1 && !xbroken_sh) {
+        // every lane of the warp waits (acquire) before it reads the pairs
+        const bool got = mbar_wait(&xbar[j], (k >> 1) & 1u, nullptr, kWaitLimitNs);
+        if (!__all_sync(0xffffffffu, got) && lane == 0) {
+          xbroken_sh = 1;
+          *abort_flag = 1;
+          set_status(a.status, FLCE_ETIMEOUT);
+        }
+      }
+      float m = -INFINITY, sp = 0.0f;
       if (lane < static_cast<int>(P)) {
-        m = ld_shared_cluster_f32(mapa_shared(smem_u32(&part_m[nb & 1]), lane));
-        sv = ld_shared_cluster_f32(mapa_shared(smem_u32(&part_s[nb & 1]), lane));
+        const float2 pr = pairs[j][lane];
+        m = pr.x;
+        sp = pr.y;
       }
       Lse2 all;
       for (int q = 0; q < static_cast<int>(P); ++q)
-        all.merge(__shfl_sync(0xffffffffu, m, q), __shfl_sync(0xffffffffu, sv, q));
+        all.merge(__shfl_sync(0xffffffffu, m, q), __shfl_sync(0xffffffffu, sp, q));
       if (lane == 0) lse2_sh = all.m + log2f(all.s);
     }
     __syncthreads();
     const float lse2 = lse2_sh;
-    ++nb;
-    phase ^= 1u;
     if (!*abort_flag) {
+      uint4* out = reinterpret_cast<uint4*>(static_cast<T*>(a.grad) + row * a.ldg) + v_lo;
       const int64_t ylocal = y - v_lo * EPV;  // label element relative to the slice
       for (int v0 = 0; v0 < nv; v0 += 4 * kResThreads)
-        dz_from_smem<T, 4, kResThreads>(buf, v0 + tid, nv, ylocal, lse2, c, out);
+        dz_from_smem<T, 4, kResThreads>(buf, v0 + tid, nv, ylocal, lse2, coef, out);
     }
-    __syncthreads();  // the slice buffer and lse2_sh are free for the next row
+    __syncthreads();  // the slice buffer and lse2_sh are free again
   }
-  // a peer may still read this CTA's last (m, s) pair
+  // no CTA leaves while a peer may still be running
   cluster_sync();
-  if (tid == 0 && *abort_flag && issued_parity >= 0) {
+  if (tid == 0 && *abort_flag && issued_par >= 0) {
     // let this CTA's copies in flight land before its shared memory is released
     for (int sg = 0; sg < nseg; ++sg) {
       const uint64_t t0 = global_ns();
-      while (!mbar_try_wait(smem_u32(&bar[sg]), static_cast<uint32_t>(issued_parity)) &&
+      while (!mbar_try_wait(smem_u32(&bar[sg]), static_cast<uint32_t>(issued_par)) &&
              global_ns() - t0 < kWaitLimitNs) {
       }
     }
@@ -784,11 +843,11 @@ struct ResCacheEntry {
 template <typename T>
 static int launch_resident(ResArgs a, cudaStream_t s) {
   const int64_t nvec_row = a.V * static_cast<int64_t>(sizeof(T)) / 16;
-  int P = 1;
-  while (P <= kResMaxCluster && (nvec_row + P - 1) / P * 16 > kResSlice) P *= 2;
+  int P = 1;  // the fewest CTAs whose slices fit kResBuf bytes (128-byte aligned)
+  while (P <= kResMaxCluster && ((nvec_row + P - 1) / P + 7) / 8 * 8 * 16 > kResBuf) P *= 2;
   if (P > kResMaxCluster) return 1;
   a.slice_vec = (nvec_row + P - 1) / P;
-  const size_t smem = static_cast<size_t>(a.slice_vec) * 16 + 128;
+  const size_t smem = static_cast<size_t>((a.slice_vec + 7) / 8 * 8) * 16 + 128;
   auto kern = ce_bwd_resident_kernel<T>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
@@ -796,7 +855,7 @@ static int launch_resident(ResArgs a, cudaStream_t s) {
   const uint64_t bit = 1ull << (dev & 63);
   if (!(raised.load() & bit)) {
     const int rc = cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                    kResSlice + 128),
+                                                    kResBuf + 128),
                                "cudaFuncSetAttribute(ce_bwd_resident_kernel)");
     if (rc != FLCE_OK) return rc;
     raised.fetch_or(bit);

@@ -175,7 +175,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Gives up (returns
-// false) when *abort becomes nonzero or after limit_ns.
+// false) when *abort becomes nonzero (abort may be null) or after limit_ns.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
@@ -183,7 +183,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   const uint64_t t0 = global_ns();
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
-    if (*abort) return false;
+    if (abort != nullptr && *abort) return false;
     if (global_ns() - t0 > limit_ns) return false;
   }
 }
@@ -253,6 +253,14 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
           "r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Asks for `bytes` (multiple of 16) at a 16-byte aligned global address to be
+// brought into L2 ahead of a later copy; no completion to wait for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
 }
 
 // Barrier over the first `threads` threads of the block, on hardware barrier `id`.
@@ -334,6 +342,19 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t a, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
   return r;
+}
+
+// Asynchronous store of (x, y) (8 bytes, 8-byte aligned) to a shared::cluster
+// address in another CTA of the cluster; it completes 8 transaction bytes on
+// the mbarrier at `bar_cluster` in that same CTA, so the receiver learns of the
+// data by waiting on its own barrier and no cluster-wide fence is needed.
+__device__ __forceinline__ void st_async_f32x2(uint32_t addr_cluster, float x, float y,
+                                               uint32_t bar_cluster) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+          addr_cluster),
+      "f"(x), "f"(y), "r"(bar_cluster)
+      : "memory");
 }
 
 // Arrive on an mbarrier given by a shared::cluster address (possibly in the peer CTA).

@@ -45,14 +45,14 @@ def _close_to_saved(a, b, dtype):
 
 
 CASES = [
-    # dtype, N, V, ld                          path
+    # dtype, N, V, ld                          path (CTAs per row)
     (torch.bfloat16, 300, 1000, 1000),       # cluster of 1
-    (torch.bfloat16, 200, 32768, 32768),     # cluster of 1, a 64 KiB slice
     (torch.float32, 130, 4100, 4104),        # cluster of 1, padded row stride
+    (torch.bfloat16, 200, 32768, 32768),     # cluster of 1, a slice of exactly 64 KiB
     (torch.bfloat16, 700, 50264, 50264),     # cluster of 2, slices 3142 / 3141 vectors
     (torch.bfloat16, 300, 120008, 120008),   # cluster of 4, last slice shorter
     (torch.bfloat16, 40, 128256, 128256),    # cluster of 4, the Llama-3 vocabulary
-    (torch.float32, 24, 128256, 128256),     # cluster of 8
+    (torch.float32, 100, 128256, 128256),    # cluster of 8
     (torch.bfloat16, 6, 300000, 300000),     # too long for a cluster: streamed twice
     (torch.bfloat16, 77, 1003, 1011),        # not 16-byte aligned: row kernel
     (torch.float32, 5, 32777, 32777),        # not 16-byte aligned: row kernel
