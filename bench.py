@@ -296,7 +296,7 @@ def run_ours(args, rank, ws, local):
     Wh = W.cpu().pin_memory()
     yh = y.cpu().pin_memory()
     bh = b.cpu().pin_memory() if b is not None else None
-    n_e2e = max(2, min(args.steps, 10))
+    n_e2e = max(2, args.steps)
     loss_h = torch.empty(n_e2e, dtype=torch.float32).pin_memory()
     sets = [(torch.empty_like(H), torch.empty_like(W), torch.empty_like(y),
              torch.empty_like(b) if b is not None else None) for _ in range(2)]

@@ -313,13 +313,14 @@ static_assert(kSegBytes % (16 * kConsumers) == 0, "whole 16-byte vectors per con
 template <typename T, int K, int STRIDE>
 __device__ __forceinline__ void lse_add_smem(const uint4* sv, int first, int nvec, Lse2& st) {
   constexpr int EPV = Elem<T>::kPerVec;
+  const bool full = first + (K - 1) * STRIDE < nvec;  // no vector of this thread is missing
   if (sizeof(T) == 2) {
     uint4 u[K];
     __nv_bfloat162 mx = __float2bfloat162_rn(-INFINITY);
 #pragma unroll
     for (int k = 0; k < K; ++k) {
       const int v = first + k * STRIDE;
-      if (v < nvec) {
+      if (full || v < nvec) {
         u[k] = sv[v];
         mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&u[k].x));
         mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&u[k].y));
@@ -337,7 +338,7 @@ __device__ __forceinline__ void lse_add_smem(const uint4* sv, int first, int nve
 #pragma unroll
       for (int k = 0; k < K; ++k) {
         const int v = first + k * STRIDE;
-        if (v < nvec) {
+        if (full || v < nvec) {
           float x[EPV];
           Elem<T>::unpack(u[k], x);
 #pragma unroll
@@ -351,7 +352,7 @@ __device__ __forceinline__ void lse_add_smem(const uint4* sv, int first, int nve
 #pragma unroll
     for (int k = 0; k < K; ++k) {
       const int v = first + k * STRIDE;
-      if (v < nvec) {
+      if (full || v < nvec) {
         float x[EPV];
         Elem<T>::unpack(sv[v], x);
 #pragma unroll
@@ -365,34 +366,67 @@ __device__ __forceinline__ void lse_add_smem(const uint4* sv, int first, int nve
   }
 }
 
-// Writes dZ = c * (2^(x*log2e - lse2) - onehot) for K vectors sv[first +
-// k*STRIDE] (those below nvec) to out[v]; ylocal is the label's element index
-// relative to sv[0] (out of range when the label lies elsewhere).  c == 0
-// writes zeros.
+// Per-row constants of dZ = c * (softmax - onehot).  The scale is folded into
+// the exponent: c * 2^(t - lse2) = sign(c) * 2^(t - (lse2 - log2|c|)), so each
+// element costs one FFMA and one ex2; a negative c flips the sign bits of the
+// packed result.
+template <typename T>
+struct DzRow {
+  float c;       // the scale; 0: the row's gradient is zero
+  float l2c;     // lse2 - log2|c|
+  uint32_t neg;  // sign mask XORed into each packed 32-bit word when c < 0
+  __device__ DzRow(float lse2, float c_) : c(c_) {
+    l2c = c_ != 0.0f ? lse2 - log2f(fabsf(c_)) : 0.0f;
+    neg = c_ < 0.0f ? (sizeof(T) == 2 ? 0x80008000u : 0x80000000u) : 0u;
+  }
+};
+
+// Writes dZ for K vectors sv[first + k*STRIDE] (those below nvec) to out[v];
+// ylocal is the label's element index relative to sv[0] (out of range when the
+// label lies elsewhere).  c == 0 writes zeros.
 template <typename T, int K, int STRIDE>
 __device__ __forceinline__ void dz_from_smem(const uint4* sv, int first, int nvec, int64_t ylocal,
-                                             float lse2, float c, uint4* out) {
+                                             const DzRow<T>& r, uint4* out) {
   constexpr int EPV = Elem<T>::kPerVec;
+  const bool full = first + (K - 1) * STRIDE < nvec;
+  if (r.c == 0.0f) {
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int v = first + k * STRIDE;
+      if (full || v < nvec) __stcs(out + v, z);
+    }
+    return;
+  }
+  // the vector holding the label, if it is one of this call's
+  const int lab_v = (ylocal >= 0 && ylocal < static_cast<int64_t>(nvec) * EPV)
+                        ? static_cast<int>(ylocal / EPV)
+                        : -1;
 #pragma unroll
   for (int k = 0; k < K; ++k) {
     const int v = first + k * STRIDE;
-    if (v < nvec) {
+    if (full || v < nvec) {
       float x[EPV];
       Elem<T>::unpack(sv[v], x);
-      const int64_t j0 = static_cast<int64_t>(v) * EPV;
-      if (c == 0.0f) {
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) x[e] = 0.0f;
-      } else {
+      for (int e = 0; e < EPV; ++e) x[e] = ex2(fmaf(x[e], kLog2e, -r.l2c));
+      uint4 o;
+      if (v != lab_v) {
+        o = Elem<T>::pack(x);
+        o.x ^= r.neg;
+        o.y ^= r.neg;
+        o.z ^= r.neg;
+        o.w ^= r.neg;
+      } else {  // the one-hot label term
+        const int e_y = static_cast<int>(ylocal - static_cast<int64_t>(v) * EPV);
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) x[e] = ex2(fmaf(x[e], kLog2e, -lse2)) * c;
-        if (static_cast<uint64_t>(ylocal - j0) < static_cast<uint64_t>(EPV)) {
-#pragma unroll
-          for (int e = 0; e < EPV; ++e)
-            if (j0 + e == ylocal) x[e] -= c;  // the one-hot label term
+        for (int e = 0; e < EPV; ++e) {
+          x[e] = r.neg ? -x[e] : x[e];
+          if (e == e_y) x[e] -= r.c;
         }
+        o = Elem<T>::pack(x);
       }
-      __stcs(out + v, Elem<T>::pack(x));
+      __stcs(out + v, o);
     }
   }
 }
@@ -529,7 +563,7 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm)
           if (reduce_pass)
             lse_add_smem<T, kVecPerThread, kConsumers>(sv, tid, nvec, st);
           else
-            dz_from_smem<T, kVecPerThread, kConsumers>(sv, tid, nvec, y - e0, lse2, c,
+            dz_from_smem<T, kVecPerThread, kConsumers>(sv, tid, nvec, y - e0, DzRow<T>(lse2, c),
                                                        reinterpret_cast<uint4*>(out + e0));
         }
         __syncwarp();
@@ -813,8 +847,9 @@ __global__ void __launch_bounds__(kResThreads) ce_bwd_resident_kernel(const ResA
     if (!*abort_flag) {
       uint4* out = reinterpret_cast<uint4*>(static_cast<T*>(a.grad) + row * a.ldg) + v_lo;
       const int64_t ylocal = y - v_lo * EPV;  // label element relative to the slice
+      const DzRow<T> dr(lse2, coef);
       for (int v0 = 0; v0 < nv; v0 += 4 * kResThreads)
-        dz_from_smem<T, 4, kResThreads>(buf, v0 + tid, nv, ylocal, lse2, coef, out);
+        dz_from_smem<T, 4, kResThreads>(buf, v0 + tid, nv, ylocal, dr, out);
     }
     __syncthreads();  // the slice buffer and lse2_sh are free again
   }

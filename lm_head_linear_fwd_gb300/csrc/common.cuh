@@ -255,14 +255,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
-// Asks for `bytes` (multiple of 16) at a 16-byte aligned global address to be
-// brought into L2 ahead of a later copy; no completion to wait for.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
-               "r"(bytes)
-               : "memory");
-}
-
 // Barrier over the first `threads` threads of the block, on hardware barrier `id`.
 __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -328,13 +320,6 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
   return r;
-}
-
-// 32-bit load from a shared::cluster address (this CTA's or a peer's shared memory).
-__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
-  return v;
 }
 
 // shared::cluster address of the variable at shared::cta address `a` in CTA `rank`.
