@@ -334,18 +334,24 @@ __device__ __forceinline__ void lse_add_smem(const uint4* sv, int first, int nve
       st.m = bm;
     }
     if (st.m != -INFINITY) {
-      float acc = 0.0f;
+      // packed fp32 pairs (FFMA2, FADD2) and two accumulators, so the sum is
+      // not one long chain of dependent adds
+      const float2 lg = make_float2(kLog2e, kLog2e), nm = make_float2(-st.m, -st.m);
+      float2 acc[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
       for (int k = 0; k < K; ++k) {
         const int v = first + k * STRIDE;
         if (full || v < nvec) {
-          float x[EPV];
-          Elem<T>::unpack(u[k], x);
+          const uint32_t w[4] = {u[k].x, u[k].y, u[k].z, u[k].w};
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) acc += ex2(fmaf(x[e], kLog2e, -st.m));
+          for (int i = 0; i < 4; ++i) {
+            const float2 t = __ffma2_rn(make_float2(bf16_lo(w[i]), bf16_hi(w[i])), lg, nm);
+            acc[i & 1] = __fadd2_rn(acc[i & 1], make_float2(ex2(t.x), ex2(t.y)));
+          }
         }
       }
-      st.s += acc;
+      const float2 a2 = __fadd2_rn(acc[0], acc[1]);
+      st.s += a2.x + a2.y;
     }
   } else {
     float t[K * EPV];
@@ -402,6 +408,7 @@ __device__ __forceinline__ void dz_from_smem(const uint4* sv, int first, int nve
   const int lab_v = (ylocal >= 0 && ylocal < static_cast<int64_t>(nvec) * EPV)
                         ? static_cast<int>(ylocal / EPV)
                         : -1;
+  const float2 lg = make_float2(kLog2e, kLog2e), nl = make_float2(-r.l2c, -r.l2c);
 #pragma unroll
   for (int k = 0; k < K; ++k) {
     const int v = first + k * STRIDE;
@@ -409,7 +416,11 @@ __device__ __forceinline__ void dz_from_smem(const uint4* sv, int first, int nve
       float x[EPV];
       Elem<T>::unpack(sv[v], x);
 #pragma unroll
-      for (int e = 0; e < EPV; ++e) x[e] = ex2(fmaf(x[e], kLog2e, -r.l2c));
+      for (int e = 0; e < EPV; e += 2) {  // packed fp32 pairs (FFMA2)
+        const float2 t = __ffma2_rn(make_float2(x[e], x[e + 1]), lg, nl);
+        x[e] = ex2(t.x);
+        x[e + 1] = ex2(t.y);
+      }
       uint4 o;
       if (v != lab_v) {
         o = Elem<T>::pack(x);
