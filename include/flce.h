@@ -124,7 +124,8 @@ FLCE_API int ce_logits_fwd(const void* logits, int dt, int64_t N, int64_t V, int
 /* Self-test of the failure path: launches one warp that waits, with the same
  * bounded mbarrier wait every kernel of this library uses, on a barrier that
  * nothing arrives on.  After limit_ns (at most 2 s) the wait gives up and
- * FLCE_ETIMEOUT is written to *status; the kernel returns normally and the
+ * FLCE_ETIMEOUT is written to *status (a larger limit returns FLCE_ESHAPE
+ * and launches nothing); the kernel returns normally and the
  * context stays usable.  The source pages have no counterpart. */
 FLCE_API int flce_wait_selftest(int32_t* status, uint64_t limit_ns, flce_stream_t stream);
 

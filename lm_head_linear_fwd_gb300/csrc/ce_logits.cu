@@ -2,19 +2,28 @@
 //
 // Forward (Automodel PR #2996 "feat(loss): chunked masked CE, ...", first commit
 // message): per row an fp32 log-sum-exp and the gathered label logit; the
-// per-row losses are reduced to a scalar by a fixed-order fp64 sum.  Only the
-// per-row lse (4 bytes per row) is kept for the backward, so the backward is
-// one read -> write pass over the logits.
+// per-row losses are reduced to a scalar by a fixed-order fp64 sum.  The
+// per-row lse (4 bytes per row) is all the backward needs besides the logits
+// and labels, so the backward is one read -> write pass over the logits.
 //
 // Backward (same page, backward bullet and the inplace_grad commit): the
 // softmax is recomputed from the logits and the saved lse, the one-hot label is
 // subtracted, the result is scaled and written either into the logits storage
-// (in place) or into a separate buffer.
+// (in place) or into a separate buffer.  Without a saved lse (the page's
+// memory bullet: nothing but the inputs is kept) the lse is formed again in
+// the backward, still with one read of the logits where the row fits a
+// thread-block cluster's shared memory.
 //
-// Both kernels stream each row with 16-byte vector loads (a scalar head and
-// tail handle rows whose start is not 16-byte aligned), keep the online
-// maximum and sum in the base-2 domain (one MUFU ex2 per element plus one
-// rescale per 32 elements), and merge per-thread states with warp shuffles.
+// Three kernel families, chosen per call:
+// * ce_stream_kernel: rows whose start and length are 16-byte multiples
+//   stream through a cp.async.bulk shared-memory ring (forward; backward with
+//   a saved lse; backward without one for rows over 512 KiB, read twice);
+// * ce_bwd_resident_kernel: backward without a saved lse, a row held by a
+//   cluster of 1-8 CTAs;
+// * ce_fwd_rows_kernel / ce_bwd_rows_kernel: any other rows, 16-byte register
+//   loads with a scalar head and tail.
+// All keep the online maximum and sum in the base-2 domain (one MUFU ex2 per
+// element) and merge per-thread states with warp shuffles in a fixed order.
 #include <math.h>
 #include <stdio.h>
 
