@@ -717,7 +717,6 @@ def run_reference(args, rank, ws):
     p = wl.WORKLOADS[args.workload](device="cpu")
     rng = np.random.default_rng(0)
     rows = args.cpu_rows
-    W64 = None
     times = []
     for i in range(args.warmup + args.steps):
         sel = np.sort(rng.choice(p.N, rows, replace=False))
@@ -728,7 +727,6 @@ def run_reference(args, rank, ws):
                              p.num_label_tokens, rows=sel)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
-    del W64
     per = sum(times) / len(times)
     v = rows / per
     line = {

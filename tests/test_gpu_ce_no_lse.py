@@ -149,3 +149,25 @@ def test_no_lse_rejected_for_a_shard(lh):
                                   nv.data_ptr(), g.data_ptr(), 0, out.data_ptr(), 64,
                                   st.data_ptr(), torch.cuda.current_stream().cuda_stream)
     assert rc == -1  # FLCE_EINVAL: a shard needs the global lse
+
+
+@pytest.mark.parametrize("dtype,N,V", [
+    (torch.bfloat16, 1, 128256),   # one row, cluster of 4
+    (torch.bfloat16, 1, 8),        # one 16-byte vector
+    (torch.bfloat16, 3, 16),
+    (torch.bfloat16, 2, 262144),   # the longest row a cluster of 8 holds (8 x 64 KiB)
+    (torch.bfloat16, 2, 262152),   # one vector longer: streamed twice
+    (torch.float32, 2, 131072),    # the longest fp32 row a cluster holds
+])
+def test_no_lse_edge_shapes(lh, dtype, N, V):
+    p = wl.random_ce(N, V, dtype, seed=N * 7 + V, ignore_frac=0.0)
+    logits, labels = p.logits.cuda(), p.labels.cuda()
+    out = lh.ce_logits_fwd(logits, labels, -100, "sum")
+    g = torch.tensor([0.5], device="cuda")
+    grad = lh.ce_logits_bwd(logits, labels, None, out.n_valid, g, -100, "sum",
+                            status=out.status)
+    saved = lh.ce_logits_bwd(logits, labels, out.lse, out.n_valid, g, -100, "sum")
+    torch.cuda.synchronize()
+    lh.check_status(out.status)
+    _check_grad(grad, oracle.ce_backward(p.logits, p.labels, -100, "sum", grad_loss=0.5))
+    _close_to_saved(grad, saved, dtype)

@@ -53,3 +53,41 @@ def test_flce_and_ce_in_a_cuda_graph():
         lh.check_status(st)
         for a, e in zip((fo.loss, fo.lse, gH, gW, gb, co.loss, logits), eager):
             assert torch.equal(a, e)
+
+
+def test_ce_without_saved_lse_in_a_cuda_graph():
+    # the row-cluster backward (a cluster launch) and the unaligned-row
+    # fallback, each captured after one eager run
+    import lm_head_linear_fwd_gb300 as lh
+    cases = [wl.random_ce(96, 128256, torch.bfloat16, seed=41),
+             wl.random_ce(64, 1003, torch.bfloat16, seed=42)]
+    dev = [(c.logits.cuda().contiguous(), c.labels.cuda()) for c in cases]
+    st = lh.new_status("cuda")
+    one = torch.ones(1, device="cuda")
+    outs = [lh.ce_logits_fwd(x, y, reduction="mean", status=st) for x, y in dev]
+    grads = [torch.empty_like(x) for x, _ in dev]
+
+    def step():
+        for (x, y), o, g in zip(dev, outs, grads):
+            lh.ce_logits_fwd(x, y, reduction="mean", status=st, out=o)
+            lh.ce_logits_bwd(x, y, None, o.n_valid, one, reduction="mean", grad_logits=g,
+                             status=st)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    eager = [g.clone() for g in grads]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(2):
+        for g in grads:
+            g.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        lh.check_status(st)
+        for g, e in zip(grads, eager):
+            assert torch.equal(g, e)
