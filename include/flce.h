@@ -82,7 +82,8 @@ typedef enum {
   FLCE_EWORKSPACE = -6,  /* workspace pointer null or too small              */
   FLCE_ECUDA = -7,       /* a CUDA runtime/driver call failed                */
   FLCE_ENOSUP = -8,      /* valid request this build does not support        */
-  FLCE_ETIMEOUT = -9     /* (device) a bounded wait inside a kernel gave up  */
+  FLCE_ETIMEOUT = -9,    /* (device) a bounded wait inside a kernel gave up  */
+  FLCE_EBOUNDS = -10     /* (device, checked builds) an index left its range  */
 } flce_status_t;
 
 typedef enum { FLCE_BF16 = 0, FLCE_F32 = 1 } flce_dtype_t;
@@ -120,6 +121,19 @@ FLCE_API int ce_logits_fwd(const void* logits, int dt, int64_t N, int64_t V, int
                   int64_t num_label_tokens, float* loss, int64_t* n_valid, float* lse,
                   float* loss_rows, float* label_logit, void* ws, size_t ws_bytes,
                   int32_t* status, flce_stream_t stream);
+
+/* 1 when this library was built with device-side index checks
+ * (FLCE_DEVICE_CHECKS=1: the debug build that stands in for a memory checker;
+ * an index outside its tensor or buffer records FLCE_EBOUNDS in the status
+ * word and the access is skipped, never a trap), 0 for the ordinary build.
+ * The source pages have no counterpart. */
+FLCE_API int flce_device_checks(void);
+
+/* Self-test of the device-side index check: one thread checks an index equal
+ * to the length of a range (one past its end) and performs no access either
+ * way.  In a checked build *status becomes FLCE_EBOUNDS; in the ordinary
+ * build the check is compiled out and *status is left unchanged. */
+FLCE_API int flce_bounds_selftest(int32_t* status, flce_stream_t stream);
 
 /* Self-test of the failure path: launches one warp that waits, with the same
  * bounded mbarrier wait every kernel of this library uses, on a barrier that

@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", platform.machine(), "libflce.so")
 FLCE_OK = 0
 FLCE_ELABEL = -5
 FLCE_ETIMEOUT = -9
+FLCE_EBOUNDS = -10
 FLCE_BF16 = 0
 FLCE_F32 = 1
 FLCE_SUM = 0
@@ -60,6 +61,8 @@ _SIGNATURES = {
     "flce_grad_scale": (_i, [_p, _i, _i64, _p, _p]),
     "flce_count_valid": (_i, [_p, _i64, _i64, _i64, _p, _p]),
     "flce_wait_selftest": (_i, [_p, ctypes.c_uint64, _p]),
+    "flce_device_checks": (_i, []),
+    "flce_bounds_selftest": (_i, [_p, _p]),
     "flce_mask_packed_labels": (_i, [_p, _p, _i64, _i64, _i64, _p]),
     "flce_gemm_set_pair": (_i, [_i]),
     "flce_gemm_pair_slots": (_i, []),
@@ -71,11 +74,9 @@ EXPORTED = tuple(_SIGNATURES)
 _lib = None
 
 
-def load(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Loads libflce.so once; raises if it has not been built."""
-    global _lib
-    if _lib is not None:
-        return _lib
+def open_library(path: str) -> ctypes.CDLL:
+    """Opens a build of the library at `path` with every signature set (the
+    package itself always uses libflce.so through load())."""
     if not os.path.exists(path):
         raise ImportError(
             f"libflce.so not found at {path}: build it with "
@@ -85,8 +86,15 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    _lib = lib
     return lib
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libflce.so once; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        _lib = open_library(path)
+    return _lib
 
 
 def status_string(code: int) -> str:
@@ -136,6 +144,8 @@ flce_fwd_bwd = _call("flce_fwd_bwd")
 flce_grad_scale = _call("flce_grad_scale")
 flce_count_valid = _call("flce_count_valid")
 flce_wait_selftest = _call("flce_wait_selftest")
+flce_device_checks = _call("flce_device_checks")
+flce_bounds_selftest = _call("flce_bounds_selftest")
 flce_mask_packed_labels = _call("flce_mask_packed_labels")
 flce_gemm_set_pair = _call("flce_gemm_set_pair")
 flce_gemm_pair_slots = _call("flce_gemm_pair_slots")

@@ -2,7 +2,7 @@
 
 Each translation unit is compiled in parallel, then linked into
 ``lm_head_linear_fwd_gb300/_lib/<machine>/libflce.so`` (static CUDA runtime, no torch
-dependency).  ``python lm_head_linear_fwd_gb300/build.py`` runs it.
+dependency).  ``python lm_head_linear_fwd_gb300/build.py [--checked]`` runs it.
 """
 from __future__ import annotations
 
@@ -46,28 +46,36 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compiles (if needed) and returns the path of libflce.so."""
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    """Compiles (if needed) and returns the path of libflce.so.
+
+    ``checked=True`` builds the debug variant ``libflce_checked.so`` instead,
+    with device-side index checks (``FLCE_DEVICE_CHECKS=1``): an index that
+    leaves its range records FLCE_EBOUNDS in the status word and the access is
+    skipped.  It is a separate file; the package always loads libflce.so."""
     nvcc = _nvcc()
     os.makedirs(LIBDIR, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     headers += [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))]
+    suffix = "_checked" if checked else ""
+    defs = ["-DFLCE_DEVICE_CHECKS=1"] if checked else []
+    lib = os.path.join(LIBDIR, f"libflce{suffix}.so")
     objs, jobs = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(LIBDIR, src.replace(".cu", ".o"))
+        o = os.path.join(LIBDIR, src.replace(".cu", f"{suffix}.o"))
         objs.append(o)
         if force or _stale(o, [s] + headers):
-            jobs.append([nvcc, *ARCH, *FLAGS, "-c", s, "-o", o])
+            jobs.append([nvcc, *ARCH, *FLAGS, *defs, "-c", s, "-o", o])
     if jobs:
         with concurrent.futures.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
             for out in ex.map(_run, jobs):
                 if verbose and out.strip():
                     print(out)
-    if force or jobs or _stale(LIB, objs):
-        _run([nvcc, *ARCH, "-shared", "-o", LIB, *objs, "-ldl"])
-    return LIB
+    if force or jobs or _stale(lib, objs):
+        _run([nvcc, *ARCH, "-shared", "-o", lib, *objs, "-ldl"])
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, checked="--checked" in sys.argv))

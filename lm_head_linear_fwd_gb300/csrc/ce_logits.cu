@@ -521,9 +521,16 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm)
           }
           const uint32_t bytes = static_cast<uint32_t>(
               min(static_cast<int64_t>(kSegBytes), row_bytes - static_cast<int64_t>(sg) * kSegBytes));
-          mbar_arrive_expect_tx(&full_bar[stage], bytes);
-          bulk_load(ring + stage * kSegBytes, src + static_cast<int64_t>(sg) * kSegBytes, bytes,
-                    &full_bar[stage]);
+          // checked builds: the segment lies inside its row and its stage; a
+          // failed check completes the stage without a copy
+          if (span_in_range(static_cast<int64_t>(sg) * kSegBytes, bytes, row_bytes, a.status) &&
+              smem_in_range(stage * kSegBytes + 128, kSegBytes, a.status)) {
+            mbar_arrive_expect_tx(&full_bar[stage], bytes);
+            bulk_load(ring + stage * kSegBytes, src + static_cast<int64_t>(sg) * kSegBytes, bytes,
+                      &full_bar[stage]);
+          } else {
+            mbar_arrive(&full_bar[stage]);
+          }
           ++issued;
           if (++stage == kRingStages) {
             stage = 0;
@@ -580,7 +587,9 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm)
               min(static_cast<int64_t>(kSegBytes), row_bytes - static_cast<int64_t>(sg) * kSegBytes) /
               16);
           const uint4* sv = reinterpret_cast<const uint4*>(ring + stage * kSegBytes);
-          if (reduce_pass)
+          // checked builds: the segment's vectors lie inside the row
+          if (!span_in_range(e0, static_cast<int64_t>(nvec) * (16 / sizeof(T)), a.V, a.status)) {
+          } else if (reduce_pass)
             lse_add_smem<T, kVecPerThread, kConsumers>(sv, tid, nvec, st);
           else
             dz_from_smem<T, kVecPerThread, kConsumers>(sv, tid, nvec, y - e0, DzRow<T>(lse2, c),
@@ -738,7 +747,13 @@ __global__ void __launch_bounds__(kResThreads) ce_bwd_resident_kernel(const ResA
     for (int i = 0; i < kResMaxSegs; ++i) mbar_init(&bar[i], 1);
     mbar_init(&xbar[0], 1);
     mbar_init(&xbar[1], 1);
-    abort_sh = 0;
+    // checked builds: the slice lies inside the row and fits the shared memory
+    // and the barriers of this launch; a failed check skips every copy
+    const bool fits =
+        span_in_range(v_lo, nv, nvec_row, a.status) && in_range(rank, kResMaxCluster, a.status) &&
+        span_in_range(0, nseg, kResMaxSegs + 1, a.status) &&
+        smem_in_range(128, (a.slice_vec + 7) / 8 * 8 * 16, a.status);
+    abort_sh = fits ? 0 : 1;
     xbroken_sh = 0;
     fence_barrier_init();
   }
@@ -1006,6 +1021,7 @@ extern "C" const char* flce_status_string(int status) {
     case FLCE_ECUDA: return "FLCE_ECUDA: CUDA call failed";
     case FLCE_ENOSUP: return "FLCE_ENOSUP: not supported by this build";
     case FLCE_ETIMEOUT: return "FLCE_ETIMEOUT: a bounded wait inside a kernel gave up";
+    case FLCE_EBOUNDS: return "FLCE_EBOUNDS: a device-side index check failed (checked build)";
     default: return "FLCE: unknown status";
   }
 }
@@ -1137,6 +1153,23 @@ extern "C" int flce_wait_selftest(int32_t* status, uint64_t limit_ns, flce_strea
   if (limit_ns > 2000000000ull) return FLCE_ESHAPE;
   wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(status, limit_ns);
   return launch_status("wait_selftest_kernel launch");
+}
+
+// ------------------------------------------------- device-side index checks
+
+__global__ void bounds_selftest_kernel(int32_t* status) {
+  const int64_t n = 16;
+  // one past the end: the check fails in a checked build; nothing is accessed
+  if (in_range(n, n, status)) {
+  }
+}
+
+extern "C" int flce_device_checks(void) { return kDeviceChecks ? 1 : 0; }
+
+extern "C" int flce_bounds_selftest(int32_t* status, flce_stream_t stream) {
+  if (status == nullptr) return FLCE_EINVAL;
+  bounds_selftest_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(status);
+  return launch_status("bounds_selftest_kernel launch");
 }
 
 // ------------------------------------------------- packed-document labels

@@ -32,6 +32,43 @@ __device__ __forceinline__ uint64_t global_ns() {
 // A wait that has not completed after this long is treated as a failure.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
 
+// Device-side index checks of the debug build (FLCE_DEVICE_CHECKS=1), which
+// stands in for a memory checker: in_range(i, n) is true for 0 <= i < n; a
+// check that fails records FLCE_EBOUNDS and the caller skips the access.  In
+// the ordinary build every check is true and compiles away.
+#ifndef FLCE_DEVICE_CHECKS
+#define FLCE_DEVICE_CHECKS 0
+#endif
+constexpr bool kDeviceChecks = FLCE_DEVICE_CHECKS != 0;
+
+__device__ __forceinline__ bool in_range(int64_t i, int64_t n, int32_t* status) {
+  if (!kDeviceChecks || (i >= 0 && i < n)) return true;
+  set_status(status, FLCE_EBOUNDS);
+  return false;
+}
+
+// Bytes of dynamic shared memory this launch was given.
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
+  return r;
+}
+
+// [i0, i0 + len) lies within [0, n).
+__device__ __forceinline__ bool span_in_range(int64_t i0, int64_t len, int64_t n,
+                                              int32_t* status) {
+  if (!kDeviceChecks || (i0 >= 0 && len >= 0 && i0 + len <= n)) return true;
+  set_status(status, FLCE_EBOUNDS);
+  return false;
+}
+
+// Bytes [off, off + len) of dynamic shared memory lie within what this launch
+// was given (read from the special register only in checked builds).
+__device__ __forceinline__ bool smem_in_range(int64_t off, int64_t len, int32_t* status) {
+  if (!kDeviceChecks) return true;
+  return span_in_range(off, len, dynamic_smem_bytes(), status);
+}
+
 // --------------------------------------------------------------------- numerics
 
 // 2^x with the MUFU instruction (flushes denormal results to 0).

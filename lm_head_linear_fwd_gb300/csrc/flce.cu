@@ -83,6 +83,7 @@ struct EpiLse {
     float* part_s;     // [nNt, part_ld], sum of 2^(t - max)
     float* zlab;       // [M] label logit (written by the tile holding the label)
     int64_t v0;        // vocabulary id of this shard's column 0 (0 unsharded)
+    int32_t* status = nullptr;  // device status word (index checks of checked builds)
   };
   template <int BN>
   __device__ static void tile(const Params& p, int mt, int nt, int row_in_tile, uint32_t taddr,
@@ -110,7 +111,7 @@ struct EpiLse {
       }
       st.addk(t);
     }
-    if (row_ok) {
+    if (row_ok && in_range(row, p.part_ld, p.status)) {
       p.part_m[nt * p.part_ld + row] = st.m;
       p.part_s[nt * p.part_ld + row] = st.s;
       if (ylocal >= 0 && ylocal < BN) p.zlab[row] = zy;
@@ -183,7 +184,7 @@ struct EpiLseStore {
       }
       ctx.store_slab(packed, col0, r0, false);
     }
-    if (row_ok) {
+    if (row_ok && in_range(row, p.part_ld, p.status)) {
       p.part_m[nt * p.part_ld + row] = m;
       p.part_s[nt * p.part_ld + row] = s;
       if (ylocal >= 0 && ylocal < BN) p.zlab[row] = zy;
@@ -932,6 +933,7 @@ static int fwd_gemm(const void* H, const void* W, const void* bias, int dt, int6
     using E = EpiLse<__nv_bfloat16>;
     E::Params ep{bias, labels, ignore_index, static_cast<int>(N), static_cast<int>(V),
                  p.part_ld, part_m, part_s, zlab, v0};
+    ep.status = status;
     return launch_gemm<__nv_bfloat16, kBNFwd, false, false, E>(kRoleFwd, a, b, nullptr, (int)N,
                                                                (int)V, (int)D, group, ep, status,
                                                                s);
@@ -939,6 +941,7 @@ static int fwd_gemm(const void* H, const void* W, const void* bias, int dt, int6
   using E = EpiLse<float>;
   E::Params ep{bias, labels, ignore_index, static_cast<int>(N), static_cast<int>(V), p.part_ld,
                part_m, part_s, zlab, v0};
+  ep.status = status;
   return launch_gemm<float, kBNFwd, false, false, E>(kRoleFwd, a, b, nullptr, (int)N, (int)V,
                                                      (int)D, group, ep, status, s);
 }
@@ -1206,6 +1209,7 @@ static int flce_fused_impl(const void* H, const void* W, const void* bias, int64
       using E = EpiLseStore<T>;
       typename E::Params ep{bias, labels + r0, ignore_index, C, static_cast<int>(V),
                             p.fpart_ld, part_m, part_s, zlab + r0};
+      ep.status = status;
       const Operand a{Ht + r0 * D, C, D, D, false};
       const Operand b{W, V, D, D, false};
       const OutDesc o{dz, dt, C, V, p.ldV};

@@ -179,7 +179,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&acce_bar[i], 4);
     }
     mbar_init(&drain_bar, 1);
-    abort_sh = 0;
+    // checked builds: the stages and staging buffers fit the launch's shared memory
+    abort_sh = smem_in_range(0, G::kSmemBytes, ga.status) ? 0 : 1;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -215,6 +216,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int mt = mte - split * ga.nMt;
         const int kb0 = split * ga.kb_per_split;
         const int kb1 = min(ga.nK, kb0 + ga.kb_per_split);
+        // checked builds: the tile and its K range lie inside the problem
+        if (!in_range(mt, ga.nMt, ga.status) || !in_range(nt, ga.nNt, ga.status) ||
+            !span_in_range(kb0, kb1 - kb0, ga.nK, ga.status)) {
+          ok = false;
+          break;
+        }
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
             ok = false;
@@ -417,7 +424,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&acce_bar[i], 8);
     }
     mbar_init(&drain_bar, 1);
-    abort_sh = 0;
+    // checked builds: the stages and staging buffers fit the launch's shared memory
+    abort_sh = smem_in_range(0, G::kSmemBytes, ga.status) ? 0 : 1;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -453,6 +461,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tile_coords(t, ga.nMt, ga.nNt, ga.group_m, mt, nt);
         const int arow = mt * 2 * kBM + static_cast<int>(rank) * kBM;
         const int brow = nt * BN + static_cast<int>(rank) * G::kHalfN;
+        // checked builds: the tile lies inside the problem (the same test in both CTAs)
+        if (!in_range(mt, ga.nMt, ga.status) || !in_range(nt, ga.nNt, ga.status)) {
+          ok = false;
+          break;
+        }
         for (int kb = 0; kb < ga.nK; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
             ok = false;

@@ -50,7 +50,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_status_strings(lib):
     from lm_head_linear_fwd_gb300 import _abi
-    for code in range(0, -10, -1):
+    for code in range(0, -11, -1):
         assert _abi.status_string(code).startswith("FLCE")
 
 
