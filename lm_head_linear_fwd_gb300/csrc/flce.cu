@@ -70,6 +70,52 @@ __device__ __forceinline__ void add_bias32(const void* bias, int col0, int V, fl
   }
 }
 
+// Adds the first n (<= 32) of 32 logits v to a base-2 online log-sum-exp: the
+// chunk maximum (the order of v equals the order of v*log2e), one rescale,
+// then 2^(v*log2e - m) by packed pairs (FFMA2) summed into four independent
+// packed accumulators, so the sum is not one long chain of dependent adds.
+__device__ __forceinline__ void lse_add32(const float (&v)[32], int n, Lse2& st) {
+  float mx = -INFINITY;
+  if (n >= 32) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) mx = fmaxf(mx, v[j]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < n) mx = fmaxf(mx, v[j]);
+  }
+  const float bm = mx * kLog2e;
+  if (bm > st.m) {
+    st.s *= ex2(st.m - bm);
+    st.m = bm;
+  }
+  if (st.m == -INFINITY) return;
+  const float2 lg = make_float2(kLog2e, kLog2e), nm = make_float2(-st.m, -st.m);
+  float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                   make_float2(0.0f, 0.0f)};
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    const float2 t = __ffma2_rn(make_float2(v[j], v[j + 1]), lg, nm);
+    float2 e = make_float2(ex2(t.x), ex2(t.y));
+    if (n < 32) {
+      e.x = j < n ? e.x : 0.0f;
+      e.y = j + 1 < n ? e.y : 0.0f;
+    }
+    acc[(j >> 1) & 3] = __fadd2_rn(acc[(j >> 1) & 3], e);
+  }
+  const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+  st.s += a.x + a.y;
+}
+
+// v[j] for the one j with base + j == idx (idx in [base, base + 32)).
+__device__ __forceinline__ float pick32(const float (&v)[32], int64_t idx, int base) {
+  float r = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    if (base + j == idx) r = v[j];
+  return r;
+}
+
 // Forward: per-row partial log-sum-exp of one logits tile + label gather.
 template <typename T>
 struct EpiLse {
@@ -102,14 +148,9 @@ struct EpiLse {
       float v[32];
       tmem_ld32(taddr + c * 32, v);
       if (p.bias != nullptr) add_bias32<T>(p.bias, col0, p.V, v);
-      float t[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float x = v[j];
-        if (c * 32 + j == ylocal) zy = x;
-        t[j] = (col0 + j < p.V) ? x * kLog2e : -INFINITY;
-      }
-      st.addk(t);
+      // the label's logit, in the one chunk that holds it (rarely any lane of a warp)
+      if (static_cast<uint64_t>(ylocal - c * 32) < 32u) zy = pick32(v, ylocal, c * 32);
+      lse_add32(v, p.V - col0, st);
     }
     if (row_ok && in_range(row, p.part_ld, p.status)) {
       p.part_m[nt * p.part_ld + row] = st.m;
@@ -221,6 +262,11 @@ struct EpiDlogits {
     const float c = valid ? grad_coef(p.reduction, p.num_label_tokens, p.n_valid, p.grad_loss)
                           : 0.0f;
     const float lse2 = row_ok ? p.lse[row] * kLog2e : 0.0f;
+    // c * 2^(t - lse2) = sign(c) * 2^(t - (lse2 - log2|c|)): one FFMA and one
+    // ex2 per element; a negative c flips the sign bits of the packed words
+    const float l2c = c != 0.0f ? lse2 - log2f(fabsf(c)) : 0.0f;
+    const uint32_t neg = c < 0.0f ? (sizeof(T) == 2 ? 0x80008000u : 0x80000000u) : 0u;
+    const float2 lg = make_float2(kLog2e, kLog2e), nl = make_float2(-l2c, -l2c);
     const int col_base = nt * BN;
     const int64_t ylocal = valid ? (y - p.v0) - col_base : -1;
     const int r0 = mt * kBM + (row_in_tile & ~31);
@@ -235,15 +281,38 @@ struct EpiDlogits {
         tmem_ld32(taddr + g * CPS + h * 32, v);
         const int cl = g * CPS + h * 32;  // column within the tile
         if (p.bias != nullptr) add_bias32<T>(p.bias, col_base + cl, p.V, v);
+        if (c == 0.0f) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          v[j] = (ex2(fmaf(v[j], kLog2e, -lse2)) - (cl + j == ylocal ? 1.0f : 0.0f)) * c;
+          for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float2 t = __ffma2_rn(make_float2(v[j], v[j + 1]), lg, nl);
+            v[j] = ex2(t.x);
+            v[j + 1] = ex2(t.y);
+          }
+        }
+        const bool has_label = static_cast<uint64_t>(ylocal - cl) < 32u;
+        if (has_label) {  // the one-hot term, in the chunk holding the label
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            v[j] = neg ? -v[j] : v[j];
+            if (cl + j == ylocal) v[j] -= c;
+          }
+        }
 #pragma unroll
         for (int k = 0; k < 32 / EPV; ++k) {
           float x[EPV];
 #pragma unroll
           for (int e = 0; e < EPV; ++e) x[e] = v[k * EPV + e];
-          packed[h * (32 / EPV) + k] = Elem<T>::pack(x);
+          uint4 w = Elem<T>::pack(x);
+          if (!has_label) {
+            w.x ^= neg;
+            w.y ^= neg;
+            w.z ^= neg;
+            w.w ^= neg;
+          }
+          packed[h * (32 / EPV) + k] = w;
         }
       }
       ctx.store_slab(packed, col0, r0, false);
