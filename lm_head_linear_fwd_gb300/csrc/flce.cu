@@ -360,16 +360,50 @@ struct EpiStore {
 
 // ------------------------------------------------------------ small kernels
 
-// Merges the per-tile partials of each row in a fixed order.
-__global__ void __launch_bounds__(256) lse_combine_kernel(
+// Merge of the per-(row, vocab tile) partials of 32 rows per block of nw
+// warps (nw = min(16, tiles)): warp w merges the tiles p = w, w + nw, ... of
+// its lane's row (lane = row, so each load of a warp reads 32 consecutive rows
+// of one tile: 128 bytes), then warp 0 merges the nw warp states of each row in
+// warp order.  Fixed order, so the result is the same on every run.
+constexpr int kCombineRows = 32;
+constexpr int kCombineWarps = 16;
+
+static unsigned combine_threads(int nparts) {
+  return static_cast<unsigned>(32 * std::max(1, std::min(kCombineWarps, nparts)));
+}
+
+__device__ __forceinline__ bool combine_rows(const float* __restrict__ part_m,
+                                             const float* __restrict__ part_s, int nparts,
+                                             int64_t part_ld, int64_t N, int64_t& row,
+                                             Lse2& all) {
+  __shared__ float sm[kCombineWarps][kCombineRows], ss[kCombineWarps][kCombineRows];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = static_cast<int>(blockDim.x >> 5);
+  row = static_cast<int64_t>(blockIdx.x) * kCombineRows + lane;
+  Lse2 st;
+  if (row < N) {
+#pragma unroll 4
+    for (int p = warp; p < nparts; p += nw)
+      st.merge(part_m[p * part_ld + row], part_s[p * part_ld + row]);
+  }
+  sm[warp][lane] = st.m;
+  ss[warp][lane] = st.s;
+  __syncthreads();
+  if (warp != 0 || row >= N) return false;
+  for (int w = 0; w < nw; ++w) all.merge(sm[w][lane], ss[w][lane]);
+  return true;
+}
+
+// Forward: per row, the tile partials merged into the lse, and the row loss
+// from the label logit (the tile holding the label wrote it).
+__global__ void __launch_bounds__(kCombineRows * kCombineWarps) lse_combine_kernel(
     const float* __restrict__ part_m, const float* __restrict__ part_s, int nparts,
     int64_t part_ld, const float* __restrict__ zlab, const int64_t* __restrict__ labels,
     int64_t N, int64_t V, int64_t ignore_index, float* __restrict__ lse_out,
     float* __restrict__ loss_rows, float* __restrict__ label_logit, int32_t* status) {
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (row >= N) return;
+  int64_t row;
   Lse2 st;
-  for (int p = 0; p < nparts; ++p) st.merge(part_m[p * part_ld + row], part_s[p * part_ld + row]);
+  if (!combine_rows(part_m, part_s, nparts, part_ld, N, row, st)) return;
   const float lse = st.m * kLn2 + logf(st.s);
   lse_out[row] = lse;
   const int64_t y = labels[row];
@@ -389,15 +423,14 @@ __global__ void __launch_bounds__(256) lse_combine_kernel(
 // Vocabulary-parallel forward: merges this shard's tile partials of each row
 // into (m, s) (base-2 max and sum over the shard's columns) and the label logit
 // when the label lies in the shard (0 otherwise).
-__global__ void __launch_bounds__(256) shard_combine_kernel(
+__global__ void __launch_bounds__(kCombineRows * kCombineWarps) shard_combine_kernel(
     const float* __restrict__ part_m, const float* __restrict__ part_s, int nparts,
     int64_t part_ld, const float* __restrict__ zlab, const int64_t* __restrict__ labels,
     int64_t N, int64_t V_shard, int64_t v0, int64_t ignore_index, float* __restrict__ m_out,
     float* __restrict__ s_out, float* __restrict__ zy_out) {
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (row >= N) return;
+  int64_t row;
   Lse2 st;
-  for (int p = 0; p < nparts; ++p) st.merge(part_m[p * part_ld + row], part_s[p * part_ld + row]);
+  if (!combine_rows(part_m, part_s, nparts, part_ld, N, row, st)) return;
   m_out[row] = st.m;
   s_out[row] = st.s;
   const int64_t y = labels[row];
@@ -437,21 +470,37 @@ __global__ void __launch_bounds__(256) shard_finish_kernel(
   loss_rows[i] = li;
 }
 
-constexpr int kColSplits = 16;
+constexpr int kColSplits = 32;
 
-// Column sums of dZ [M, ldd] over row slices: part[s, v] = sum of rows in slice s.
+// Column sums of dZ [M, ldd] over row slices: part[s, v] = sum of rows in slice
+// s.  Each thread sums one 16-byte vector of columns (the chunk buffer's row
+// stride is a multiple of 64 elements and its start 256-byte aligned, so every
+// vector lies inside the allocation; columns at or past V are not written).
 template <typename T>
 __global__ void __launch_bounds__(256) colsum_partial_kernel(const T* __restrict__ dz, int M,
                                                              int64_t ldd, int V,
                                                              float* __restrict__ part) {
-  const int v = blockIdx.x * blockDim.x + threadIdx.x;
-  if (v >= V) return;
+  constexpr int EPV = Elem<T>::kPerVec;
+  const int v0 = (blockIdx.x * blockDim.x + threadIdx.x) * EPV;
+  if (v0 >= V) return;
   const int s = blockIdx.y;
   const int per = (M + kColSplits - 1) / kColSplits;
   const int r0 = s * per, r1 = min(M, r0 + per);
-  float acc = 0.0f;
-  for (int r = r0; r < r1; ++r) acc += Elem<T>::load(dz + static_cast<int64_t>(r) * ldd + v);
-  part[static_cast<int64_t>(s) * V + v] = acc;
+  float acc[EPV];
+#pragma unroll
+  for (int e = 0; e < EPV; ++e) acc[e] = 0.0f;
+  const uint4* q = reinterpret_cast<const uint4*>(dz + static_cast<int64_t>(r0) * ldd + v0);
+  const int64_t step = ldd / EPV;
+#pragma unroll 8
+  for (int r = r0; r < r1; ++r, q += step) {
+    float x[EPV];
+    Elem<T>::unpack(__ldcs(q), x);
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) acc[e] += x[e];
+  }
+#pragma unroll
+  for (int e = 0; e < EPV; ++e)
+    if (v0 + e < V) part[static_cast<int64_t>(s) * V + v0 + e] = acc[e];
 }
 
 __global__ void __launch_bounds__(256) colsum_final_kernel(const float* __restrict__ part, int V,
@@ -1035,7 +1084,8 @@ extern "C" int flce_fwd(const void* H, const void* W, const void* bias, int dt, 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   rc = fwd_gemm(H, W, bias, dt, N, D, V, 0, labels, ignore_index, p, w, status, s);
   if (rc != FLCE_OK) return rc;
-  lse_combine_kernel<<<static_cast<unsigned>((N + 255) / 256), 256, 0, s>>>(
+  lse_combine_kernel<<<static_cast<unsigned>((N + kCombineRows - 1) / kCombineRows),
+                       combine_threads(p.nparts), 0, s>>>(
       reinterpret_cast<float*>(w + p.off_part_m), reinterpret_cast<float*>(w + p.off_part_s),
       p.nparts, p.part_ld, reinterpret_cast<float*>(w + p.off_zlab), labels, N, V, ignore_index,
       lse, rows, label_logit, status);
@@ -1067,7 +1117,8 @@ extern "C" int flce_fwd_shard(const void* H, const void* W_shard, const void* bi
   rc = fwd_gemm(H, W_shard, bias_shard, dt, N, D, V_shard, vocab_offset, labels, ignore_index, p,
                 w, status, s);
   if (rc != FLCE_OK) return rc;
-  shard_combine_kernel<<<static_cast<unsigned>((N + 255) / 256), 256, 0, s>>>(
+  shard_combine_kernel<<<static_cast<unsigned>((N + kCombineRows - 1) / kCombineRows),
+                         combine_threads(p.nparts), 0, s>>>(
       reinterpret_cast<float*>(w + p.off_part_m), reinterpret_cast<float*>(w + p.off_part_s),
       p.nparts, p.part_ld, reinterpret_cast<float*>(w + p.off_zlab), labels, N, V_shard,
       vocab_offset, ignore_index, m_local, s_local, zy_local);
@@ -1129,7 +1180,8 @@ static int bwd_tail(const void* W, const T* Hc, int64_t D, int64_t V, int C, boo
   int rc = FLCE_OK;
   // 2. bias gradient
   if (grad_bias != nullptr) {
-    dim3 g1(static_cast<unsigned>((V + 255) / 256), kColSplits);
+    constexpr int kEpv = Elem<T>::kPerVec;
+    dim3 g1(static_cast<unsigned>(((V + kEpv - 1) / kEpv + 255) / 256), kColSplits);
     colsum_partial_kernel<T><<<g1, 256, 0, s>>>(dz, C, p.ldV, (int)V, colsum);
     colsum_final_kernel<<<static_cast<unsigned>((V + 255) / 256), 256, 0, s>>>(
         colsum, (int)V, grad_bias, first_chunk ? 0 : 1);
@@ -1287,7 +1339,8 @@ static int flce_fused_impl(const void* H, const void* W, const void* bias, int64
       if (rc != FLCE_OK) return rc;
     }
     // 2. lse and per-row loss of the chunk
-    lse_combine_kernel<<<static_cast<unsigned>((C + 255) / 256), 256, 0, s>>>(
+    lse_combine_kernel<<<static_cast<unsigned>((C + kCombineRows - 1) / kCombineRows),
+                         combine_threads(p.nparts), 0, s>>>(
         part_m, part_s, p.nparts, p.fpart_ld, zlab + r0, labels + r0, C, V, ignore_index,
         lse + r0, rows + r0, nullptr, status);
     // 3. dZ in place
