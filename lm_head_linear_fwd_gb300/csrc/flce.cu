@@ -181,7 +181,9 @@ struct EpiLseStore {
     const int col_base = nt * BN;
     const int64_t ylocal = (y < 0) ? -1 : (y - p.v0) - col_base;
     const int r0 = mt * kBM + (row_in_tile & ~31);
-    float m = -INFINITY, zy = 0.0f;
+    // pass 1: the tile maximum (the order of z equals the order of z*log2e)
+    // and the label's logit, in the one chunk that holds it
+    float mx = -INFINITY, zy = 0.0f;
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       const int col0 = col_base + c * 32;
@@ -189,14 +191,22 @@ struct EpiLseStore {
       float v[32];
       tmem_ld32(taddr + c * 32, v);
       if (p.bias != nullptr) add_bias32<T>(p.bias, col0, p.V, v);
+      if (static_cast<uint64_t>(ylocal - c * 32) < 32u) zy = pick32(v, ylocal, c * 32);
+      if (col0 + 32 <= p.V) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float x = v[j];
-        if (c * 32 + j == ylocal) zy = x;
-        if (col0 + j < p.V) m = fmaxf(m, x * kLog2e);
+        for (int j = 0; j < 32; ++j) mx = fmaxf(mx, v[j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (col0 + j < p.V) mx = fmaxf(mx, v[j]);
       }
     }
-    float s = 0.0f;
+    const float m = mx * kLog2e;
+    // pass 2: u = z*log2e - m by packed pairs, stored; the sum of 2^u in four
+    // packed accumulators
+    const float2 lg = make_float2(kLog2e, kLog2e), nm = make_float2(-m, -m);
+    float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                     make_float2(0.0f, 0.0f)};
 #pragma unroll 1
     for (int g = 0; g < BN / CPS; ++g) {
       const int col0 = col_base + g * CPS;
@@ -208,12 +218,18 @@ struct EpiLseStore {
         tmem_ld32(taddr + g * CPS + h * 32, v);
         const int cb = col0 + h * 32;
         if (p.bias != nullptr) add_bias32<T>(p.bias, cb, p.V, v);
+        const bool full = cb + 32 <= p.V;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float x = v[j];
-          const float u = fmaf(x, kLog2e, -m);
-          if (cb + j < p.V) s += ex2(u);
-          v[j] = u;
+        for (int j = 0; j < 32; j += 2) {
+          const float2 u = __ffma2_rn(make_float2(v[j], v[j + 1]), lg, nm);
+          float2 e = make_float2(ex2(u.x), ex2(u.y));
+          if (!full) {
+            e.x = cb + j < p.V ? e.x : 0.0f;
+            e.y = cb + j + 1 < p.V ? e.y : 0.0f;
+          }
+          acc[(j >> 1) & 3] = __fadd2_rn(acc[(j >> 1) & 3], e);
+          v[j] = u.x;
+          v[j + 1] = u.y;
         }
 #pragma unroll
         for (int k = 0; k < 32 / EPV; ++k) {
@@ -225,6 +241,8 @@ struct EpiLseStore {
       }
       ctx.store_slab(packed, col0, r0, false);
     }
+    const float2 a2 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+    const float s = a2.x + a2.y;
     if (row_ok && in_range(row, p.part_ld, p.status)) {
       p.part_m[nt * p.part_ld + row] = m;
       p.part_s[nt * p.part_ld + row] = s;
