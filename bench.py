@@ -39,7 +39,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # profiles/ce_logits_16384x128256_launch_list_and_full_set.md, valid only for
 # the kernel sources they were taken from (sha256 prefix below); any change to
 # them reports null.
-TRAFFIC = {"flce_step_bytes": 30.67e9, "ce_step_bytes": 12.55e9, "csrc_sha": "4ce36294d65f9fb6"}
+TRAFFIC = {"flce_step_bytes": 29.51e9, "ce_step_bytes": 12.55e9, "csrc_sha": "f111cf99f5024848"}
 
 
 def csrc_sha():
