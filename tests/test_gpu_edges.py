@@ -126,3 +126,39 @@ def test_ce_single_column(lh):
     torch.cuda.synchronize()
     assert abs(out.loss.item()) <= 1e-6 and out.n_valid.item() == 30
     assert float(grad.float().abs().max()) <= 1e-6
+
+
+@pytest.mark.parametrize("reduction", ["sum", "mean"])
+def test_flce_one_valid_row(lh, reduction):
+    # every row ignored but one: the loss is that row's, every other row's
+    # gradient is zero, and grad_W / grad_b come from that row alone
+    p = wl.random_flce(300, 128, 2000, torch.bfloat16, bias=True, seed=61, ignore_frac=0.0)
+    y = torch.full_like(p.labels, -100)
+    y[137] = 1999  # in the last, partial vocabulary tile
+    res = _flce_all(lh, p.H, p.W, p.bias, y, reduction)
+    _compare(p.H, p.W, p.bias, y, res, reduction)
+    out, bw, fo, fb = res
+    assert int(out.n_valid.item()) == 1
+    for g in (bw, fb):
+        gh = g.grad_H.float().cpu()
+        assert torch.count_nonzero(torch.cat([gh[:137], gh[138:]])) == 0
+
+
+@pytest.mark.parametrize("reduction", ["sum", "mean"])
+def test_ce_one_valid_row(lh, reduction):
+    p = wl.random_ce(200, 5000, torch.bfloat16, seed=62, ignore_frac=0.0)
+    logits = p.logits.cuda()
+    y = torch.full_like(p.labels, -100)
+    y[3] = 4999
+    out = lh.ce_logits_fwd(logits, y.cuda(), -100, reduction)
+    g = torch.ones(1, device="cuda")
+    for lse in (out.lse, None):
+        grad = lh.ce_logits_bwd(logits, y.cuda(), lse, out.n_valid, g, -100, reduction)
+        torch.cuda.synchronize()
+        lh.check_status(out.status)
+        ref = oracle.ce_forward(p.logits, y, -100, reduction)
+        assert int(out.n_valid.item()) == 1
+        assert abs(out.loss.item() - ref["loss"]) <= 1e-3 * abs(ref["loss"])
+        _grad_ok(grad, oracle.ce_backward(p.logits, y, -100, reduction), "dlogits")
+        gc = grad.float().cpu()
+        assert torch.count_nonzero(torch.cat([gc[:3], gc[4:]])) == 0
