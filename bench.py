@@ -35,11 +35,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per step of the
 # default workloads (FLCE fwd+bwd; CE fwd + in-place bwd), from the ncu launch
-# lists summarised in profiles/flce_llama3_8b_launch_list.md and
-# profiles/ce_logits_16384x128256_launch_list_and_full_set.md, valid only for
-# the kernel sources they were taken from (sha256 prefix below); any change to
+# lists of the two workloads summarised under profiles/, valid only for the
+# kernel sources they were taken from (sha256 prefix below); any change to
 # them reports null.
-TRAFFIC = {"flce_step_bytes": 29.51e9, "ce_step_bytes": 12.55e9, "csrc_sha": "f111cf99f5024848"}
+TRAFFIC = {"flce_step_bytes": 29.51e9, "ce_step_bytes": 12.55e9, "csrc_sha": "ff604bf7e5f2a349"}
 
 
 def csrc_sha():

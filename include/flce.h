@@ -81,7 +81,7 @@ typedef enum {
   FLCE_ELABEL = -5,      /* (device) label outside [0,V) and != ignore_index */
   FLCE_EWORKSPACE = -6,  /* workspace pointer null or too small              */
   FLCE_ECUDA = -7,       /* a CUDA runtime/driver call failed                */
-  FLCE_ENOSUP = -8,      /* valid request this build does not support        */
+  FLCE_ENOSUP = -8,      /* valid request this library does not support      */
   FLCE_ETIMEOUT = -9,    /* (device) a bounded wait inside a kernel gave up  */
   FLCE_EBOUNDS = -10     /* (device, checked builds) an index left its range  */
 } flce_status_t;

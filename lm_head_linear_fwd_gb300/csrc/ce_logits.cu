@@ -1019,7 +1019,7 @@ extern "C" const char* flce_status_string(int status) {
     case FLCE_ELABEL: return "FLCE_ELABEL: label outside [0, V) that is not ignore_index";
     case FLCE_EWORKSPACE: return "FLCE_EWORKSPACE: workspace missing or too small";
     case FLCE_ECUDA: return "FLCE_ECUDA: CUDA call failed";
-    case FLCE_ENOSUP: return "FLCE_ENOSUP: not supported by this build";
+    case FLCE_ENOSUP: return "FLCE_ENOSUP: not supported by this library";
     case FLCE_ETIMEOUT: return "FLCE_ETIMEOUT: a bounded wait inside a kernel gave up";
     case FLCE_EBOUNDS: return "FLCE_EBOUNDS: a device-side index check failed (checked build)";
     default: return "FLCE: unknown status";
