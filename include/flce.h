@@ -44,8 +44,9 @@
  * Errors.  Every entry point returns a flce_status_t.  Errors that the host can
  * see (null pointers, bad sizes, bad alignment, too small a workspace) are
  * returned before anything is enqueued.  Errors only the device can see (a
- * label outside [0, V) that is not ignore_index; a bounded wait that gave up)
- * are written to the device word *status with "first error wins" semantics:
+ * label outside [0, V) that is not ignore_index; a bounded wait that gave up;
+ * in the debug build, an index check that failed) are written to the device
+ * word *status with "first error wins" semantics:
  * the library never clears *status, so a nonzero value stays until the caller
  * resets it.  Rows whose label is out of range contribute nothing to the loss,
  * n_valid or the gradients.  No kernel traps or asserts.
