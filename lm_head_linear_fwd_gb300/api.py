@@ -85,6 +85,7 @@ def _labels(labels: torch.Tensor, N: int) -> torch.Tensor:
 
 @dataclasses.dataclass
 class ForwardOut:
+    """Device outputs of a forward call (reusable through ``out=``)."""
     loss: torch.Tensor           # [1] f32
     n_valid: torch.Tensor        # [1] i64
     lse: torch.Tensor            # [N] f32
@@ -94,12 +95,18 @@ class ForwardOut:
 
 
 def ce_logits_workspace_bytes(N: int, V: int) -> int:
+    """Bytes of device workspace ce_logits_fwd needs for [N, V] logits."""
     return int(_abi.ce_logits_workspace_bytes(N, V))
 
 
 def ce_logits_fwd(logits, labels, ignore_index=-100, reduction="sum", num_label_tokens=None, *,
                   want_rows=False, want_label_logit=False, ws=None, status=None,
                   out=None) -> ForwardOut:
+    """Forward of cross-entropy on given logits [N, V] (bf16 or fp32, row
+    stride free, unit stride along V).  Returns the loss, n_valid, the per-row
+    lse (what the backward needs) and, on request, per-row losses and the
+    gathered label logits.  ``ws``/``status``/``out`` let a caller reuse
+    buffers (a CUDA graph, a loop); otherwise they are allocated here."""
     _cuda(logits, "logits")
     if logits.dim() != 2 or logits.stride(1) != 1:
         raise ValueError("logits must be 2-D with unit stride along the vocabulary")
@@ -226,10 +233,12 @@ def mask_packed_labels(labels: torch.Tensor, doc_ids: torch.Tensor, ignore_index
 # ---------------------------------------------------------- fused linear CE
 
 def flce_workspace_bytes(dt_code: int, N: int, D: int, V: int, chunk: int = 0) -> int:
+    """Bytes of device workspace flce_fwd / flce_bwd need (chunk 0: the default)."""
     return int(_abi.flce_workspace_bytes(dt_code, N, D, V, chunk))
 
 
 def flce_default_chunk(dt_code: int, N: int, D: int, V: int) -> int:
+    """Rows per backward chunk when none is given (sizes the dZ buffer)."""
     return int(_abi.flce_default_chunk(dt_code, N, D, V))
 
 
@@ -252,6 +261,10 @@ def _flce_inputs(H, W, bias):
 def flce_fwd(H, W, labels, bias=None, ignore_index=-100, reduction="sum", num_label_tokens=None,
              *, want_rows=False, want_label_logit=False, ws=None, status=None,
              out=None) -> ForwardOut:
+    """Forward of fused linear cross-entropy: logits = H @ W.T (+ bias) are
+    reduced tile by tile and never stored.  H [N, D], W [V, D], bias [V] or
+    None, one dtype (bf16, or fp32 computed in tf32).  Returns the loss,
+    n_valid and the per-row lse the backward needs."""
     N, D, V = _flce_inputs(H, W, bias)
     labels = _labels(labels, N)
     dev = H.device
@@ -277,6 +290,7 @@ def flce_fwd(H, W, labels, bias=None, ignore_index=-100, reduction="sum", num_la
 
 @dataclasses.dataclass
 class BackwardOut:
+    """Gradients of a backward call (None where not requested)."""
     grad_H: Optional[torch.Tensor]
     grad_W: Optional[torch.Tensor]     # fp32
     grad_bias: Optional[torch.Tensor]  # fp32
@@ -286,6 +300,10 @@ def flce_bwd(H, W, labels, lse, n_valid, grad_loss, bias=None, ignore_index=-100
              num_label_tokens=None, chunk=None, *, want_grad_H=True, want_grad_W=True,
              want_grad_bias=None, grad_W=None, accumulate_grad_W=False, grad_H=None,
              grad_bias=None, ws=None, status=None) -> BackwardOut:
+    """Backward of fused linear cross-entropy, recomputing the logits chunk
+    by chunk: grad_H (dtype of H), grad_W (fp32; added to ``grad_W`` when
+    ``accumulate_grad_W``) and grad_bias (fp32), from the forward's lse and
+    n_valid and the incoming gradient ``grad_loss``."""
     N, D, V = _flce_inputs(H, W, bias)
     labels = _labels(labels, N)
     dev = H.device

@@ -45,6 +45,7 @@ class TorchDistExchange:
 
 @dataclasses.dataclass
 class ShardForward:
+    """Forward results of a vocabulary shard, already reduced over the ranks."""
     loss: torch.Tensor      # [1] f32, identical on every rank
     n_valid: torch.Tensor   # [1] i64
     lse: torch.Tensor       # [N] f32 (global)
