@@ -27,8 +27,7 @@ numpy's ``@``; rows are processed in blocks only so that no float64 [N, V]
 array is ever held (blocking does not change the definition: each row is
 independent and the gradient sums are plain sums over rows).
 
-Readings of points the pages leave open (each is also listed in the design
-notes of the repository):
+Readings of points the pages leave open:
 
 1. ``reduction="mean"`` divides by the number of non-ignored rows (the
    ``F.cross_entropy`` meaning).  If every row is ignored the loss and all
