@@ -26,6 +26,23 @@ for i in range(12):
         seed=1000 + i))
 
 
+# a second draw: larger vocabularies, ignored fractions up to one half, and
+# row counts around multiples of the 128-row tile
+_rng2 = np.random.default_rng(7)
+for i in range(8):
+    CASES.append(dict(
+        N=int(_rng2.integers(1, 12)) * 128 + int(_rng2.integers(-2, 3)) + 2,
+        D=int(_rng2.integers(1, 40)) * 16,
+        V=int(_rng2.integers(9000, 40000)),
+        dtype=torch.bfloat16,
+        bias=bool(_rng2.random() < 0.5),
+        reduction=str(_rng2.choice(["sum", "mean"])),
+        nlt=None,
+        chunk=None if _rng2.random() < 0.5 else int(_rng2.integers(1, 6)) * 128,
+        ignore=float(_rng2.choice([0.0, 0.1, 0.5])),
+        seed=2000 + i))
+
+
 def _grad_ok(got, want, name):
     mr = oracle.max_rel_err(got.float().cpu(), want)
     nw = oracle.normwise_err(got.float().cpu(), want)
@@ -36,8 +53,8 @@ def _grad_ok(got, want, name):
 def test_flce_random_shape(case):
     import lm_head_linear_fwd_gb300 as lh
     p = wl.random_flce(case["N"], case["D"], case["V"], case["dtype"], bias=case["bias"],
-                       seed=case["seed"], reduction=case["reduction"],
-                       num_label_tokens=case["nlt"], w_std=0.05)
+                       seed=case["seed"], ignore_frac=case.get("ignore", 0.1),
+                       reduction=case["reduction"], num_label_tokens=case["nlt"], w_std=0.05)
     H, W, y = p.H.cuda(), p.W.cuda(), p.labels.cuda()
     b = p.bias.cuda() if p.bias is not None else None
     ref = oracle.flce_forward(p.H, p.W, p.bias, p.labels, -100, p.reduction, p.num_label_tokens)
