@@ -94,6 +94,12 @@ def test_ce_random_shape(case):
     assert abs(out.loss.item() - ref["loss"]) <= 1e-3 * abs(ref["loss"]) + 1e-6
     lse = out.lse.cpu().double().numpy()
     assert np.all(np.abs(lse - ref["lse"]) <= 5e-5 * (1 + np.abs(ref["lse"])))
+    # the same gradient without the saved lse (formed again in the backward)
+    grad2 = lh.ce_logits_bwd(logits, y, None, out.n_valid, torch.ones(1, device="cuda"), -100,
+                             c.reduction, c.num_label_tokens, status=out.status)
+    torch.cuda.synchronize()
+    lh.check_status(out.status)
     if ref["loss"] != 0.0:
-        _grad_ok(grad, oracle.ce_backward(c.logits, c.labels, -100, c.reduction,
-                                          c.num_label_tokens), "dZ")
+        want = oracle.ce_backward(c.logits, c.labels, -100, c.reduction, c.num_label_tokens)
+        _grad_ok(grad, want, "dZ")
+        _grad_ok(grad2, want, "dZ without a saved lse")
