@@ -447,6 +447,7 @@ def run_ours(args, rank, ws, local):
     # the backward alone, with the saved lse and without it (out of place)
     restore()
     ce_bwd_line = ce_bwd_compare(c, co, cst, one, stream, args, ws, peaks)
+    ce_one_line = ce_one_call(c, cst, stream, args, ws, peaks)
     del pristine, logits, c, cws, co
     torch.cuda.empty_cache()
 
@@ -505,6 +506,7 @@ def run_ours(args, rank, ws, local):
             "peak_extra_gib": round(ce_peak_extra / 2**30, 6),
             "tokens_per_s": round(ce_N * ws / (ce_ms * 1e-3), 1),
             "bwd_only": ce_bwd_line,
+            "fwd_bwd_one_call": ce_one_line,
         },
         "roofline": {
             "bound": "tensor",
@@ -598,6 +600,40 @@ def ce_bwd_compare(c, co, cst, one, stream, args, ws, peaks):
     return line
 
 
+def ce_one_call(c, cst, stream, args, ws, peaks):
+    """Device time of ce_logits_fwd_bwd (loss and gradient in one call, g = 1)
+    on the given-logits workload, out of place, against the same bytes as the
+    separate forward and in-place backward."""
+    import torch
+    import lm_head_linear_fwd_gb300 as lh
+    logits, labels = c.logits, c.labels
+    gbuf = torch.empty_like(logits)
+    cws = torch.empty(max(1, lh.ce_logits_fwd_bwd_workspace_bytes(c.N, c.V)), dtype=torch.uint8,
+                      device=logits.device)
+    out, _ = lh.ce_logits_fwd_bwd(logits, labels, c.ignore_index, c.reduction,
+                                  c.num_label_tokens, grad_logits=gbuf, ws=cws, status=cst)
+
+    def fn():
+        lh.ce_logits_fwd_bwd(logits, labels, c.ignore_index, c.reduction, c.num_label_tokens,
+                             grad_logits=gbuf, ws=cws, status=cst, out=out)
+
+    for _ in range(max(3, args.warmup)):
+        fn()
+    t = _events_time(fn, args.steps, stream)
+    ms = max_over_ranks(sum(t) / len(t), ws)
+    lh.check_status(cst, "ce_logits_fwd_bwd")
+    n_valid_rows = int((labels != c.ignore_index).sum().item())
+    nbytes = (n_valid_rows + c.N) * float(c.V * 2)
+    del gbuf, cws
+    return {"what": "ce_logits_fwd_bwd: loss and gradient in one call (g = 1), out of place",
+            "ms": round(ms, 4),
+            "tokens_per_s": round(c.N * ws / (ms * 1e-3), 1),
+            "gb_s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+            "frac_of_hbm": round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "bytes": (f"read of the {n_valid_rows} non-ignored rows + write of all {c.N} rows "
+                      "(a row cluster holds each row in shared memory)")}
+
+
 def run_ce_only(args, rank, ws, local, dev, stream, peaks, peak_src):
     """Given-logits part alone (profiling runs)."""
     import torch
@@ -622,6 +658,7 @@ def run_ce_only(args, rank, ws, local, dev, stream, peaks, peak_src):
     ms = max_over_ranks(sum(t) / len(t), ws)
     gbs = 3.0 * c.N * c.V * 2 / (ms * 1e-3) / 1e9
     bwd_line = ce_bwd_compare(c, co, cst, one, stream, args, ws, peaks)
+    one_line = ce_one_call(c, cst, stream, args, ws, peaks)
     if rank == 0:
         print(json.dumps({"metric": METRIC, "value": round(gbs, 1), "unit": "GB/s",
                           "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
@@ -629,6 +666,7 @@ def run_ce_only(args, rank, ws, local, dev, stream, peaks, peak_src):
                           "config": {"workload": f"CE on logits only [{c.N},{c.V}] bf16"},
                           "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
                           "bwd_only": bwd_line,
+                          "fwd_bwd_one_call": one_line,
                           "note": "profiling run: given-logits part only"}))
 
 

@@ -209,6 +209,36 @@ FLCE_API int ce_logits_bwd(const void* logits, int dt, int64_t N, int64_t V, int
                   const float* grad_loss, int inplace_grad, void* grad_logits,
                   int64_t ld_grad, int32_t* status, flce_stream_t stream);
 
+/* Bytes of device workspace ce_logits_fwd_bwd needs for N rows.  Returns 0
+ * for N <= 0. */
+FLCE_API size_t ce_logits_fwd_bwd_workspace_bytes(int64_t N, int64_t V);
+
+/* Forward and backward in one call: the loss (as ce_logits_fwd) and the
+ * gradient of the logits (as ce_logits_bwd) when the incoming gradient is
+ * known before the loss, typically g = 1 for a loss that is the last node.
+ * The eager-gradient counterpart of flce_fwd_bwd for given logits (Automodel
+ * PR #2996 computes the logits' gradient during the forward in the same way);
+ * the source pages define no separate operation.
+ *
+ * Arguments as ce_logits_fwd and ce_logits_bwd.  grad_loss ([1] f32 device)
+ * may be NULL, meaning g = 1 (scale later with flce_grad_scale).  lse ([N] f32)
+ * may be NULL; when given it holds the lse of every row with a valid label
+ * (other rows: unspecified).  inplace_grad, grad_logits, ld_grad: as in
+ * ce_logits_bwd; in place, the logits are overwritten by their gradient.
+ * ws: ce_logits_fwd_bwd_workspace_bytes(N, V) bytes, 16-byte aligned.
+ *
+ * Rows whose start, stride and length are 16-byte multiples in both the
+ * logits and the gradient, and at most 8 x 64 KiB long, are read once: a
+ * thread-block cluster holds each row in shared memory, forms its lse and
+ * loss and writes its gradient (rows with an ignored label are not read).
+ * Other rows run the forward and then the backward (two reads). */
+FLCE_API int ce_logits_fwd_bwd(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
+                  const int64_t* labels, int64_t ignore_index, int reduction,
+                  int64_t num_label_tokens, const float* grad_loss, float* loss,
+                  int64_t* n_valid, float* lse, int inplace_grad, void* grad_logits,
+                  int64_t ld_grad, void* ws, size_t ws_bytes, int32_t* status,
+                  flce_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Fused linear cross-entropy                                               */
 /* ------------------------------------------------------------------------ */

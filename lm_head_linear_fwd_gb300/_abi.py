@@ -38,6 +38,9 @@ _SIGNATURES = {
                                    _p]),
     "ce_logits_bwd": (_i, [_p, _i, _i64, _i64, _i64, _p, _i64, _i, _i64, _p, _p, _p, _i, _p,
                            _i64, _p, _p]),
+    "ce_logits_fwd_bwd_workspace_bytes": (_sz, [_i64, _i64]),
+    "ce_logits_fwd_bwd": (_i, [_p, _i, _i64, _i64, _i64, _p, _i64, _i, _i64, _p, _p, _p, _p, _i,
+                               _p, _i64, _p, _sz, _p, _p]),
     "flce_workspace_bytes": (_sz, [_i, _i64, _i64, _i64, _i64]),
     "flce_default_chunk": (_i64, [_i, _i64, _i64, _i64]),
     "flce_fwd": (_i, [_p, _p, _p, _i, _i64, _i64, _i64, _p, _i64, _i, _i64, _p, _p, _p, _p, _p,
@@ -128,6 +131,8 @@ ce_logits_workspace_bytes = _call("ce_logits_workspace_bytes")
 ce_logits_fwd = _call("ce_logits_fwd")
 ce_logits_fwd_noalloc = _call("ce_logits_fwd_noalloc")
 ce_logits_bwd = _call("ce_logits_bwd")
+ce_logits_fwd_bwd_workspace_bytes = _call("ce_logits_fwd_bwd_workspace_bytes")
+ce_logits_fwd_bwd = _call("ce_logits_fwd_bwd")
 flce_workspace_bytes = _call("flce_workspace_bytes")
 flce_default_chunk = _call("flce_default_chunk")
 flce_fwd = _call("flce_fwd")

@@ -6,10 +6,11 @@ C ABI (``_abi``).  There is no CPU or eager-PyTorch fallback: a missing
 library or a non-CUDA tensor raises.
 
 Low-level calls (same names as the C entry points):
-    ce_logits_fwd, ce_logits_bwd, flce_fwd, flce_bwd, flce_fwd_bwd, flce_gemm
+    ce_logits_fwd, ce_logits_bwd, ce_logits_fwd_bwd, flce_fwd, flce_bwd,
+    flce_fwd_bwd, flce_gemm
 Autograd front ends:
     ce_logits(logits, labels, *, ignore_index, reduction, num_label_tokens,
-              inplace_grad=False, mask=None)
+              inplace_grad=False, mask=None, save_lse=True, eager=False)
     flce(H, W, labels, bias=None, *, ignore_index, reduction, num_label_tokens,
          chunk=None, mask=None, eager=False)
 """
@@ -159,6 +160,77 @@ def ce_logits_bwd(logits, labels, lse, n_valid, grad_loss, ignore_index=-100, re
     return grad_logits
 
 
+def ce_logits_fwd_bwd_workspace_bytes(N: int, V: int) -> int:
+    """Bytes of device workspace ce_logits_fwd_bwd needs for [N, V] logits."""
+    return int(_abi.ce_logits_fwd_bwd_workspace_bytes(N, V))
+
+
+def ce_logits_fwd_bwd(logits, labels, ignore_index=-100, reduction="sum", num_label_tokens=None,
+                      grad_loss=None, *, inplace_grad=False, grad_logits=None, want_lse=False,
+                      ws=None, status=None, out=None):
+    """Loss and gradient of the logits in one call (the gradient for the
+    incoming gradient ``grad_loss``, a [1] tensor; None means 1).  Aligned rows
+    are read once.  Returns (ForwardOut, grad_logits); ``ForwardOut.lse`` is
+    None unless ``want_lse`` (then valid on rows with a valid label).
+    ``ws``/``status``/``out``/``grad_logits`` let a caller reuse buffers."""
+    _cuda(logits, "logits")
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be 2-D with unit stride along the vocabulary")
+    N, V = logits.shape
+    labels = _labels(labels, N)
+    dev = logits.device
+    if inplace_grad:
+        grad_logits = logits
+    elif grad_logits is None:
+        grad_logits = torch.empty((N, V), dtype=logits.dtype, device=dev)
+    if grad_logits.dtype != logits.dtype or grad_logits.stride(1) != 1:
+        raise ValueError("grad_logits must have the logits dtype and unit column stride")
+    g = None
+    if grad_loss is not None:
+        g = grad_loss.to(device=dev, dtype=torch.float32).reshape(1).contiguous()
+    if out is None:
+        out = ForwardOut(
+            loss=torch.empty(1, dtype=torch.float32, device=dev),
+            n_valid=torch.empty(1, dtype=torch.int64, device=dev),
+            lse=torch.empty(N, dtype=torch.float32, device=dev) if want_lse else None,
+            loss_rows=None, label_logit=None,
+            status=status if status is not None else new_status(dev))
+    nbytes = ce_logits_fwd_bwd_workspace_bytes(N, V)
+    if ws is None:
+        ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    rc = _abi.ce_logits_fwd_bwd(_ptr(logits), _dtype_code(logits), N, V, logits.stride(0),
+                                _ptr(labels), int(ignore_index), _red_code(reduction),
+                                _nlt(num_label_tokens), _ptr(g), _ptr(out.loss),
+                                _ptr(out.n_valid), _ptr(out.lse), 1 if inplace_grad else 0,
+                                _ptr(grad_logits), grad_logits.stride(0), _ptr(ws), ws.numel(),
+                                _ptr(out.status), _stream(dev))
+    _abi.check(rc, "ce_logits_fwd_bwd")
+    return out, grad_logits
+
+
+class _CELogitsEager(torch.autograd.Function):
+    """The gradient formed during the forward (ce_logits_fwd_bwd with g = 1),
+    scaled by the incoming gradient in the backward."""
+
+    @staticmethod
+    def forward(ctx, logits, labels, ignore_index, reduction, num_label_tokens, inplace_grad):
+        out, grad = ce_logits_fwd_bwd(logits, labels, ignore_index, reduction, num_label_tokens,
+                                      inplace_grad=inplace_grad)
+        ctx.grad = grad
+        ctx.status = out.status
+        return out.loss.reshape(())
+
+    @staticmethod
+    @once_differentiable
+    def backward(ctx, g):
+        grad, ctx.grad = ctx.grad, None
+        if grad is None:
+            raise RuntimeError("ce_logits(eager=True): the gradient was already handed out; "
+                               "a second backward is not possible")
+        grad_scale_(grad, g)
+        return grad, None, None, None, None, None
+
+
 class _CELogits(torch.autograd.Function):
     @staticmethod
     def forward(ctx, logits, labels, ignore_index, reduction, num_label_tokens, inplace_grad,
@@ -198,15 +270,26 @@ def _fold_mask(labels, mask, ignore_index):
 
 
 def ce_logits(logits, labels, *, ignore_index=-100, reduction="sum", num_label_tokens=None,
-              inplace_grad=False, mask=None, save_lse=True):
+              inplace_grad=False, mask=None, save_lse=True, eager=False):
     """Masked cross-entropy on given logits [N, V] (bf16 or fp32).
 
     ``inplace_grad=True`` writes the gradient into the logits storage during
     backward (the logits are destroyed); it is keyword-only and off by default.
     ``mask`` (same shape as labels) marks rows to ignore with 0.
     ``save_lse=False`` keeps only the logits and labels (and the valid-row
-    count) for the backward, which then forms each row's lse again."""
+    count) for the backward, which then forms each row's lse again.
+    ``eager=True`` forms the gradient during the forward, reading each row
+    once for both, and keeps it until the backward scales it by the incoming
+    gradient (no work when that is 1); with ``inplace_grad=True`` the logits
+    are overwritten by their gradient already in the forward, and must then
+    be contiguous."""
     labels = _fold_mask(labels, mask, ignore_index)
+    if eager:
+        _cuda(logits, "logits")
+        if inplace_grad and not logits.is_contiguous():
+            raise ValueError("ce_logits(eager=True, inplace_grad=True) needs contiguous logits")
+        return _CELogitsEager.apply(logits, labels, int(ignore_index), reduction,
+                                    num_label_tokens, bool(inplace_grad))
     return _CELogits.apply(logits, labels, int(ignore_index), reduction, num_label_tokens,
                            bool(inplace_grad), bool(save_lse))
 

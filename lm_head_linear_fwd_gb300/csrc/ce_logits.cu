@@ -715,10 +715,15 @@ struct ResArgs {
   int64_t ldg;
   int32_t* status;
   int64_t slice_vec;  // 16-byte vectors per CTA slice (the last slice may be shorter)
+  // forward and backward in one pass (ce_logits_fwd_bwd): per-row losses and
+  // lse are written too, and every row with a valid label is read, also when
+  // its gradient is zero.  loss_rows == nullptr: the backward alone.
+  float* loss_rows;
+  float* lse_out;  // may be null
 };
 
 template <typename T>
-__global__ void __launch_bounds__(kResThreads) ce_bwd_resident_kernel(const ResArgs a) {
+__global__ void __launch_bounds__(kResThreads, 3) ce_bwd_resident_kernel(const ResArgs a) {
   constexpr int EPV = Elem<T>::kPerVec;
   extern __shared__ uint8_t res_raw[];
   __shared__ uint64_t bar[kResMaxSegs];
@@ -760,6 +765,7 @@ __global__ void __launch_bounds__(kResThreads) ce_bwd_resident_kernel(const ResA
   // the exchange barriers must be initialised in every CTA before any pair is sent
   cluster_sync();
   const float coef = grad_coef(a.reduction, a.num_label_tokens, a.n_valid, a.grad_loss);
+  const bool fused = a.loss_rows != nullptr;
   const int64_t first = blockIdx.x / P;
 
   // Rows of this cluster: first + i * nclusters.  Each warp reads the labels
@@ -779,7 +785,7 @@ __global__ void __launch_bounds__(kResThreads) ce_bwd_resident_kernel(const ResA
         bool nd = false;
         if (r < a.N) {
           const int64_t yr = __ldg(a.labels + r);
-          nd = coef != 0.0f && yr != a.ignore_index && label_ok(yr, a.V);
+          nd = (fused || coef != 0.0f) && yr != a.ignore_index && label_ok(yr, a.V);
         }
         todo = __ballot_sync(0xffffffffu, r < a.N);
         need = __ballot_sync(0xffffffffu, nd);
@@ -791,6 +797,12 @@ __global__ void __launch_bounds__(kResThreads) ce_bwd_resident_kernel(const ResA
       uint4* out = reinterpret_cast<uint4*>(static_cast<T*>(a.grad) + r * a.ldg) + v_lo;
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
       for (int v = tid; v < nv; v += kResThreads) __stcs(out + v, z);
+      if (fused && rank == 0 && tid == 0) {  // an ignored (or out-of-range) label: no loss
+        const int64_t yr = __ldg(a.labels + r);
+        if (yr != a.ignore_index) set_status(a.status, FLCE_ELABEL);
+        a.loss_rows[r] = 0.0f;
+        if (a.lse_out != nullptr) a.lse_out[r] = NAN;
+      }
     }
   };
 
@@ -879,6 +891,14 @@ __global__ void __launch_bounds__(kResThreads) ce_bwd_resident_kernel(const ResA
     }
     __syncthreads();
     const float lse2 = lse2_sh;
+    if (fused && tid == 0) {
+      // the row's loss, from the CTA whose slice holds the label's logit
+      const float lse = lse2 * kLn2;
+      const int64_t yl = y - v_lo * EPV;
+      if (yl >= 0 && yl < static_cast<int64_t>(nv) * EPV)
+        a.loss_rows[row] = lse - Elem<T>::load(reinterpret_cast<const T*>(buf) + yl);
+      if (rank == 0 && a.lse_out != nullptr) a.lse_out[row] = lse;
+    }
     if (!*abort_flag) {
       uint4* out = reinterpret_cast<uint4*>(static_cast<T*>(a.grad) + row * a.ldg) + v_lo;
       const int64_t ylocal = y - v_lo * EPV;  // label element relative to the slice
@@ -1251,20 +1271,11 @@ extern "C" int ce_logits_fwd_noalloc(const void* logits, int dt, int64_t N, int6
                        loss, n_valid, lse, rows, nullptr, nullptr, 0, status, stream);
 }
 
-static int ce_bwd_entry(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
-                        int64_t v0, int64_t V_total, const int64_t* labels,
-                        int64_t ignore_index, int reduction, int64_t num_label_tokens,
-                        const float* lse, const int64_t* n_valid, const float* grad_loss,
-                        int inplace_grad, void* grad_logits, int64_t ld_grad, int32_t* status,
-                        flce_stream_t stream) {
-  int rc = ce_common_checks(logits, dt, N, V, ld, labels, reduction);
-  if (rc != FLCE_OK) return rc;
-  if (v0 < 0 || V_total < v0 + V || V_total >= (int64_t(1) << 31)) return FLCE_ESHAPE;
-  if (status == nullptr) return FLCE_EINVAL;
-  if (N == 0) return FLCE_OK;
-  if (n_valid == nullptr || grad_loss == nullptr || grad_logits == nullptr) return FLCE_EINVAL;
-  // no saved lse: only for a whole vocabulary (a shard needs the global lse)
-  if (lse == nullptr && (v0 != 0 || V_total != V)) return FLCE_EINVAL;
+// The gradient buffer's rules (N > 0): in place it is the logits storage with
+// the same row stride; otherwise it must not overlap the logits.
+static int grad_buffer_checks(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
+                              int inplace_grad, const void* grad_logits, int64_t ld_grad) {
+  if (grad_logits == nullptr) return FLCE_EINVAL;
   if (inplace_grad != 0 && inplace_grad != 1) return FLCE_EINVAL;
   if (ld_grad < V) return FLCE_ESHAPE;
   if (!aligned(grad_logits, dtype_size(dt))) return FLCE_EALIGN;
@@ -1278,6 +1289,27 @@ static int ce_bwd_entry(const void* logits, int dt, int64_t N, int64_t V, int64_
   } else if (b0 < a1 && a0 < b1) {
     return FLCE_EINVAL;  // out-of-place buffers must not overlap
   }
+  return FLCE_OK;
+}
+
+// grad_loss may be null only for the library's own calls (g = 1).
+static int ce_bwd_entry(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
+                        int64_t v0, int64_t V_total, const int64_t* labels,
+                        int64_t ignore_index, int reduction, int64_t num_label_tokens,
+                        const float* lse, const int64_t* n_valid, const float* grad_loss,
+                        int inplace_grad, void* grad_logits, int64_t ld_grad, int32_t* status,
+                        flce_stream_t stream, bool g_optional = false) {
+  int rc = ce_common_checks(logits, dt, N, V, ld, labels, reduction);
+  if (rc != FLCE_OK) return rc;
+  if (v0 < 0 || V_total < v0 + V || V_total >= (int64_t(1) << 31)) return FLCE_ESHAPE;
+  if (status == nullptr) return FLCE_EINVAL;
+  if (N == 0) return FLCE_OK;
+  if (n_valid == nullptr || (grad_loss == nullptr && !g_optional)) return FLCE_EINVAL;
+  // no saved lse: only for a whole vocabulary (a shard needs the global lse)
+  if (lse == nullptr && (v0 != 0 || V_total != V)) return FLCE_EINVAL;
+  rc = grad_buffer_checks(logits, dt, N, V, ld, inplace_grad, grad_logits, ld_grad);
+  if (rc != FLCE_OK) return rc;
+  const size_t es = dtype_size(dt);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool stream_ok = streamable(logits, ld, V, es) && streamable(grad_logits, ld_grad, V, es);
   if (stream_ok && lse == nullptr) {
@@ -1358,4 +1390,74 @@ extern "C" int ce_logits_bwd_shard(const void* logits_shard, int dt, int64_t N, 
   return ce_bwd_entry(logits_shard, dt, N, V_shard, ld, vocab_offset, V_total, labels,
                       ignore_index, reduction, num_label_tokens, lse, n_valid, grad_loss,
                       inplace_grad, grad_logits, ld_grad, status, stream);
+}
+
+// ------------------------------------------------- forward and backward in one call
+
+extern "C" size_t ce_logits_fwd_bwd_workspace_bytes(int64_t N, int64_t V) {
+  if (N < 0 || V < 1) return 0;
+  // per-row losses and, for the two-call fallback, a per-row lse
+  return 2 * round_up(static_cast<size_t>(N) * 4, 256) + ce_logits_workspace_bytes(N, V);
+}
+
+extern "C" int ce_logits_fwd_bwd(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
+                                 const int64_t* labels, int64_t ignore_index, int reduction,
+                                 int64_t num_label_tokens, const float* grad_loss, float* loss,
+                                 int64_t* n_valid, float* lse, int inplace_grad,
+                                 void* grad_logits, int64_t ld_grad, void* ws, size_t ws_bytes,
+                                 int32_t* status, flce_stream_t stream) {
+  int rc = ce_common_checks(logits, dt, N, V, ld, labels, reduction);
+  if (rc != FLCE_OK) return rc;
+  if (loss == nullptr || n_valid == nullptr || status == nullptr) return FLCE_EINVAL;
+  if (N > 0) {
+    rc = grad_buffer_checks(logits, dt, N, V, ld, inplace_grad, grad_logits, ld_grad);
+    if (rc != FLCE_OK) return rc;
+  }
+  const size_t need = ce_logits_fwd_bwd_workspace_bytes(N, V);
+  if (N > 0 && (ws == nullptr || ws_bytes < need)) return FLCE_EWORKSPACE;
+  if (ws != nullptr && !aligned(ws, 16)) return FLCE_EALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  float* rows = reinterpret_cast<float*>(w);
+  float* lse_buf = reinterpret_cast<float*>(w + round_up(static_cast<size_t>(N) * 4, 256));
+  char* fwd_ws = w + 2 * round_up(static_cast<size_t>(N) * 4, 256);
+  const size_t fwd_ws_bytes = ws_bytes > 2 * round_up(static_cast<size_t>(N) * 4, 256)
+                                  ? ws_bytes - 2 * round_up(static_cast<size_t>(N) * 4, 256)
+                                  : 0;
+  const size_t es = dtype_size(dt);
+  if (N > 0 && streamable(logits, ld, V, es) && streamable(grad_logits, ld_grad, V, es)) {
+    // one pass: the count of valid rows first (the mean's divisor), then each
+    // row read once by a row cluster that forms its lse, loss and gradient
+    rc = flce_count_valid(labels, N, V, ignore_index, n_valid, stream);
+    if (rc != FLCE_OK) return rc;
+    ResArgs r{};
+    r.logits = logits;
+    r.N = N;
+    r.V = V;
+    r.ld = ld;
+    r.labels = labels;
+    r.ignore_index = ignore_index;
+    r.reduction = reduction;
+    r.num_label_tokens = num_label_tokens;
+    r.n_valid = n_valid;
+    r.grad_loss = grad_loss;  // null: g = 1
+    r.grad = grad_logits;
+    r.ldg = ld_grad;
+    r.status = status;
+    r.loss_rows = rows;
+    r.lse_out = lse;
+    rc = dt == FLCE_BF16 ? launch_resident<__nv_bfloat16>(r, s) : launch_resident<float>(r, s);
+    if (rc == FLCE_OK)
+      return launch_finalize(rows, labels, N, V, ignore_index, reduction, num_label_tokens, loss,
+                             n_valid, s);
+    if (rc != 1) return rc;
+  }
+  // rows that no cluster holds: the forward, then the backward
+  float* l = lse != nullptr ? lse : lse_buf;
+  rc = ce_logits_fwd(logits, dt, N, V, ld, labels, ignore_index, reduction, num_label_tokens, loss,
+                     n_valid, l, rows, nullptr, fwd_ws, fwd_ws_bytes, status, stream);
+  if (rc != FLCE_OK || N == 0) return rc;
+  return ce_bwd_entry(logits, dt, N, V, ld, 0, V, labels, ignore_index, reduction,
+                      num_label_tokens, l, n_valid, grad_loss, inplace_grad, grad_logits,
+                      ld_grad, status, stream, true);
 }

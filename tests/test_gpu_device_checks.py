@@ -50,7 +50,8 @@ def test_build_flags_and_bounds_selftest(libs):
 
 def _ce_cases():
     # (dtype, N, V, ld): the bulk-copy ring, the unaligned row kernels, and for
-    # the no-lse backward clusters of 1 and 4 and the twice-streamed rows
+    # the no-lse backward and the one-call forward and backward clusters of 1
+    # and 4 and the twice-streamed rows
     return [(torch.bfloat16, 300, 5000, 5000), (torch.bfloat16, 77, 1003, 1011),
             (torch.float32, 64, 4100, 4104), (torch.bfloat16, 64, 128256, 128256),
             (torch.bfloat16, 4, 300000, 300000)]
@@ -64,8 +65,11 @@ def _run_ce(lh, dtype, N, V, ld):
     g = torch.tensor([0.9], device="cuda")
     saved = lh.ce_logits_bwd(logits, labels, o.lse, o.n_valid, g, -100, "mean", status=st)
     nolse = lh.ce_logits_bwd(logits, labels, None, o.n_valid, g, -100, "mean", status=st)
+    fo, fg = lh.ce_logits_fwd_bwd(logits, labels, -100, "mean", None, g, want_lse=True,
+                                  status=st)
     torch.cuda.synchronize()
-    return st, [o.loss, o.lse, o.loss_rows, o.n_valid, saved, nolse]
+    return st, [o.loss, o.lse, o.loss_rows, o.n_valid, saved, nolse, fo.loss,
+                fo.lse.nan_to_num(0.0), fg]
 
 
 def _run_flce(lh, dtype, N, D, V, bias):

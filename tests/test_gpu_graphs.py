@@ -91,3 +91,44 @@ def test_ce_without_saved_lse_in_a_cuda_graph():
         lh.check_status(st)
         for g, e in zip(grads, eager):
             assert torch.equal(g, e)
+
+
+def test_ce_fwd_bwd_in_a_cuda_graph():
+    # the one-call forward and backward: the row-cluster kernel in its fused
+    # mode, and the two-call fallback for unaligned rows
+    import lm_head_linear_fwd_gb300 as lh
+    cases = [wl.random_ce(96, 128256, torch.bfloat16, seed=43),
+             wl.random_ce(64, 1003, torch.bfloat16, seed=44)]
+    dev = [(c.logits.cuda().contiguous(), c.labels.cuda()) for c in cases]
+    st = lh.new_status("cuda")
+    half = torch.full((1,), 0.5, device="cuda")
+    grads = [torch.empty_like(x) for x, _ in dev]
+    outs = [lh.ce_logits_fwd_bwd(x, y, reduction="mean", grad_loss=half, grad_logits=g,
+                                 want_lse=True, status=st)[0]
+            for (x, y), g in zip(dev, grads)]
+
+    def step():
+        for (x, y), o, g in zip(dev, outs, grads):
+            lh.ce_logits_fwd_bwd(x, y, reduction="mean", grad_loss=half, grad_logits=g,
+                                 status=st, out=o)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    res = lambda: [t for o, g in zip(outs, grads) for t in (o.loss, o.lse.nan_to_num(0.0), g)]
+    eager = [t.clone() for t in res()]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(2):
+        for o, g in zip(outs, grads):
+            g.zero_()
+            o.loss.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        lh.check_status(st)
+        for a, e in zip(res(), eager):
+            assert torch.equal(a, e)
