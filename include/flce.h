@@ -216,9 +216,11 @@ FLCE_API size_t ce_logits_fwd_bwd_workspace_bytes(int64_t N, int64_t V);
 /* Forward and backward in one call: the loss (as ce_logits_fwd) and the
  * gradient of the logits (as ce_logits_bwd) when the incoming gradient is
  * known before the loss, typically g = 1 for a loss that is the last node.
- * The eager-gradient counterpart of flce_fwd_bwd for given logits (Automodel
- * PR #2996 computes the logits' gradient during the forward in the same way);
- * the source pages define no separate operation.
+ * The eager-gradient counterpart of flce_fwd_bwd for given logits: the
+ * gradient is formed while the loss is computed and handed out later, as
+ * Liger's fused linear cross-entropy does with its weight gradient
+ * (Liger-Kernel issue #533, "Gradient checkpointing for grad_weight in
+ * LFCE"); the pages define no such call for given logits.
  *
  * Arguments as ce_logits_fwd and ce_logits_bwd.  grad_loss ([1] f32 device)
  * may be NULL, meaning g = 1 (scale later with flce_grad_scale).  lse ([N] f32)

@@ -689,7 +689,9 @@ static int launch_stream(const StreamArgs& a, cudaStream_t s) {
 // cluster drift apart by a row) need twice the CTAs per row and were 15-30%
 // slower; one barrier.cluster per row instead of st.async 5% slower; streaming
 // each row twice through the ring 25% slower (about even with L2 evict_last /
-// evict_first hints at 2 CTAs per SM).
+// evict_first hints at 2 CTAs per SM); copying the next row into each pair of
+// segments as soon as its dZ is written (same shared memory) 0.3% faster, not
+// worth its bookkeeping.
 #ifndef FLCE_CE_RES_BUF
 #define FLCE_CE_RES_BUF 65536
 #endif
