@@ -269,6 +269,23 @@ def _fold_mask(labels, mask, ignore_index):
     return labels.masked_fill(mask.to(device=labels.device) == 0, ignore_index)
 
 
+def _rows(x, labels, mask, what):
+    """Leading dimensions flattened into rows: x [..., K] -> [N, K] (a view when
+    the strides allow it; autograd maps the gradient back), labels and mask
+    [...] -> [N]."""
+    if not isinstance(x, torch.Tensor) or x.dim() < 2:
+        raise ValueError(f"{what} must be at least 2-D")
+    lead = x.shape[:-1]
+    if tuple(labels.shape) != tuple(lead):
+        raise ValueError(f"labels must have the leading shape {tuple(lead)} of {what}")
+    if mask is not None and tuple(mask.shape) != tuple(lead):
+        raise ValueError(f"mask must have the shape {tuple(lead)} of the labels")
+    if x.dim() == 2:
+        return x, labels, mask
+    return (x.reshape(-1, x.shape[-1]), labels.reshape(-1),
+            None if mask is None else mask.reshape(-1))
+
+
 def ce_logits(logits, labels, *, ignore_index=-100, reduction="sum", num_label_tokens=None,
               inplace_grad=False, mask=None, save_lse=True, eager=False):
     """Masked cross-entropy on given logits [N, V] (bf16 or fp32).
@@ -282,7 +299,9 @@ def ce_logits(logits, labels, *, ignore_index=-100, reduction="sum", num_label_t
     once for both, and keeps it until the backward scales it by the incoming
     gradient (no work when that is 1); with ``inplace_grad=True`` the logits
     are overwritten by their gradient already in the forward, and must then
-    be contiguous."""
+    be contiguous.  Leading dimensions are flattened: logits [..., V] with
+    labels (and mask) [...]."""
+    logits, labels, mask = _rows(logits, labels, mask, "logits")
     labels = _fold_mask(labels, mask, ignore_index)
     if eager:
         _cuda(logits, "logits")
@@ -524,7 +543,9 @@ def flce(H, W, labels, bias=None, *, ignore_index=-100, reduction="mean", num_la
     [N] int64.  Default: the backward recomputes the logits chunk by chunk
     (``chunk`` rows at a time; None picks the library default), 8NDV flops in
     all.  ``eager=True`` forms the gradients during the forward (6NDV flops)
-    and keeps them, fp32 grad_W included, until the backward scales them."""
+    and keeps them, fp32 grad_W included, until the backward scales them.
+    Leading dimensions are flattened: H [..., D] with labels (and mask) [...]."""
+    H, labels, mask = _rows(H, labels, mask, "H")
     labels = _fold_mask(labels, mask, ignore_index)
     fn = _FLCEEager if eager else _FLCE
     return fn.apply(H, W, labels, bias, int(ignore_index), reduction, num_label_tokens, chunk)

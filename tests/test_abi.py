@@ -175,3 +175,17 @@ def test_product_path_has_no_fallback():
     out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True)
     assert "raised" in out.stdout
     ctypes  # noqa: B018  (ctypes import kept for symbol lookups above)
+
+
+def test_front_ends_check_leading_shapes():
+    # shape checks of the autograd front ends happen on the host, before any launch
+    import torch
+    import lm_head_linear_fwd_gb300 as lh
+    x = torch.zeros(2, 3, 10)
+    with pytest.raises(ValueError):
+        lh.ce_logits(x, torch.zeros(6, dtype=torch.int64))
+    with pytest.raises(ValueError):
+        lh.ce_logits(torch.zeros(10), torch.zeros(1, dtype=torch.int64))
+    with pytest.raises(ValueError):
+        lh.flce(x, torch.zeros(10, 10), torch.zeros(2, 3, dtype=torch.int64),
+                mask=torch.ones(6))

@@ -162,3 +162,26 @@ def test_ce_one_valid_row(lh, reduction):
         _grad_ok(grad, oracle.ce_backward(p.logits, y, -100, reduction), "dlogits")
         gc = grad.float().cpu()
         assert torch.count_nonzero(torch.cat([gc[:3], gc[4:]])) == 0
+
+
+def test_leading_dimensions_are_rows(lh):
+    # logits [B, T, V] / H [B, T, D] with labels [B, T]: the same results as the
+    # flattened call, and gradients in the input's shape
+    c = wl.random_ce(2 * 48, 3000, torch.bfloat16, seed=71)
+    x2 = c.logits.cuda().requires_grad_(True)
+    l2 = lh.ce_logits(x2, c.labels.cuda(), reduction="mean")
+    l2.backward()
+    x3 = c.logits.cuda().reshape(2, 48, 3000).requires_grad_(True)
+    l3 = lh.ce_logits(x3, c.labels.cuda().reshape(2, 48), reduction="mean")
+    l3.backward()
+    assert torch.equal(l2, l3) and x3.grad.shape == (2, 48, 3000)
+    assert torch.equal(x3.grad.reshape(96, 3000), x2.grad)
+    p = wl.random_flce(2 * 128, 128, 2000, torch.bfloat16, seed=72)
+    H2 = p.H.cuda().requires_grad_(True)
+    W2 = p.W.cuda().requires_grad_(True)
+    lh.flce(H2, W2, p.labels.cuda(), reduction="sum").backward()
+    H3 = p.H.cuda().reshape(2, 128, 128).requires_grad_(True)
+    W3 = p.W.cuda().requires_grad_(True)
+    lh.flce(H3, W3, p.labels.cuda().reshape(2, 128), reduction="sum").backward()
+    assert H3.grad.shape == (2, 128, 128)
+    assert torch.equal(H3.grad.reshape(256, 128), H2.grad) and torch.equal(W3.grad, W2.grad)
