@@ -12,14 +12,17 @@
 // (in place) or into a separate buffer.  Without a saved lse (the page's
 // memory bullet: nothing but the inputs is kept) the lse is formed again in
 // the backward, still with one read of the logits where the row fits a
-// thread-block cluster's shared memory.
+// thread-block cluster's shared memory.  When the incoming gradient is known
+// in advance, the forward and the backward run as one such pass (the
+// eager-gradient scheme of Liger-Kernel issue #533, applied to given logits).
 //
 // Three kernel families, chosen per call:
 // * ce_stream_kernel: rows whose start and length are 16-byte multiples
 //   stream through a cp.async.bulk shared-memory ring (forward; backward with
 //   a saved lse; backward without one for rows over 512 KiB, read twice);
 // * ce_bwd_resident_kernel: backward without a saved lse, a row held by a
-//   cluster of 1-8 CTAs;
+//   cluster of 1-8 CTAs; in its fused mode also the forward's per-row loss
+//   and lse (ce_logits_fwd_bwd: forward and backward with one read);
 // * ce_fwd_rows_kernel / ce_bwd_rows_kernel: any other rows, 16-byte register
 //   loads with a scalar head and tail.
 // All keep the online maximum and sum in the base-2 domain (one MUFU ex2 per
@@ -682,7 +685,10 @@ static int launch_stream(const StreamArgs& a, cudaStream_t s) {
 // cluster hold the same lse) and writes its slice of dZ from shared memory.
 // The logits are read from HBM once, as when the lse is saved.  Rows with a
 // zero gradient (ignored labels, or a zero coefficient) are written as zeros
-// without being read.
+// without being read.  The fused mode (forward and backward in one call)
+// also writes each row's loss, from the CTA whose slice holds the label's
+// logit, and its lse; it reads every row with a valid label, also when the
+// coefficient is zero, since the loss still needs the row.
 //
 // Measured alternatives on GB300 ([16384, 128256] bf16): two slice buffers
 // per CTA (the next row copied in, or a row pipeline that lets the CTAs of a
