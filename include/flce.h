@@ -260,7 +260,10 @@ FLCE_API int64_t flce_default_chunk(int dt, int64_t N, int64_t D, int64_t V);
  * H and W must be 16-byte aligned and D * sizeof(dt) a multiple of 16.
  * Outputs as in ce_logits_fwd (loss, n_valid, lse, optional loss_rows and
  * label_logit, the latter the fp32 GEMM value of z_{i,y_i}).
- * Requires 1 <= N, 1 <= V < 2^31, 8 <= D. */
+ * Requires 0 <= N, 1 <= V < 2^31, 8 <= D.  N == 0 (an empty batch; H,
+ * labels, lse and ws may then be NULL) gives loss 0 and n_valid 0, and the
+ * backward calls (flce_bwd, flce_fwd_bwd and the shard steps) then write a
+ * zero grad_W (left as it is when accumulating) and a zero grad_bias. */
 FLCE_API int flce_fwd(const void* H, const void* W, const void* bias, int dt, int64_t N, int64_t D,
              int64_t V, const int64_t* labels, int64_t ignore_index, int reduction,
              int64_t num_label_tokens, float* loss, int64_t* n_valid, float* lse,

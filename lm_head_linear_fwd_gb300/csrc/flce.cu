@@ -638,6 +638,29 @@ __global__ void __launch_bounds__(256) scale_kernel(T* x, int64_t n, const float
     Elem<T>::store(x + i, Elem<T>::load(x + i) * s);
 }
 
+// x[0..n) = 0: the weight and bias gradients of an empty batch.
+__global__ void __launch_bounds__(256) zero_kernel(float* x, int64_t n) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    x[i] = 0.0f;
+}
+
+static int launch_zero(float* x, int64_t n, cudaStream_t s) {
+  if (x == nullptr || n == 0) return FLCE_OK;
+  const int grid = static_cast<int>(std::min<int64_t>((n + 255) / 256, sm_count() * 8));
+  zero_kernel<<<grid, 256, 0, s>>>(x, n);
+  return launch_status("zero_kernel launch");
+}
+
+// Backward of an empty batch (N = 0): the loss has no terms, so grad_W (unless
+// accumulated) and grad_bias are zero; grad_H has no rows.
+static int empty_bwd(int64_t D, int64_t V, float* grad_W, int accumulate_grad_W,
+                     float* grad_bias, cudaStream_t s) {
+  int rc = accumulate_grad_W ? FLCE_OK : launch_zero(grad_W, V * D, s);
+  if (rc != FLCE_OK) return rc;
+  return launch_zero(grad_bias, V, s);
+}
+
 // out[r, d] = sum over s of part[s * split_stride + r * D + d], in split order
 // (deterministic), converted to OutT.  Closes a split-K contraction.
 template <typename OutT>
@@ -1030,10 +1053,11 @@ static int flce_checks(const void* H, const void* W, int dt, int64_t N, int64_t 
                        const int64_t* labels, int reduction) {
   if (!valid_dtype(dt)) return FLCE_EDTYPE;
   if (!valid_reduction(reduction)) return FLCE_EINVAL;
-  if (N < 1 || D < 8 || V < 1 || V >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) ||
+  if (N < 0 || D < 8 || V < 1 || V >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) ||
       D >= (int64_t(1) << 31))
     return FLCE_ESHAPE;
-  if (H == nullptr || W == nullptr || labels == nullptr) return FLCE_EINVAL;
+  // N == 0 (an empty batch) is valid; H and labels may then be null
+  if (W == nullptr || (N > 0 && (H == nullptr || labels == nullptr))) return FLCE_EINVAL;
   if (!aligned(H, 16) || !aligned(W, 16) || (D * static_cast<int64_t>(dtype_size(dt))) % 16 != 0)
     return FLCE_EALIGN;
   if (!aligned(labels, 8)) return FLCE_EALIGN;
@@ -1089,9 +1113,13 @@ extern "C" int flce_fwd(const void* H, const void* W, const void* bias, int dt, 
                         size_t ws_bytes, int32_t* status, flce_stream_t stream) {
   int rc = flce_checks(H, W, dt, N, D, V, labels, reduction);
   if (rc != FLCE_OK) return rc;
-  if (loss == nullptr || n_valid == nullptr || lse == nullptr || status == nullptr)
+  if (loss == nullptr || n_valid == nullptr || status == nullptr || (N > 0 && lse == nullptr))
     return FLCE_EINVAL;
   if (bias != nullptr && !aligned(bias, dtype_size(dt))) return FLCE_EALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (N == 0)  // loss 0, n_valid 0
+    return launch_finalize(nullptr, labels, 0, V, ignore_index, reduction, num_label_tokens,
+                           loss, n_valid, s);
   const FlcePlan p = plan(dt, N, D, V, 0);
   if (ws == nullptr || ws_bytes < p.fwd_bytes) return FLCE_EWORKSPACE;
   if (!aligned(ws, 256)) return FLCE_EALIGN;
@@ -1099,7 +1127,6 @@ extern "C" int flce_fwd(const void* H, const void* W, const void* bias, int dt, 
   if (rc != FLCE_OK) return rc;
   char* w = static_cast<char*>(ws);
   float* rows = loss_rows != nullptr ? loss_rows : reinterpret_cast<float*>(w + p.off_rows);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   rc = fwd_gemm(H, W, bias, dt, N, D, V, 0, labels, ignore_index, p, w, status, s);
   if (rc != FLCE_OK) return rc;
   lse_combine_kernel<<<static_cast<unsigned>((N + kCombineRows - 1) / kCombineRows),
@@ -1122,9 +1149,11 @@ extern "C" int flce_fwd_shard(const void* H, const void* W_shard, const void* bi
   if (rc != FLCE_OK) return rc;
   if (vocab_offset < 0 || V_total < vocab_offset + V_shard || V_total >= (int64_t(1) << 31))
     return FLCE_ESHAPE;
-  if (m_local == nullptr || s_local == nullptr || zy_local == nullptr || status == nullptr)
+  if (status == nullptr ||
+      (N > 0 && (m_local == nullptr || s_local == nullptr || zy_local == nullptr)))
     return FLCE_EINVAL;
   if (bias_shard != nullptr && !aligned(bias_shard, dtype_size(dt))) return FLCE_EALIGN;
+  if (N == 0) return FLCE_OK;  // no rows, no partials
   const FlcePlan p = plan(dt, N, D, V_shard, 0);
   if (ws == nullptr || ws_bytes < p.fwd_bytes) return FLCE_EWORKSPACE;
   if (!aligned(ws, 256)) return FLCE_EALIGN;
@@ -1163,10 +1192,14 @@ extern "C" int flce_shard_finish(const float* m_global, const float* s_global,
                                  float* loss, int64_t* n_valid, void* ws, size_t ws_bytes,
                                  int32_t* status, flce_stream_t stream) {
   if (!valid_reduction(reduction)) return FLCE_EINVAL;
-  if (N < 1 || V_total < 1 || V_total >= (int64_t(1) << 31)) return FLCE_ESHAPE;
-  if (m_global == nullptr || s_global == nullptr || zy_global == nullptr || labels == nullptr ||
-      lse == nullptr || loss == nullptr || n_valid == nullptr || status == nullptr)
+  if (N < 0 || V_total < 1 || V_total >= (int64_t(1) << 31)) return FLCE_ESHAPE;
+  if (loss == nullptr || n_valid == nullptr || status == nullptr ||
+      (N > 0 && (m_global == nullptr || s_global == nullptr || zy_global == nullptr ||
+                 labels == nullptr || lse == nullptr)))
     return FLCE_EINVAL;
+  if (N == 0)  // loss 0, n_valid 0
+    return launch_finalize(nullptr, labels, 0, V_total, ignore_index, reduction,
+                           num_label_tokens, loss, n_valid, reinterpret_cast<cudaStream_t>(stream));
   float* rows = loss_rows;
   if (rows == nullptr) {
     if (ws == nullptr || ws_bytes < round_up(static_cast<size_t>(N) * 4, 256))
@@ -1389,7 +1422,8 @@ static int flce_bwd_entry(const void* H, const void* W, const void* bias, int dt
   int rc = flce_checks(H, W, dt, N, D, V, labels, reduction);
   if (rc != FLCE_OK) return rc;
   if (v0 < 0 || V_total < v0 + V || V_total >= (int64_t(1) << 31)) return FLCE_ESHAPE;
-  if (lse == nullptr || n_valid == nullptr || grad_loss == nullptr || status == nullptr)
+  if (n_valid == nullptr || grad_loss == nullptr || status == nullptr ||
+      (N > 0 && lse == nullptr))
     return FLCE_EINVAL;
   if (accumulate_grad_W != 0 && accumulate_grad_W != 1) return FLCE_EINVAL;
   if (chunk > 0 && chunk % kBM != 0 && chunk < N) return FLCE_ESHAPE;
@@ -1397,6 +1431,9 @@ static int flce_bwd_entry(const void* H, const void* W, const void* bias, int dt
   if (grad_H != nullptr && !aligned(grad_H, 16)) return FLCE_EALIGN;
   if (grad_W != nullptr && !aligned(grad_W, 16)) return FLCE_EALIGN;
   if (grad_bias != nullptr && !aligned(grad_bias, 4)) return FLCE_EALIGN;
+  if (N == 0)
+    return empty_bwd(D, V, grad_W, accumulate_grad_W, grad_bias,
+                     reinterpret_cast<cudaStream_t>(stream));
   const FlcePlan p = plan(dt, N, D, V, chunk);
   if (ws == nullptr || ws_bytes < p.bwd_bytes) return FLCE_EWORKSPACE;
   if (!aligned(ws, 256)) return FLCE_EALIGN;
@@ -1455,7 +1492,7 @@ extern "C" int flce_fwd_bwd(const void* H, const void* W, const void* bias, int 
                             flce_stream_t stream) {
   int rc = flce_checks(H, W, dt, N, D, V, labels, reduction);
   if (rc != FLCE_OK) return rc;
-  if (loss == nullptr || n_valid == nullptr || lse == nullptr || status == nullptr)
+  if (loss == nullptr || n_valid == nullptr || status == nullptr || (N > 0 && lse == nullptr))
     return FLCE_EINVAL;
   if (accumulate_grad_W != 0 && accumulate_grad_W != 1) return FLCE_EINVAL;
   if (chunk > 0 && chunk % kBM != 0 && chunk < N) return FLCE_ESHAPE;
@@ -1463,6 +1500,13 @@ extern "C" int flce_fwd_bwd(const void* H, const void* W, const void* bias, int 
   if (grad_H != nullptr && !aligned(grad_H, 16)) return FLCE_EALIGN;
   if (grad_W != nullptr && !aligned(grad_W, 16)) return FLCE_EALIGN;
   if (grad_bias != nullptr && !aligned(grad_bias, 4)) return FLCE_EALIGN;
+  if (N == 0) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    rc = launch_finalize(nullptr, labels, 0, V, ignore_index, reduction, num_label_tokens, loss,
+                         n_valid, s);
+    if (rc != FLCE_OK) return rc;
+    return empty_bwd(D, V, grad_W, accumulate_grad_W, grad_bias, s);
+  }
   const FlcePlan p = plan(dt, N, D, V, chunk);
   if (p.nparts > kMaxTilesPerRow) return FLCE_ESHAPE;
   if (ws == nullptr || ws_bytes < p.fused_bytes) return FLCE_EWORKSPACE;

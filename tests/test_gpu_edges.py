@@ -185,3 +185,37 @@ def test_leading_dimensions_are_rows(lh):
     lh.flce(H3, W3, p.labels.cuda().reshape(2, 128), reduction="sum").backward()
     assert H3.grad.shape == (2, 128, 128)
     assert torch.equal(H3.grad.reshape(256, 128), H2.grad) and torch.equal(W3.grad, W2.grad)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_flce_empty_batch(lh, dtype):
+    # N = 0: loss 0, n_valid 0, no grad_H rows, grad_W and grad_bias zero
+    # (grad_W left as it is when accumulating); every call path
+    V, D = 1000, 128
+    W = torch.randn(V, D, device="cuda").to(dtype)
+    b = torch.randn(V, device="cuda").to(dtype)
+    H = torch.empty(0, D, dtype=dtype, device="cuda")
+    y = torch.empty(0, dtype=torch.int64, device="cuda")
+    out = lh.flce_fwd(H, W, y, b, -100, "mean")
+    gW = torch.full((V, D), float("nan"), device="cuda")
+    gb = torch.full((V,), float("nan"), device="cuda")
+    bw = lh.flce_bwd(H, W, y, out.lse, out.n_valid, torch.ones(1, device="cuda"), b, -100,
+                     "mean", grad_W=gW, grad_bias=gb)
+    acc = torch.ones(V, D, device="cuda")
+    lh.flce_bwd(H, W, y, out.lse, out.n_valid, torch.ones(1, device="cuda"), b, -100, "mean",
+                want_grad_H=False, want_grad_bias=False, grad_W=acc, accumulate_grad_W=True)
+    fo, fr = lh.flce_fwd_bwd(H, W, y, b, -100, "sum")
+    torch.cuda.synchronize()
+    lh.check_status(out.status)
+    assert out.loss.item() == 0.0 and out.n_valid.item() == 0
+    assert bw.grad_H.shape == (0, D)
+    assert torch.count_nonzero(gW) == 0 and torch.count_nonzero(gb) == 0
+    assert torch.all(acc == 1.0)
+    assert fo.loss.item() == 0.0 and fo.n_valid.item() == 0
+    assert torch.count_nonzero(fr.grad_W) == 0 and torch.count_nonzero(fr.grad_bias) == 0
+    Hr = H.clone().requires_grad_(True)
+    Wr = W.clone().requires_grad_(True)
+    loss = lh.flce(Hr, Wr, y, reduction="sum")
+    loss.backward()
+    assert loss.item() == 0.0 and Hr.grad.shape == (0, D)
+    assert torch.count_nonzero(Wr.grad) == 0
