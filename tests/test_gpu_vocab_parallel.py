@@ -98,3 +98,32 @@ def test_ce_on_logit_shards_matches_the_oracle(bounds, inplace):
     _grad_ok(dz, oracle.ce_backward(c.logits, c.labels, -100, "mean", grad_loss=0.5), "dZ")
     if inplace:
         assert torch.equal(work, dz)
+
+
+def test_empty_batch_on_shards():
+    # a rank with no tokens: every shard step accepts N = 0; the loss is 0 and
+    # the shards' weight and bias gradients are zero
+    import lm_head_linear_fwd_gb300 as lh
+    from lm_head_linear_fwd_gb300 import vocab_parallel as vp
+    V, D = 3001, 128
+    W = torch.randn(V, D, device="cuda").to(torch.bfloat16)
+    b = torch.randn(V, device="cuda").to(torch.bfloat16)
+    H = torch.empty(0, D, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(0, dtype=torch.int64, device="cuda")
+    bounds = [(0, 1024), (1024, V)]
+    ops = vp.CudaShardOps()
+    st = lh.new_status("cuda")
+    parts = [ops.partials(H, W[a:c], y, a, V, b[a:c], -100, st) for a, c in bounds]
+    m_g = torch.stack([q[0] for q in parts]).amax(0)
+    s_g = torch.stack([ops.rescale(q[0], q[1], m_g) for q in parts]).sum(0)
+    zy_g = torch.stack([q[2] for q in parts]).sum(0)
+    lse, loss, n_valid = ops.finish(m_g, s_g, zy_g, y, V, -100, "mean", None, st)
+    grads = [ops.backward(H, W[a:c], y, a, V, b[a:c], -100, "mean", None, lse, n_valid,
+                          torch.ones(1, device="cuda"), None, True, True, st)
+             for a, c in bounds]
+    torch.cuda.synchronize()
+    lh.check_status(st)
+    assert loss.item() == 0.0 and n_valid.item() == 0 and lse.numel() == 0
+    for gH, gW, gb in grads:
+        assert gH.shape == (0, D)
+        assert torch.count_nonzero(gW) == 0 and torch.count_nonzero(gb) == 0
