@@ -1405,7 +1405,7 @@ extern "C" int ce_logits_bwd_shard(const void* logits_shard, int dt, int64_t N, 
 extern "C" size_t ce_logits_fwd_bwd_workspace_bytes(int64_t N, int64_t V) {
   if (N < 0 || V < 1) return 0;
   // per-row losses and, for the two-call fallback, a per-row lse
-  return 2 * round_up(static_cast<size_t>(N) * 4, 256) + ce_logits_workspace_bytes(N, V);
+  return 2 * round_up(static_cast<size_t>(N) * 4, 256);
 }
 
 extern "C" int ce_logits_fwd_bwd(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
@@ -1428,10 +1428,6 @@ extern "C" int ce_logits_fwd_bwd(const void* logits, int dt, int64_t N, int64_t 
   char* w = static_cast<char*>(ws);
   float* rows = reinterpret_cast<float*>(w);
   float* lse_buf = reinterpret_cast<float*>(w + round_up(static_cast<size_t>(N) * 4, 256));
-  char* fwd_ws = w + 2 * round_up(static_cast<size_t>(N) * 4, 256);
-  const size_t fwd_ws_bytes = ws_bytes > 2 * round_up(static_cast<size_t>(N) * 4, 256)
-                                  ? ws_bytes - 2 * round_up(static_cast<size_t>(N) * 4, 256)
-                                  : 0;
   const size_t es = dtype_size(dt);
   if (N > 0 && streamable(logits, ld, V, es) && streamable(grad_logits, ld_grad, V, es)) {
     // one pass: the count of valid rows first (the mean's divisor), then each
@@ -1462,8 +1458,9 @@ extern "C" int ce_logits_fwd_bwd(const void* logits, int dt, int64_t N, int64_t 
   }
   // rows that no cluster holds: the forward, then the backward
   float* l = lse != nullptr ? lse : lse_buf;
+  // (the per-row losses go to the workspace: ce_logits_fwd needs none of its own)
   rc = ce_logits_fwd(logits, dt, N, V, ld, labels, ignore_index, reduction, num_label_tokens, loss,
-                     n_valid, l, rows, nullptr, fwd_ws, fwd_ws_bytes, status, stream);
+                     n_valid, l, rows, nullptr, nullptr, 0, status, stream);
   if (rc != FLCE_OK || N == 0) return rc;
   return ce_bwd_entry(logits, dt, N, V, ld, 0, V, labels, ignore_index, reduction,
                       num_label_tokens, l, n_valid, grad_loss, inplace_grad, grad_logits,
