@@ -718,10 +718,40 @@ def latency_configs(dev, stream, steps):
 
 # ------------------------------------------------------------- oracle timing
 
+def blas_info():
+    """Name and thread count of the BLAS numpy (and so the oracle) runs on."""
+    import ctypes
+    import glob
+    import numpy as np
+    name = None
+    try:
+        name = np.show_config(mode="dicts")["Build Dependencies"]["blas"]["name"]
+    except Exception:
+        pass
+    try:
+        import threadpoolctl
+        for d in threadpoolctl.threadpool_info():
+            if d.get("user_api") == "blas":
+                return {"name": d.get("internal_api") or name, "threads": d.get("num_threads")}
+    except ImportError:
+        pass
+    libdir = os.path.join(os.path.dirname(np.__file__), os.pardir, "numpy.libs")
+    for path in glob.glob(os.path.join(libdir, "*openblas*.so*")):
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for sym in ("scipy_openblas_get_num_threads64_", "scipy_openblas_get_num_threads",
+                    "openblas_get_num_threads64_", "openblas_get_num_threads"):
+            f = getattr(lib, sym, None)
+            if f is not None:
+                return {"name": name, "threads": int(f())}
+    return {"name": name, "threads": None}
+
+
 def cpu_baseline(args, rows=None, workload=None):
     """The fp64 oracle (as it stands) on a bounded row sample of the FLCE workload."""
     import numpy as np
-    import torch
 
     import oracle
     import workloads as wl
@@ -737,8 +767,10 @@ def cpu_baseline(args, rows=None, workload=None):
     oracle.flce_backward(p.H, p.W, p.bias, p.labels, p.ignore_index, p.reduction,
                          p.num_label_tokens, rows=sel)
     dt = time.perf_counter() - t0
-    return {"value": round(rows / dt, 3), "unit": "tokens/s", "cores": os.cpu_count(),
-            "threads": torch.get_num_threads(), "kind": "oracle",
+    blas = blas_info()
+    return {"value": round(rows / dt, 3), "unit": "tokens/s",
+            "cores": blas["threads"] or os.cpu_count(), "host_cores": os.cpu_count(),
+            "blas": blas, "kind": "oracle",
             "sample": f"{rows} sampled rows of {wname} (N={p.N}, D={p.D}, V={p.V}), fwd+bwd in "
                       f"fp64 numpy, {dt:.2f} s"}
 
@@ -747,7 +779,6 @@ def run_reference(args, rank, ws):
     if rank != 0:
         return
     import numpy as np
-    import torch
 
     import oracle
     import workloads as wl
@@ -766,6 +797,7 @@ def run_reference(args, rank, ws):
             times.append(time.perf_counter() - t0)
     per = sum(times) / len(times)
     v = rows / per
+    blas = blas_info()
     line = {
         "impl": "reference",
         "metric": METRIC,
@@ -783,8 +815,9 @@ def run_reference(args, rank, ws):
         "config": {"workload": f"FLCE fwd+bwd {args.workload}: N={p.N} D={p.D} V={p.V}; each "
                                f"step a {rows}-row sample",
                    "global_batch": rows, "parallelism": "host cores"},
-        "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "cores": os.cpu_count(),
-                         "threads": torch.get_num_threads(), "kind": "oracle",
+        "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s",
+                         "cores": blas["threads"] or os.cpu_count(), "host_cores": os.cpu_count(),
+                         "blas": blas, "kind": "oracle",
                          "sample": f"{rows} rows per step of {args.workload}"},
         "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
