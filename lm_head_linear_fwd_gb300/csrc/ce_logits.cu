@@ -17,14 +17,18 @@
 // eager-gradient scheme of Liger-Kernel issue #533, applied to given logits).
 //
 // Three kernel families, chosen per call:
-// * ce_stream_kernel: rows whose start and length are 16-byte multiples
-//   stream through a cp.async.bulk shared-memory ring (forward; backward with
-//   a saved lse; backward without one for rows over 512 KiB, read twice);
+// * ce_stream_kernel: rows stream through a cp.async.bulk shared-memory ring
+//   as whole 16-byte blocks (a row that starts or ends inside a block has its
+//   first and last block finished element by element): the forward; the
+//   backward with a saved lse; the backward without one for rows over
+//   512 KiB, read twice;
 // * ce_bwd_resident_kernel: backward without a saved lse, a row held by a
 //   cluster of 1-8 CTAs; in its fused mode also the forward's per-row loss
 //   and lse (ce_logits_fwd_bwd: forward and backward with one read);
-// * ce_fwd_rows_kernel / ce_bwd_rows_kernel: any other rows, 16-byte register
-//   loads with a scalar head and tail.
+// * ce_bwd_rows_kernel: a backward whose gradient rows start at other offsets
+//   within a 16-byte block than the logits rows (separate buffers whose
+//   starts or row strides differ modulo 16 bytes): 16-byte register loads
+//   with a scalar head and tail.
 // All keep the online maximum and sum in the base-2 domain (one MUFU ex2 per
 // element) and merge per-thread states with warp shuffles in a fixed order.
 #include <math.h>
@@ -66,7 +70,7 @@ struct ShardOut {
   }
 };
 
-// ---------------------------------------------------------------- forward kernel
+// ------------------------------------------------------------ row reduction
 
 // Base-2 log-sum-exp state of one row p[0..V) over the block: every thread
 // reduces a strided share (16-byte vector loads; a scalar head and tail when
@@ -127,39 +131,6 @@ __device__ Lse2 block_row_lse2(const T* p, int64_t V, float* red_m, float* red_s
   for (int w = 0; w < NW; ++w) all.merge(red_m[w], red_s[w]);
   __syncthreads();
   return all;
-}
-
-template <typename T, int THREADS>
-__global__ void __launch_bounds__(THREADS) ce_fwd_rows_kernel(
-    const T* __restrict__ logits, int64_t N, int64_t V, int64_t ld,
-    const int64_t* __restrict__ labels, int64_t ignore_index, float* __restrict__ lse_out,
-    float* __restrict__ loss_rows, float* __restrict__ label_logit, int32_t* status,
-    ShardOut sh) {
-  __shared__ float red_m[THREADS / 32], red_s[THREADS / 32];
-  for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
-    const T* p = logits + row * ld;
-    const Lse2 all = block_row_lse2<T, THREADS>(p, V, red_m, red_s);
-    if (threadIdx.x == 0) {
-      const int64_t y = labels[row];
-      if (sh.m_out != nullptr) {
-        sh.write(row, all.m, all.s, y, ignore_index, V, p, status);
-      } else {
-        const float lse = all.m * kLn2 + logf(all.s);
-        lse_out[row] = lse;
-        float li = 0.0f, zy = NAN;
-        if (y != ignore_index) {
-          if (label_ok(y, V)) {
-            zy = Elem<T>::load(p + y);
-            li = lse - zy;
-          } else {
-            set_status(status, FLCE_ELABEL);
-          }
-        }
-        loss_rows[row] = li;
-        if (label_logit != nullptr) label_logit[row] = zy;
-      }
-    }
-  }
 }
 
 // ------------------------------------------------------------- finalize kernel
@@ -294,9 +265,8 @@ __global__ void __launch_bounds__(THREADS) ce_bwd_rows_kernel(
 
 // ------------------------------------------------ bulk-copy (TMA) row streaming
 
-// Rows whose start and length are 16-byte multiples are streamed through a
-// shared-memory ring instead: one producer thread copies 32 KB row segments
-// with cp.async.bulk (a 2-stage mbarrier ring, so up to 64 KB per CTA is in
+// Rows are streamed through a shared-memory ring: one producer thread copies
+// 32 KB segments of a row's 16-byte blocks with cp.async.bulk (a 2-stage mbarrier ring, so up to 64 KB per CTA is in
 // flight without holding registers; 3 CTAs per SM), and 8 consumer warps
 // reduce (forward) or transform and store (backward) each segment from shared
 // memory.  The segment size, stage count and CTAs per SM were chosen by a
@@ -454,6 +424,101 @@ __device__ __forceinline__ void dz_from_smem(const uint4* sv, int first, int nve
   }
 }
 
+// A row as the bulk copies see it: the 16-byte blocks that hold any of its
+// elements.  A row need not start on a 16-byte boundary (an odd vocabulary, a
+// row stride that is not a multiple of 16 bytes, a column slice): its first
+// block then starts `head` elements before the row, and its last block may end
+// after it.  Those outside elements belong to a neighbouring row (or lie just
+// outside the tensor); they are copied, never used and never written.  A
+// 16-byte block never straddles a page, so a block that holds one byte of the
+// row is mapped memory as a whole.
+struct RowSpan {
+  const char* a0;  // the first block
+  int head;        // elements of the first block before the row (0: aligned)
+  int64_t nvec;    // blocks
+};
+
+template <typename T>
+__device__ __forceinline__ RowSpan row_span(const void* base, int64_t row, int64_t ld, int64_t V) {
+  const uintptr_t rs = reinterpret_cast<uintptr_t>(static_cast<const T*>(base) + row * ld);
+  const uintptr_t a0 = rs & ~static_cast<uintptr_t>(15);
+  const uintptr_t a1 = (rs + static_cast<uintptr_t>(V) * sizeof(T) + 15) &
+                       ~static_cast<uintptr_t>(15);
+  RowSpan sp;
+  sp.a0 = reinterpret_cast<const char*>(a0);
+  sp.head = static_cast<int>((rs - a0) / sizeof(T));
+  sp.nvec = static_cast<int64_t>((a1 - a0) / 16);
+  return sp;
+}
+
+// Elements [lo, hi) of one 16-byte block (a row's first or last block, the
+// rest belonging to other rows) added to a base-2 log-sum-exp state.
+template <typename T>
+__device__ __forceinline__ void lse_add_part(const uint4& v, int lo, int hi, Lse2& st) {
+  float x[Elem<T>::kPerVec];
+  Elem<T>::unpack(v, x);
+#pragma unroll
+  for (int e = 0; e < Elem<T>::kPerVec; ++e) {  // unrolled: x stays in registers
+    const float t = x[e] * kLog2e;
+    if (e >= lo && e < hi && t != -INFINITY) st.add1(t);
+  }
+}
+
+// dZ of elements [lo, hi) of one 16-byte block, stored one by one to
+// out[lo..hi) (the block's other elements belong to other rows); e_y: the
+// label's position in the block, or -1.  The same arithmetic as dz_from_smem.
+template <typename T>
+__device__ __forceinline__ void dz_part(const uint4& v, int lo, int hi, int e_y,
+                                        const DzRow<T>& r, T* out) {
+  if (r.c == 0.0f) {  // a zero gradient: the block is not read
+    for (int e = lo; e < hi; ++e) Elem<T>::store(out + e, 0.0f);
+    return;
+  }
+  float x[Elem<T>::kPerVec];
+  Elem<T>::unpack(v, x);
+#pragma unroll
+  for (int e = 0; e < Elem<T>::kPerVec; ++e) {
+    if (e < lo || e >= hi) continue;
+    float d = ex2(__fmaf_rn(x[e], kLog2e, -r.l2c));
+    if (r.neg) d = -d;
+    if (e == e_y) d -= r.c;
+    Elem<T>::store(out + e, d);
+  }
+}
+
+// The blocks [0, nvec) of a piece of a row that starts at row element e0
+// (negative in the first piece of a row with a head): the first and the last
+// block may hold elements outside [0, V).  Whole blocks are [vb, ve).
+struct PieceEdges {
+  int vb, ve;
+  bool head_part, tail_part;
+  __device__ PieceEdges(int64_t e0, int nvec, int64_t V, int epv) {
+    head_part = nvec > 0 && e0 < 0;
+    tail_part = nvec > 0 && e0 + static_cast<int64_t>(nvec) * epv > V;
+    vb = head_part ? 1 : 0;
+    ve = tail_part ? nvec - 1 : nvec;
+    if (ve < vb) ve = vb;
+  }
+  __device__ PieceEdges() {}
+  // a piece of whole blocks only
+  __device__ static PieceEdges whole(int nvec) {
+    PieceEdges p;
+    p.vb = 0;
+    p.ve = nvec;
+    p.head_part = p.tail_part = false;
+    return p;
+  }
+};
+
+// The valid element range [lo, hi) of block v of a piece starting at row
+// element e0.
+__device__ __forceinline__ void block_range(int64_t e0, int v, int64_t V, int epv, int& lo,
+                                            int& hi) {
+  const int64_t eb = e0 + static_cast<int64_t>(v) * epv;
+  lo = eb < 0 ? static_cast<int>(-eb) : 0;
+  hi = eb + epv > V ? static_cast<int>(V - eb) : epv;
+}
+
 struct StreamArgs {
   const void* logits;
   int64_t N, V, ld;
@@ -479,7 +544,9 @@ struct StreamArgs {
 };
 
 // kTwoPass (backward only): no saved lse, each row is streamed twice.
-template <typename T, bool kBwd, bool kTwoPass = false>
+// kWhole: every row starts and ends on a 16-byte boundary (the partial-block
+// handling is compiled out).
+template <typename T, bool kBwd, bool kTwoPass, bool kWhole>
 __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm)
     ce_stream_kernel(const StreamArgs a) {
   constexpr int kVecPerSeg = kSegBytes / 16;
@@ -502,9 +569,16 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm)
     fence_barrier_init();
   }
   __syncthreads();
-  const int64_t row_bytes = a.V * static_cast<int64_t>(sizeof(T));
-  const int nseg = static_cast<int>((row_bytes + kSegBytes - 1) / kSegBytes);
+  constexpr int EPV = Elem<T>::kPerVec;
   const int seg_elems = kSegBytes / static_cast<int>(sizeof(T));
+  auto span = [&](int64_t row) -> RowSpan {
+    if (!kWhole) return row_span<T>(a.logits, row, a.ld, a.V);
+    RowSpan sp;
+    sp.a0 = reinterpret_cast<const char*>(static_cast<const T*>(a.logits) + row * a.ld);
+    sp.head = 0;
+    sp.nvec = a.V * static_cast<int64_t>(sizeof(T)) / 16;
+    return sp;
+  };
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------- producer
@@ -514,8 +588,9 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm)
       bool ok = true;
       constexpr int npass = (kBwd && kTwoPass) ? 2 : 1;
       for (int64_t row = blockIdx.x; row < a.N && ok; row += gridDim.x) {
-        const char* src = reinterpret_cast<const char*>(static_cast<const T*>(a.logits) +
-                                                        row * a.ld);
+        const RowSpan sp = span(row);
+        const int64_t cb = sp.nvec * 16;  // bytes copied: the row's blocks
+        const int nseg = static_cast<int>((cb + kSegBytes - 1) / kSegBytes);
         for (int it = 0; it < npass * nseg && ok; ++it) {
           const int sg = it % nseg;
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
@@ -523,14 +598,14 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm)
             break;
           }
           const uint32_t bytes = static_cast<uint32_t>(
-              min(static_cast<int64_t>(kSegBytes), row_bytes - static_cast<int64_t>(sg) * kSegBytes));
-          // checked builds: the segment lies inside its row and its stage; a
-          // failed check completes the stage without a copy
-          if (span_in_range(static_cast<int64_t>(sg) * kSegBytes, bytes, row_bytes, a.status) &&
+              min(static_cast<int64_t>(kSegBytes), cb - static_cast<int64_t>(sg) * kSegBytes));
+          // checked builds: the segment lies inside the row's blocks and its
+          // stage; a failed check completes the stage without a copy
+          if (span_in_range(static_cast<int64_t>(sg) * kSegBytes, bytes, cb, a.status) &&
               smem_in_range(stage * kSegBytes + 128, kSegBytes, a.status)) {
             mbar_arrive_expect_tx(&full_bar[stage], bytes);
-            bulk_load(ring + stage * kSegBytes, src + static_cast<int64_t>(sg) * kSegBytes, bytes,
-                      &full_bar[stage]);
+            bulk_load(ring + stage * kSegBytes, sp.a0 + static_cast<int64_t>(sg) * kSegBytes,
+                      bytes, &full_bar[stage]);
           } else {
             mbar_arrive(&full_bar[stage]);
           }
@@ -576,7 +651,14 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm)
       c = valid ? coef : 0.0f;
       if (!kTwoPass) lse2 = a.lse_in[row] * kLog2e;
     }
-    T* out = kBwd ? static_cast<T*>(a.grad) + row * a.ldg : nullptr;
+    const RowSpan sp = span(row);
+    const int64_t cb = sp.nvec * 16;
+    const int nseg = static_cast<int>((cb + kSegBytes - 1) / kSegBytes);
+    // the output row: same offset within its first block as the input row
+    T* out_row = kBwd ? static_cast<T*>(a.grad) + row * a.ldg : nullptr;
+    uint4* out_blk = kBwd ? reinterpret_cast<uint4*>(reinterpret_cast<uintptr_t>(out_row) &
+                                                     ~static_cast<uintptr_t>(15))
+                          : nullptr;
     for (int pass = 0; pass < npass; ++pass) {
       const bool reduce_pass = !kBwd || pass + 1 < npass;
       Lse2 st;
@@ -584,19 +666,47 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm)
         int ok = 1;
         if (lane == 0) ok = mbar_wait(&full_bar[stage], phase, abort_flag) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok) {
-          const int64_t e0 = static_cast<int64_t>(sg) * seg_elems;
-          const int nvec = static_cast<int>(
-              min(static_cast<int64_t>(kSegBytes), row_bytes - static_cast<int64_t>(sg) * kSegBytes) /
-              16);
+        const int nvec = static_cast<int>(
+            min(static_cast<int64_t>(kSegBytes), cb - static_cast<int64_t>(sg) * kSegBytes) / 16);
+        // checked builds: the segment's blocks lie inside the row's blocks
+        if (ok && span_in_range(static_cast<int64_t>(sg) * (kSegBytes / 16), nvec, sp.nvec,
+                                a.status)) {
           const uint4* sv = reinterpret_cast<const uint4*>(ring + stage * kSegBytes);
-          // checked builds: the segment's vectors lie inside the row
-          if (!span_in_range(e0, static_cast<int64_t>(nvec) * (16 / sizeof(T)), a.V, a.status)) {
-          } else if (reduce_pass)
-            lse_add_smem<T, kVecPerThread, kConsumers>(sv, tid, nvec, st);
-          else
-            dz_from_smem<T, kVecPerThread, kConsumers>(sv, tid, nvec, y - e0, DzRow<T>(lse2, c),
-                                                       reinterpret_cast<uint4*>(out + e0));
+          // row element of the segment's first block element
+          const int64_t e0 = static_cast<int64_t>(sg) * seg_elems - sp.head;
+          const PieceEdges pe = kWhole ? PieceEdges::whole(nvec) : PieceEdges(e0, nvec, a.V, EPV);
+          const bool one = pe.head_part && pe.tail_part && nvec == 1;
+          if (reduce_pass) {
+            lse_add_smem<T, kVecPerThread, kConsumers>(sv + pe.vb, tid, pe.ve - pe.vb, st);
+            int lo, hi;
+            if (pe.head_part && tid == 0) {
+              block_range(e0, 0, a.V, EPV, lo, hi);
+              lse_add_part<T>(sv[0], lo, hi, st);
+            }
+            if (pe.tail_part && !one && tid == kConsumers - 1) {
+              block_range(e0, nvec - 1, a.V, EPV, lo, hi);
+              lse_add_part<T>(sv[nvec - 1], lo, hi, st);
+            }
+          } else {
+            const DzRow<T> dr(lse2, c);
+            const int64_t yb = e0 + static_cast<int64_t>(pe.vb) * EPV;  // row element of sv[vb]
+            dz_from_smem<T, kVecPerThread, kConsumers>(
+                sv + pe.vb, tid, pe.ve - pe.vb, y >= 0 ? y - yb : -1, dr,
+                out_blk + static_cast<int64_t>(sg) * (kSegBytes / 16) + pe.vb);
+            int lo, hi;
+            if (pe.head_part && tid == 0) {
+              block_range(e0, 0, a.V, EPV, lo, hi);
+              dz_part<T>(sv[0], lo, hi, (y >= e0 && y < e0 + EPV) ? static_cast<int>(y - e0) : -1,
+                         dr, out_row + e0);
+            }
+            if (pe.tail_part && !one && tid == kConsumers - 1) {
+              const int64_t el = e0 + static_cast<int64_t>(nvec - 1) * EPV;
+              block_range(e0, nvec - 1, a.V, EPV, lo, hi);
+              dz_part<T>(sv[nvec - 1], lo, hi,
+                         (y >= el && y < el + EPV) ? static_cast<int>(y - el) : -1, dr,
+                         out_row + el);
+            }
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[stage]);
@@ -649,9 +759,9 @@ __global__ void __launch_bounds__(kStreamThreads, kStreamCtasPerSm)
   }
 }
 
-template <typename T, bool kBwd, bool kTwoPass = false>
-static int launch_stream(const StreamArgs& a, cudaStream_t s) {
-  auto kern = ce_stream_kernel<T, kBwd, kTwoPass>;
+template <typename T, bool kBwd, bool kTwoPass, bool kWhole>
+static int launch_stream_k(const StreamArgs& a, cudaStream_t s) {
+  auto kern = ce_stream_kernel<T, kBwd, kTwoPass, kWhole>;
   static std::atomic<uint64_t> done{0};  // devices whose smem limit is raised
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
@@ -668,6 +778,18 @@ static int launch_stream(const StreamArgs& a, cudaStream_t s) {
   const int grid = static_cast<int>(a.N < g ? a.N : g);
   kern<<<grid, kStreamThreads, kStreamSmem, s>>>(a);
   return launch_status(kBwd ? "ce_stream_kernel<bwd> launch" : "ce_stream_kernel<fwd> launch");
+}
+
+// Rows that all start and end on 16-byte boundaries take the instance without
+// partial-block handling.  (The backward's gradient rows sit at the same
+// offsets as the logits rows: the callers check that.)
+template <typename T, bool kBwd, bool kTwoPass = false>
+static int launch_stream(const StreamArgs& a, cudaStream_t s) {
+  const bool whole = reinterpret_cast<uintptr_t>(a.logits) % 16 == 0 &&
+                     (a.ld * static_cast<int64_t>(sizeof(T))) % 16 == 0 &&
+                     (a.V * static_cast<int64_t>(sizeof(T))) % 16 == 0;
+  return whole ? launch_stream_k<T, kBwd, kTwoPass, true>(a, s)
+               : launch_stream_k<T, kBwd, kTwoPass, false>(a, s);
 }
 
 // ------------------------------ backward without a saved lse: resident rows
@@ -730,7 +852,9 @@ struct ResArgs {
   float* lse_out;  // may be null
 };
 
-template <typename T>
+// kWhole: every row starts and ends on a 16-byte boundary (no partial blocks;
+// the edge handling is compiled out).
+template <typename T, bool kWhole>
 __global__ void __launch_bounds__(kResThreads, 3) ce_bwd_resident_kernel(const ResArgs a) {
   constexpr int EPV = Elem<T>::kPerVec;
   extern __shared__ uint8_t res_raw[];
@@ -752,19 +876,34 @@ __global__ void __launch_bounds__(kResThreads, 3) ce_bwd_resident_kernel(const R
   const uint32_t rank = cluster_ctarank();
   const uint32_t P = cluster_nctarank();
   const int64_t nclusters = gridDim.x / P;
-  const int64_t nvec_row = a.V * static_cast<int64_t>(sizeof(T)) / 16;
-  const int64_t v_lo = min(nvec_row, static_cast<int64_t>(rank) * a.slice_vec);
-  const int nv = static_cast<int>(min(nvec_row, v_lo + a.slice_vec) - v_lo);
-  const int nseg = (nv + kResSegVec - 1) / kResSegVec;
+  auto span = [&](int64_t r) -> RowSpan {
+    if (!kWhole) return row_span<T>(a.logits, r, a.ld, a.V);
+    RowSpan sp;
+    sp.a0 = reinterpret_cast<const char*>(static_cast<const T*>(a.logits) + r * a.ld);
+    sp.head = 0;
+    sp.nvec = a.V * static_cast<int64_t>(sizeof(T)) / 16;
+    return sp;
+  };
+  auto edges = [&](int64_t e0, int n) -> PieceEdges {
+    return kWhole ? PieceEdges::whole(n) : PieceEdges(e0, n, a.V, EPV);
+  };
+  // this CTA's slice of a row: blocks [v_lo, v_lo + nv) of the row's 16-byte
+  // blocks (rows that start at different offsets within a block can differ by
+  // one block)
+  auto slice = [&](const RowSpan& sp, int64_t& v_lo, int& nv) {
+    v_lo = min(sp.nvec, static_cast<int64_t>(rank) * a.slice_vec);
+    nv = static_cast<int>(min(sp.nvec, v_lo + a.slice_vec) - v_lo);
+  };
   if (tid == 0) {
     for (int i = 0; i < kResMaxSegs; ++i) mbar_init(&bar[i], 1);
     mbar_init(&xbar[0], 1);
     mbar_init(&xbar[1], 1);
-    // checked builds: the slice lies inside the row and fits the shared memory
-    // and the barriers of this launch; a failed check skips every copy
+    // checked builds: a slice fits the shared memory and the barriers of this
+    // launch; a failed check skips every copy
     const bool fits =
-        span_in_range(v_lo, nv, nvec_row, a.status) && in_range(rank, kResMaxCluster, a.status) &&
-        span_in_range(0, nseg, kResMaxSegs + 1, a.status) &&
+        in_range(rank, kResMaxCluster, a.status) &&
+        span_in_range(0, (a.slice_vec + kResSegVec - 1) / kResSegVec, kResMaxSegs + 1,
+                      a.status) &&
         smem_in_range(128, (a.slice_vec + 7) / 8 * 8 * 16, a.status);
     abort_sh = fits ? 0 : 1;
     xbroken_sh = 0;
@@ -776,6 +915,36 @@ __global__ void __launch_bounds__(kResThreads, 3) ce_bwd_resident_kernel(const R
   const bool fused = a.loss_rows != nullptr;
   const int64_t first = blockIdx.x / P;
 
+  // Writes this CTA's part of row r of dZ: whole blocks with 16-byte stores,
+  // the row's first and last block (shared with other rows) element by
+  // element.  sv: the slice in shared memory (unused when dr.c == 0).
+  auto write_dz = [&](int64_t r, const RowSpan& sp, int64_t v_lo, int nv, int64_t y,
+                      const DzRow<T>& dr) {
+    T* out_row = static_cast<T*>(a.grad) + r * a.ldg;
+    uint4* ob = reinterpret_cast<uint4*>(reinterpret_cast<uintptr_t>(out_row) &
+                                         ~static_cast<uintptr_t>(15)) +
+                v_lo;
+    const int64_t e0 = v_lo * EPV - sp.head;  // row element of the slice's first block
+    const PieceEdges pe = edges(e0, nv);
+    const int64_t yb = e0 + static_cast<int64_t>(pe.vb) * EPV;
+    const int64_t ylocal = y >= 0 ? y - yb : -1;
+    for (int v0 = 0; v0 < pe.ve - pe.vb; v0 += 4 * kResThreads)
+      dz_from_smem<T, 4, kResThreads>(buf + pe.vb, v0 + tid, pe.ve - pe.vb, ylocal, dr,
+                                      ob + pe.vb);
+    int lo, hi;
+    if (pe.head_part && tid == 0) {
+      block_range(e0, 0, a.V, EPV, lo, hi);
+      dz_part<T>(buf[0], lo, hi, (y >= e0 && y < e0 + EPV) ? static_cast<int>(y - e0) : -1, dr,
+                 out_row + e0);
+    }
+    if (pe.tail_part && !(pe.head_part && nv == 1) && tid == kResThreads - 1) {
+      const int64_t el = e0 + static_cast<int64_t>(nv - 1) * EPV;
+      block_range(e0, nv - 1, a.V, EPV, lo, hi);
+      dz_part<T>(buf[nv - 1], lo, hi, (y >= el && y < el + EPV) ? static_cast<int>(y - el) : -1,
+                 dr, out_row + el);
+    }
+  };
+
   // Rows of this cluster: first + i * nclusters.  Each warp reads the labels
   // of 32 rows at a time (one per lane) and keeps a bit mask of those that need
   // a copy (a nonzero gradient: the same answer in every thread and every CTA
@@ -784,6 +953,7 @@ __global__ void __launch_bounds__(kResThreads, 3) ce_bwd_resident_kernel(const R
   int64_t win = -32;   // index i of the window's first row
   uint32_t todo = 0u;  // bit t: row win + t exists and is not handed out yet
   uint32_t need = 0u;  // bit t: row win + t needs a copy
+  const DzRow<T> zero_dr(0.0f, 0.0f);
   auto next_row = [&]() -> int64_t {
     while (true) {
       if (todo == 0u) {
@@ -802,9 +972,11 @@ __global__ void __launch_bounds__(kResThreads, 3) ce_bwd_resident_kernel(const R
       todo &= todo - 1u;
       const int64_t r = first + (win + t) * nclusters;
       if ((need >> t) & 1u) return r;
-      uint4* out = reinterpret_cast<uint4*>(static_cast<T*>(a.grad) + r * a.ldg) + v_lo;
-      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-      for (int v = tid; v < nv; v += kResThreads) __stcs(out + v, z);
+      const RowSpan sp = span(r);
+      int64_t v_lo;
+      int nv;
+      slice(sp, v_lo, nv);
+      write_dz(r, sp, v_lo, nv, -1, zero_dr);
       if (fused && rank == 0 && tid == 0) {  // an ignored (or out-of-range) label: no loss
         const int64_t yr = __ldg(a.labels + r);
         if (yr != a.ignore_index) set_status(a.status, FLCE_ELABEL);
@@ -814,28 +986,41 @@ __global__ void __launch_bounds__(kResThreads, 3) ce_bwd_resident_kernel(const R
     }
   };
 
-  uint32_t phase = 0u;  // parity of the slice barriers' current phase
-  int issued_par = -1;  // thread 0: parity of the last copies issued (drain on abort)
-  uint32_t k = 0;       // copied rows so far
+  uint32_t par = 0u;         // bit sg: parity of bar[sg]'s current phase
+  uint32_t issued = 0u;      // thread 0: segments with a copy issued
+  uint32_t issued_par = 0u;  // thread 0: bit sg, the phase parity of that copy
+  uint32_t k = 0;            // copied rows so far
   for (int64_t row = next_row(); row < a.N; row = next_row(), ++k) {
     const int64_t y = __ldg(a.labels + row);
+    const RowSpan sp = span(row);
+    int64_t v_lo;
+    int nv;
+    slice(sp, v_lo, nv);
+    const int nseg = (nv + kResSegVec - 1) / kResSegVec;
+    const int64_t e0 = v_lo * EPV - sp.head;  // row element of the slice's first block
     if (tid == 0 && !*abort_flag) {
-      const char* src = reinterpret_cast<const char*>(static_cast<const T*>(a.logits) +
-                                                      row * a.ld) +
-                        v_lo * 16;
-      for (int sg = 0; sg < nseg; ++sg) {
-        const uint32_t bytes = static_cast<uint32_t>(min(kResSegVec, nv - sg * kResSegVec)) * 16u;
-        mbar_arrive_expect_tx(&bar[sg], bytes);
-        bulk_load(buf + sg * kResSegVec, src + static_cast<int64_t>(sg) * kResSeg, bytes,
-                  &bar[sg]);
+      // checked builds: the slice lies inside the row's blocks
+      if (!span_in_range(v_lo, nv, sp.nvec, a.status) ||
+          !span_in_range(0, nseg, kResMaxSegs + 1, a.status)) {
+        *abort_flag = 1;
+      } else {
+        const char* src = sp.a0 + v_lo * 16;
+        for (int sg = 0; sg < nseg; ++sg) {
+          const uint32_t bytes =
+              static_cast<uint32_t>(min(kResSegVec, nv - sg * kResSegVec)) * 16u;
+          mbar_arrive_expect_tx(&bar[sg], bytes);
+          bulk_load(buf + sg * kResSegVec, src + static_cast<int64_t>(sg) * kResSeg, bytes,
+                    &bar[sg]);
+          issued |= 1u << sg;
+          issued_par = (issued_par & ~(1u << sg)) | (par & (1u << sg));
+        }
       }
-      issued_par = static_cast<int>(phase);
     }
     // reduction of the slice, piece by piece as the copies land
     Lse2 st;
     for (int sg = 0; sg < nseg; ++sg) {
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(&bar[sg], phase, abort_flag) ? 1 : 0;
+      if (lane == 0) ok = mbar_wait(&bar[sg], (par >> sg) & 1u, abort_flag) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
         if (lane == 0 && !*abort_flag) {
@@ -844,10 +1029,22 @@ __global__ void __launch_bounds__(kResThreads, 3) ce_bwd_resident_kernel(const R
         }
         break;
       }
-      lse_add_smem<T, kResSegVec / kResThreads, kResThreads>(
-          buf + sg * kResSegVec, tid, min(kResSegVec, nv - sg * kResSegVec), st);
+      const int cnt = min(kResSegVec, nv - sg * kResSegVec);
+      const int64_t es0 = e0 + static_cast<int64_t>(sg) * kResSegVec * EPV;
+      const PieceEdges pe = edges(es0, cnt);
+      const uint4* sv = buf + sg * kResSegVec;
+      lse_add_smem<T, kResSegVec / kResThreads, kResThreads>(sv + pe.vb, tid, pe.ve - pe.vb, st);
+      int lo, hi;
+      if (pe.head_part && tid == 0) {
+        block_range(es0, 0, a.V, EPV, lo, hi);
+        lse_add_part<T>(sv[0], lo, hi, st);
+      }
+      if (pe.tail_part && !(pe.head_part && cnt == 1) && tid == kResThreads - 1) {
+        block_range(es0, cnt - 1, a.V, EPV, lo, hi);
+        lse_add_part<T>(sv[cnt - 1], lo, hi, st);
+      }
     }
-    phase ^= 1u;
+    par ^= (1u << nseg) - 1u;  // the segments this row used moved to their next phase
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float m2 = __shfl_xor_sync(0xffffffffu, st.m, o);
@@ -886,15 +1083,15 @@ __global__ void __launch_bounds__(kResThreads, 3) ce_bwd_resident_kernel(const R
           set_status(a.status, FLCE_ETIMEOUT);
         }
       }
-      float m = -INFINITY, sp = 0.0f;
+      float m = -INFINITY, sp2 = 0.0f;
       if (lane < static_cast<int>(P)) {
         const float2 pr = pairs[j][lane];
         m = pr.x;
-        sp = pr.y;
+        sp2 = pr.y;
       }
       Lse2 all;
       for (int q = 0; q < static_cast<int>(P); ++q)
-        all.merge(__shfl_sync(0xffffffffu, m, q), __shfl_sync(0xffffffffu, sp, q));
+        all.merge(__shfl_sync(0xffffffffu, m, q), __shfl_sync(0xffffffffu, sp2, q));
       if (lane == 0) lse2_sh = all.m + log2f(all.s);
     }
     __syncthreads();
@@ -902,27 +1099,22 @@ __global__ void __launch_bounds__(kResThreads, 3) ce_bwd_resident_kernel(const R
     if (fused && tid == 0) {
       // the row's loss, from the CTA whose slice holds the label's logit
       const float lse = lse2 * kLn2;
-      const int64_t yl = y - v_lo * EPV;
+      const int64_t yl = y - e0;  // the label's element within the slice
       if (yl >= 0 && yl < static_cast<int64_t>(nv) * EPV)
         a.loss_rows[row] = lse - Elem<T>::load(reinterpret_cast<const T*>(buf) + yl);
       if (rank == 0 && a.lse_out != nullptr) a.lse_out[row] = lse;
     }
-    if (!*abort_flag) {
-      uint4* out = reinterpret_cast<uint4*>(static_cast<T*>(a.grad) + row * a.ldg) + v_lo;
-      const int64_t ylocal = y - v_lo * EPV;  // label element relative to the slice
-      const DzRow<T> dr(lse2, coef);
-      for (int v0 = 0; v0 < nv; v0 += 4 * kResThreads)
-        dz_from_smem<T, 4, kResThreads>(buf, v0 + tid, nv, ylocal, dr, out);
-    }
+    if (!*abort_flag) write_dz(row, sp, v_lo, nv, y, DzRow<T>(lse2, coef));
     __syncthreads();  // the slice buffer and lse2_sh are free again
   }
   // no CTA leaves while a peer may still be running
   cluster_sync();
-  if (tid == 0 && *abort_flag && issued_par >= 0) {
+  if (tid == 0 && *abort_flag) {
     // let this CTA's copies in flight land before its shared memory is released
-    for (int sg = 0; sg < nseg; ++sg) {
+    for (int sg = 0; sg < kResMaxSegs; ++sg) {
+      if (!((issued >> sg) & 1u)) continue;
       const uint64_t t0 = global_ns();
-      while (!mbar_try_wait(smem_u32(&bar[sg]), static_cast<uint32_t>(issued_par)) &&
+      while (!mbar_try_wait(smem_u32(&bar[sg]), (issued_par >> sg) & 1u) &&
              global_ns() - t0 < kWaitLimitNs) {
       }
     }
@@ -932,21 +1124,16 @@ __global__ void __launch_bounds__(kResThreads, 3) ce_bwd_resident_kernel(const R
 struct ResCacheEntry {
   int dev, P, es;
   size_t smem;
+  bool whole;
   int clusters;
 };
 
-// Launches ce_bwd_resident_kernel.  Returns 1 (nothing launched) when a row
-// does not fit a cluster of kResMaxCluster slices or no cluster of that size
-// can be resident.
-template <typename T>
-static int launch_resident(ResArgs a, cudaStream_t s) {
-  const int64_t nvec_row = a.V * static_cast<int64_t>(sizeof(T)) / 16;
-  int P = 1;  // the fewest CTAs whose slices fit kResBuf bytes (128-byte aligned)
-  while (P <= kResMaxCluster && ((nvec_row + P - 1) / P + 7) / 8 * 8 * 16 > kResBuf) P *= 2;
-  if (P > kResMaxCluster) return 1;
-  a.slice_vec = (nvec_row + P - 1) / P;
+// Launches ce_bwd_resident_kernel on clusters of P CTAs (a.slice_vec set);
+// returns 1 (nothing launched) when no cluster of that size can be resident.
+template <typename T, bool kWhole>
+static int launch_resident_k(ResArgs a, int P, cudaStream_t s) {
   const size_t smem = static_cast<size_t>((a.slice_vec + 7) / 8 * 8) * 16 + 128;
-  auto kern = ce_bwd_resident_kernel<T>;
+  auto kern = ce_bwd_resident_kernel<T, kWhole>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
   static std::atomic<uint64_t> raised{0};
@@ -977,7 +1164,8 @@ static int launch_resident(ResArgs a, cudaStream_t s) {
   {
     std::lock_guard<std::mutex> lock(mu);
     for (const auto& e : cache)
-      if (e.dev == dev && e.P == P && e.es == static_cast<int>(sizeof(T)) && e.smem == smem)
+      if (e.dev == dev && e.P == P && e.es == static_cast<int>(sizeof(T)) && e.smem == smem &&
+          e.whole == kWhole)
         clusters = e.clusters;
   }
   if (clusters < 0) {
@@ -994,7 +1182,7 @@ static int launch_resident(ResArgs a, cudaStream_t s) {
     }
     if (rc != FLCE_OK) return rc;
     std::lock_guard<std::mutex> lock(mu);
-    cache.push_back({dev, P, static_cast<int>(sizeof(T)), smem, clusters});
+    cache.push_back({dev, P, static_cast<int>(sizeof(T)), smem, kWhole, clusters});
   }
   if (clusters < 1) return 1;
   const int64_t g = a.N < clusters ? a.N : clusters;
@@ -1002,10 +1190,32 @@ static int launch_resident(ResArgs a, cudaStream_t s) {
   return cuda_status(cudaLaunchKernelEx(&cfg, kern, a), "cudaLaunchKernelEx(ce_bwd_resident_kernel)");
 }
 
-// The bulk-copy path needs 16-byte aligned row starts and lengths.
-static bool streamable(const void* p, int64_t ld, int64_t V, size_t es) {
-  return aligned(p, 16) && (ld * static_cast<int64_t>(es)) % 16 == 0 &&
-         (V * static_cast<int64_t>(es)) % 16 == 0;
+// Launches ce_bwd_resident_kernel.  Returns 1 (nothing launched) when a row
+// does not fit a cluster of kResMaxCluster slices or no cluster of that size
+// can be resident.
+template <typename T>
+static int launch_resident(ResArgs a, cudaStream_t s) {
+  // 16-byte blocks of the longest row: one more than the row's own length
+  // when rows may start inside a block
+  const int64_t bytes = a.V * static_cast<int64_t>(sizeof(T));
+  const bool rows_aligned = reinterpret_cast<uintptr_t>(a.logits) % 16 == 0 &&
+                            (a.ld * static_cast<int64_t>(sizeof(T))) % 16 == 0;
+  const int64_t nvec_row = (bytes + 15) / 16 + (rows_aligned ? 0 : 1);
+  int P = 1;  // the fewest CTAs whose slices fit kResBuf bytes (128-byte aligned)
+  while (P <= kResMaxCluster && ((nvec_row + P - 1) / P + 7) / 8 * 8 * 16 > kResBuf) P *= 2;
+  if (P > kResMaxCluster) return 1;
+  a.slice_vec = (nvec_row + P - 1) / P;
+  return rows_aligned && bytes % 16 == 0 ? launch_resident_k<T, true>(a, P, s)
+                                         : launch_resident_k<T, false>(a, P, s);
+}
+
+// The bulk-copy kernels copy whole 16-byte blocks and write the gradient
+// block by block at the same positions, so every gradient row must start at
+// the same offset within its block as its logits row (in place, or two
+// buffers whose starts and row strides agree modulo 16 bytes).
+static bool rows_alike(const void* x, int64_t ld, const void* g, int64_t ldg, size_t es) {
+  return (reinterpret_cast<uintptr_t>(x) - reinterpret_cast<uintptr_t>(g)) % 16 == 0 &&
+         ((ld - ldg) * static_cast<int64_t>(es)) % 16 == 0;
 }
 
 // ------------------------------------------------------------------ host side
@@ -1077,43 +1287,29 @@ static int row_grid(int64_t N) {
   return static_cast<int>(N < g ? (N > 0 ? N : 1) : g);
 }
 
-// Launches the per-row forward kernel (bulk-copy streaming for 16-byte aligned
-// rows, register streaming otherwise).  sh.m_out != nullptr: vocabulary-shard
-// outputs instead of lse / loss rows.
+// Launches the forward (the bulk-copy ring for every row alignment).
+// sh.m_out != nullptr: vocabulary-shard outputs instead of lse / loss rows.
 static int ce_fwd_rows(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
                        const int64_t* labels, int64_t ignore_index, float* lse, float* rows,
                        float* label_logit, const ShardOut& sh, int32_t* status,
                        cudaStream_t s) {
   if (N == 0) return FLCE_OK;
-  if (streamable(logits, ld, V, dtype_size(dt))) {
-    StreamArgs a{};
-    a.logits = logits;
-    a.N = N;
-    a.V = V;
-    a.ld = ld;
-    a.labels = labels;
-    a.ignore_index = ignore_index;
-    a.lse_out = lse;
-    a.loss_rows = rows;
-    a.label_logit = label_logit;
-    a.status = status;
-    a.v0 = sh.m_out != nullptr ? sh.v0 : 0;
-    a.V_total = sh.m_out != nullptr ? sh.V_total : V;
-    a.sh = sh;
-    return dt == FLCE_BF16 ? launch_stream<__nv_bfloat16, false>(a, s)
-                           : launch_stream<float, false>(a, s);
-  }
-  const int grid = row_grid(N);
-  if (dt == FLCE_BF16) {
-    ce_fwd_rows_kernel<__nv_bfloat16, 512><<<grid, 512, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(logits), N, V, ld, labels, ignore_index, lse, rows,
-        label_logit, status, sh);
-  } else {
-    ce_fwd_rows_kernel<float, 512><<<grid, 512, 0, s>>>(static_cast<const float*>(logits), N, V,
-                                                        ld, labels, ignore_index, lse, rows,
-                                                        label_logit, status, sh);
-  }
-  return launch_status("ce_fwd_rows_kernel launch");
+  StreamArgs a{};
+  a.logits = logits;
+  a.N = N;
+  a.V = V;
+  a.ld = ld;
+  a.labels = labels;
+  a.ignore_index = ignore_index;
+  a.lse_out = lse;
+  a.loss_rows = rows;
+  a.label_logit = label_logit;
+  a.status = status;
+  a.v0 = sh.m_out != nullptr ? sh.v0 : 0;
+  a.V_total = sh.m_out != nullptr ? sh.V_total : V;
+  a.sh = sh;
+  return dt == FLCE_BF16 ? launch_stream<__nv_bfloat16, false>(a, s)
+                         : launch_stream<float, false>(a, s);
 }
 
 extern "C" int ce_logits_fwd(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
@@ -1319,7 +1515,7 @@ static int ce_bwd_entry(const void* logits, int dt, int64_t N, int64_t V, int64_
   if (rc != FLCE_OK) return rc;
   const size_t es = dtype_size(dt);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const bool stream_ok = streamable(logits, ld, V, es) && streamable(grad_logits, ld_grad, V, es);
+  const bool stream_ok = rows_alike(logits, ld, grad_logits, ld_grad, es);
   if (stream_ok && lse == nullptr) {
     ResArgs r{};
     r.logits = logits;
@@ -1429,7 +1625,7 @@ extern "C" int ce_logits_fwd_bwd(const void* logits, int dt, int64_t N, int64_t 
   float* rows = reinterpret_cast<float*>(w);
   float* lse_buf = reinterpret_cast<float*>(w + round_up(static_cast<size_t>(N) * 4, 256));
   const size_t es = dtype_size(dt);
-  if (N > 0 && streamable(logits, ld, V, es) && streamable(grad_logits, ld_grad, V, es)) {
+  if (N > 0 && rows_alike(logits, ld, grad_logits, ld_grad, es)) {
     // one pass: the count of valid rows first (the mean's divisor), then each
     // row read once by a row cluster that forms its lse, loss and gradient
     rc = flce_count_valid(labels, N, V, ignore_index, n_valid, stream);

@@ -47,7 +47,7 @@ def _check_grad(got, want):
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("reduction,nlt", [("sum", None), ("mean", None), ("sum", 1000)])
 @pytest.mark.parametrize("N,V,ld", [(300, 1000, 1000), (77, 1003, 1011), (5, 32777, 32777),
-                                    (130, 4099, 4099)])
+                                    (130, 4099, 4099), (64, 50257, 50257), (9, 128255, 128255)])
 def test_ce_parity(lh, dtype, reduction, nlt, N, V, ld):
     p = wl.random_ce(N, V, dtype, seed=N + V, reduction=reduction, num_label_tokens=nlt, ld=ld)
     logits, labels = _dev(p)
@@ -218,3 +218,35 @@ def test_full_size_workload_sampled(lh):
     assert abs(out.loss.item() - lr.sum()) <= 1e-6 * abs(lr.sum())
     dz = oracle.ce_backward(host_rows, host_labels)  # scale 1 (sum)
     _check_grad(p.logits[rows].cpu(), dz)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("col0", [1, 3, 8])
+def test_ce_on_a_column_slice(lh, dtype, col0):
+    # logits that start inside a 16-byte block: columns [col0, col0 + V) of a
+    # wider buffer; in place and out of place
+    N, V, W = 70, 5003, 5020
+    full = wl.random_ce(N, W, dtype, seed=col0 + 40).logits
+    p = wl.random_ce(N, V, dtype, seed=col0 + 41, reduction="mean")
+    x_host = full[:, col0:col0 + V]
+    dev_full = full.cuda()
+    x = dev_full[:, col0:col0 + V]
+    labels = p.labels.cuda()
+    out = lh.ce_logits_fwd(x, labels, -100, "mean")
+    ref = oracle.ce_forward(x_host, p.labels, -100, "mean")
+    _check_fwd(out, ref)
+    assert abs(out.loss.item() - ref["loss"]) <= 1e-3 * abs(ref["loss"])
+    g = torch.tensor([1.5], device="cuda")
+    want = oracle.ce_backward(x_host, p.labels, -100, "mean", grad_loss=1.5)
+    grad = lh.ce_logits_bwd(x, labels, out.lse, out.n_valid, g, -100, "mean")
+    torch.cuda.synchronize()
+    _check_grad(grad, want)
+    before = dev_full.clone()
+    lh.ce_logits_bwd(x, labels, out.lse, out.n_valid, g, -100, "mean", inplace_grad=True,
+                     status=out.status)
+    torch.cuda.synchronize()
+    lh.check_status(out.status)
+    _check_grad(x, want)
+    # the columns outside the slice are untouched
+    assert torch.equal(dev_full[:, :col0], before[:, :col0])
+    assert torch.equal(dev_full[:, col0 + V:], before[:, col0 + V:])

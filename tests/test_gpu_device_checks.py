@@ -49,12 +49,13 @@ def test_build_flags_and_bounds_selftest(libs):
 
 
 def _ce_cases():
-    # (dtype, N, V, ld): the bulk-copy ring, the unaligned row kernels, and for
-    # the no-lse backward and the one-call forward and backward clusters of 1
-    # and 4 and the twice-streamed rows
+    # (dtype, N, V, ld): the bulk-copy ring, rows that start and end inside
+    # 16-byte blocks, and for the no-lse backward and the one-call forward and
+    # backward clusters of 1, 2 and 4 and the twice-streamed rows
     return [(torch.bfloat16, 300, 5000, 5000), (torch.bfloat16, 77, 1003, 1011),
             (torch.float32, 64, 4100, 4104), (torch.bfloat16, 64, 128256, 128256),
-            (torch.bfloat16, 4, 300000, 300000)]
+            (torch.bfloat16, 4, 300000, 300000), (torch.bfloat16, 40, 50257, 50257),
+            (torch.bfloat16, 3, 262143, 262143)]
 
 
 def _run_ce(lh, dtype, N, V, ld):
