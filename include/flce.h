@@ -197,12 +197,14 @@ FLCE_API int ce_logits_fwd_noalloc(const void* logits, int dt, int64_t N, int64_
  * lse may be NULL: the backward that keeps only the logits and the labels
  * from the forward (Automodel PR #2996, the memory bullet: nothing but the
  * inputs is saved).  Each row's lse is then formed again inside the kernel.
- * Rows whose start, stride and length are 16-byte multiples and whose
- * length is at most 8 x 64 KiB (V <= 262144 bf16, 131072 f32) are split over a
- * thread-block cluster that holds the row in shared memory, so the logits are
- * still read once; longer rows, and rows that are not 16-byte aligned, are
- * read twice.  The result equals the saved-lse backward up to the rounding of
- * the recomputed lse (fp32, a few ulp). */
+ * A row of at most 8 x 64 KiB (V <= 262144 bf16, 131072 f32; one 16-byte
+ * block less when rows start inside a block) is split over a thread-block
+ * cluster that holds it in shared memory, so the logits are still read once,
+ * provided the gradient rows start at the same offsets within their 16-byte
+ * blocks as the logits rows (in place, or both buffers aligned alike); longer
+ * rows, and gradient buffers at other offsets, read the logits twice.  The
+ * result equals the saved-lse backward up to the rounding of the recomputed
+ * lse (fp32, a few ulp). */
 FLCE_API int ce_logits_bwd(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
                   const int64_t* labels, int64_t ignore_index, int reduction,
                   int64_t num_label_tokens, const float* lse, const int64_t* n_valid,
@@ -229,11 +231,12 @@ FLCE_API size_t ce_logits_fwd_bwd_workspace_bytes(int64_t N, int64_t V);
  * ce_logits_bwd; in place, the logits are overwritten by their gradient.
  * ws: ce_logits_fwd_bwd_workspace_bytes(N, V) bytes, 16-byte aligned.
  *
- * Rows whose start, stride and length are 16-byte multiples in both the
- * logits and the gradient, and at most 8 x 64 KiB long, are read once: a
- * thread-block cluster holds each row in shared memory, forms its lse and
- * loss and writes its gradient (rows with an ignored label are not read).
- * Other rows run the forward and then the backward (two reads). */
+ * Rows of at most 8 x 64 KiB whose gradient rows start at the same offsets
+ * within their 16-byte blocks as the logits rows (in place, or both buffers
+ * aligned alike) are read once: a thread-block cluster holds each row in
+ * shared memory, forms its lse and loss and writes its gradient (rows with an
+ * ignored label are not read).  Other rows run the forward and then the
+ * backward (two reads). */
 FLCE_API int ce_logits_fwd_bwd(const void* logits, int dt, int64_t N, int64_t V, int64_t ld,
                   const int64_t* labels, int64_t ignore_index, int reduction,
                   int64_t num_label_tokens, const float* grad_loss, float* loss,
