@@ -81,9 +81,14 @@ def test_flce_random_shape(case):
 @pytest.mark.parametrize("case", CASES[:8], ids=[f"{c['N']}x{c['V']}" for c in CASES[:8]])
 def test_ce_random_shape(case):
     import lm_head_linear_fwd_gb300 as lh
-    ld = case["V"] + (0 if case["seed"] % 2 else int(case["seed"] % 13))
-    c = wl.random_ce(case["N"], case["V"], case["dtype"], seed=case["seed"], ld=ld,
+    # a row stride a few elements over V, and for some cases a first column
+    # inside a 16-byte block (a column slice of a wider buffer)
+    c0 = int(case["seed"] % 5)
+    ld = case["V"] + c0 + (0 if case["seed"] % 2 else int(case["seed"] % 13))
+    c = wl.random_ce(case["N"], ld, case["dtype"], seed=case["seed"],
                      reduction=case["reduction"], num_label_tokens=case["nlt"])
+    c.logits = c.logits[:, c0:c0 + case["V"]]
+    c.labels = torch.where(c.labels >= case["V"], c.labels % case["V"], c.labels)
     logits, y = c.logits.cuda(), c.labels.cuda()
     out = lh.ce_logits_fwd(logits, y, -100, c.reduction, c.num_label_tokens)
     grad = lh.ce_logits_bwd(logits, y, out.lse, out.n_valid, torch.ones(1, device="cuda"), -100,
@@ -99,7 +104,15 @@ def test_ce_random_shape(case):
                              c.reduction, c.num_label_tokens, status=out.status)
     torch.cuda.synchronize()
     lh.check_status(out.status)
+    # and forward and backward in one call
+    o3, grad3 = lh.ce_logits_fwd_bwd(logits, y, -100, c.reduction, c.num_label_tokens,
+                                     status=out.status)
+    torch.cuda.synchronize()
+    lh.check_status(out.status)
+    assert int(o3.n_valid.item()) == ref["n_valid"]
+    assert abs(o3.loss.item() - ref["loss"]) <= 1e-3 * abs(ref["loss"]) + 1e-6
     if ref["loss"] != 0.0:
         want = oracle.ce_backward(c.logits, c.labels, -100, c.reduction, c.num_label_tokens)
         _grad_ok(grad, want, "dZ")
         _grad_ok(grad2, want, "dZ without a saved lse")
+        _grad_ok(grad3, want, "dZ in one call")
