@@ -120,6 +120,33 @@ def test_ce_bwd_rejects_bad_arguments(lib):
 
 
 @no_gpu
+def test_ce_fwd_bwd_rejects_bad_arguments(lib):
+    from lm_head_linear_fwd_gb300 import _abi
+    G = FAKE + (1 << 20)  # a separate gradient buffer
+    args = dict(logits=FAKE, dt=0, N=4, V=10, ld=10, labels=FAKE, ig=-100, red=0, nlt=-1,
+                g=None, loss=FAKE, nv=FAKE, lse=None, inplace=0, grad=G, ldg=10, ws=FAKE,
+                wsb=1024, status=FAKE, stream=None)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return _abi.ce_logits_fwd_bwd(*a.values())
+    assert call(dt=5) == -3
+    assert call(loss=None) == -1
+    assert call(status=None) == -1
+    assert call(inplace=2) == -1
+    assert call(inplace=1) == -1               # in place, but the gradient is elsewhere
+    assert call(inplace=1, grad=FAKE, ldg=12) == -1
+    assert call(grad=FAKE + 4) == -1           # out of place, overlapping the logits
+    assert call(grad=None) == -1
+    assert call(ldg=9) == -2
+    assert call(ws=None) == -6
+    assert call(wsb=8) == -6
+    assert call(ws=FAKE + 8) == -4
+    assert _abi.ce_logits_fwd_bwd_workspace_bytes(4, 10) >= 2 * 4 * 4
+    assert _abi.ce_logits_fwd_bwd_workspace_bytes(0, 10) == 0
+
+
+@no_gpu
 def test_flce_rejects_bad_arguments(lib):
     from lm_head_linear_fwd_gb300 import _abi
     base = [FAKE, FAKE, None, 0, 256, 128, 1000, FAKE, -100, 0, -1, FAKE, FAKE, FAKE, None, None,
@@ -129,6 +156,8 @@ def test_flce_rejects_bad_arguments(lib):
         a = list(base)
         a[i] = v
         return _abi.flce_fwd(*a)
+    assert call(4, -1) == -2         # N < 0 (N = 0, an empty batch, is valid)
+    assert call(1, None) == -1       # W missing
     assert call(5, 4) == -2          # D < 8
     assert call(5, 100) == -4        # D*2 not a multiple of 16
     assert call(0, FAKE + 2) == -4   # H not 16-byte aligned
