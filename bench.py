@@ -450,6 +450,7 @@ def run_ours(args, rank, ws, local):
     ce_one_line = ce_one_call(c, cst, stream, args, ws, peaks)
     del pristine, logits, c, cws, co
     torch.cuda.empty_cache()
+    ce_odd_line = ce_odd_vocab(dev, stream, args, ws, peaks)
 
     # ------------------------------------------------- latency-bound workloads
     small = latency_configs(dev, stream, args.steps)
@@ -507,6 +508,7 @@ def run_ours(args, rank, ws, local):
             "tokens_per_s": round(ce_N * ws / (ce_ms * 1e-3), 1),
             "bwd_only": ce_bwd_line,
             "fwd_bwd_one_call": ce_one_line,
+            "odd_vocabulary": ce_odd_line,
         },
         "roofline": {
             "bound": "tensor",
@@ -634,6 +636,47 @@ def ce_one_call(c, cst, stream, args, ws, peaks):
                       "(a row cluster holds each row in shared memory)")}
 
 
+def ce_odd_vocab(dev, stream, args, ws, peaks, V=50257):
+    """CE on given logits with rows that start and end inside 16-byte blocks
+    (an odd vocabulary, GPT-2's 50257): device time of the forward, the
+    backward with the saved lse (out of place) and the one-call forward and
+    backward, at the same 16384 rows."""
+    import torch
+    import workloads as wl
+    import lm_head_linear_fwd_gb300 as lh
+    c = wl.ce_logits_large(device=dev, N=args.ce_rows, V=V)
+    x, y = c.logits, c.labels
+    st = lh.new_status(dev)
+    g = torch.ones(1, device=dev)
+    gbuf = torch.empty_like(x)
+    o = lh.ce_logits_fwd(x, y, c.ignore_index, c.reduction, status=st)
+    fns = {
+        "fwd": lambda: lh.ce_logits_fwd(x, y, c.ignore_index, c.reduction, status=st, out=o),
+        "bwd_saved_lse": lambda: lh.ce_logits_bwd(x, y, o.lse, o.n_valid, g, c.ignore_index,
+                                                  c.reduction, grad_logits=gbuf, status=st),
+        "fwd_bwd_one_call": lambda: lh.ce_logits_fwd_bwd(x, y, c.ignore_index, c.reduction,
+                                                         grad_logits=gbuf, status=st),
+    }
+    n_valid_rows = int((y != c.ignore_index).sum().item())
+    row_b = float(V * 2)
+    nbytes = {"fwd": c.N * row_b, "bwd_saved_lse": 2.0 * c.N * row_b,
+              "fwd_bwd_one_call": (n_valid_rows + c.N) * row_b}
+    line = {"what": f"CE on [{c.N}, {V}] bf16 logits: rows start and end inside 16-byte "
+                    "blocks (partial first and last blocks)"}
+    for name, fn in fns.items():
+        for _ in range(max(3, args.warmup)):
+            fn()
+        t = _events_time(fn, args.steps, stream)
+        ms = max_over_ranks(sum(t) / len(t), ws)
+        gbs = nbytes[name] / (ms * 1e-3) / 1e9
+        line[name] = {"ms": round(ms, 4), "gb_s": round(gbs, 1),
+                      "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+    lh.check_status(st, "ce_odd_vocab")
+    del x, y, gbuf, o, c
+    torch.cuda.empty_cache()
+    return line
+
+
 def run_ce_only(args, rank, ws, local, dev, stream, peaks, peak_src):
     """Given-logits part alone (profiling runs)."""
     import torch
@@ -659,14 +702,19 @@ def run_ce_only(args, rank, ws, local, dev, stream, peaks, peak_src):
     gbs = 3.0 * c.N * c.V * 2 / (ms * 1e-3) / 1e9
     bwd_line = ce_bwd_compare(c, co, cst, one, stream, args, ws, peaks)
     one_line = ce_one_call(c, cst, stream, args, ws, peaks)
+    N, V = c.N, c.V
+    del c, logits, labels, cws, co
+    torch.cuda.empty_cache()
+    odd_line = ce_odd_vocab(dev, stream, args, ws, peaks)
     if rank == 0:
         print(json.dumps({"metric": METRIC, "value": round(gbs, 1), "unit": "GB/s",
                           "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
                           "ms_per_step": round(ms, 4),
-                          "config": {"workload": f"CE on logits only [{c.N},{c.V}] bf16"},
+                          "config": {"workload": f"CE on logits only [{N},{V}] bf16"},
                           "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
                           "bwd_only": bwd_line,
                           "fwd_bwd_one_call": one_line,
+                          "odd_vocabulary": odd_line,
                           "note": "profiling run: given-logits part only"}))
 
 
