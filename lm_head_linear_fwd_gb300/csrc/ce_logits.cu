@@ -182,6 +182,11 @@ int launch_finalize(const float* loss_rows, const int64_t* labels, int64_t N, in
 
 // -------------------------------------------------------------- backward kernel
 
+// The backward for a gradient buffer whose rows start at other offsets within
+// their 16-byte blocks than the logits rows (the bulk-copy kernels serve every
+// other case): such rows are read and written element by element (the 16-byte
+// path below needs both rows at one offset).  Without a saved lse (lse ==
+// nullptr) each row is reduced first (block_row_lse2), then transformed.
 template <typename T, int THREADS>
 __global__ void __launch_bounds__(THREADS) ce_bwd_rows_kernel(
     const T* logits, int64_t N, int64_t V, int64_t ld, const int64_t* __restrict__ labels,
@@ -262,14 +267,13 @@ __global__ void __launch_bounds__(THREADS) ce_bwd_rows_kernel(
   }
 }
 
-
 // ------------------------------------------------ bulk-copy (TMA) row streaming
 
 // Rows are streamed through a shared-memory ring: one producer thread copies
-// 32 KB segments of a row's 16-byte blocks with cp.async.bulk (a 2-stage mbarrier ring, so up to 64 KB per CTA is in
-// flight without holding registers; 3 CTAs per SM), and 8 consumer warps
-// reduce (forward) or transform and store (backward) each segment from shared
-// memory.  The segment size, stage count and CTAs per SM were chosen by a
+// 32 KB segments of a row's 16-byte blocks with cp.async.bulk (a 2-stage
+// mbarrier ring, so up to 64 KB per CTA is in flight without holding
+// registers; 3 CTAs per SM), and 8 consumer warps reduce (forward) or
+// transform and store (backward) each segment from shared memory.  The segment size, stage count and CTAs per SM were chosen by a
 // sweep on GB300 (16-32 KB segments, 2-8 stages, 2-4 CTAs per SM).
 #ifndef FLCE_CE_SEG_BYTES
 #define FLCE_CE_SEG_BYTES 32768
