@@ -14,7 +14,6 @@ only orders the phases and the collectives, through an ``exchange`` with
 from __future__ import annotations
 
 import dataclasses
-from typing import Optional
 
 import torch
 import torch.distributed as dist

@@ -19,7 +19,6 @@ dtype, and the recomputed lse differs from the saved one by a few fp32 ulp
 rounding flip per element: 2^-7 relative for bf16 (bound 1e-2), and for fp32
 about 1e-6 (bound 1e-5).
 """
-import numpy as np
 import pytest
 import torch
 
