@@ -201,13 +201,17 @@ def flce_forward(H, W, bias, labels, ignore_index=-100, reduction="sum",
 
 def flce_backward(H, W, bias, labels, ignore_index=-100, reduction="sum",
                   num_label_tokens=None, grad_loss=1.0, grad_W_init=None,
-                  want_grad_H=True, want_grad_W=True, rows=None, n_valid_total=None):
+                  want_grad_H=True, want_grad_W=True, rows=None, n_valid_total=None,
+                  with_forward=False):
     """Backward of the fused linear CE.
 
     grad_H = dZ @ W, grad_W = (grad_W_init or 0) + dZ.T @ H, grad_b = sum_i dZ_i,
     with dZ as in ``ce_backward``.  ``rows`` restricts the computation to a row
     subset; the scale then uses ``n_valid_total`` if given (the count over the
-    whole problem), else the subset's own count."""
+    whole problem), else the subset's own count.  ``with_forward`` also returns,
+    under "forward", what ``flce_forward`` returns for the same rows (the
+    backward forms the same logits and lse, so large problems need not form
+    them twice)."""
     H64 = None
     W64 = _f64(W)
     b64 = _f64(bias)
@@ -222,6 +226,8 @@ def flce_backward(H, W, bias, labels, ignore_index=-100, reduction="sum",
     grad_W = (np.zeros((V, D)) if grad_W_init is None else _f64(grad_W_init).copy()) \
         if want_grad_W else None
     grad_b = np.zeros(V)
+    lse_all = np.empty(len(idx))
+    zy = np.full(len(idx), np.nan)
     for b0, b1 in _blocks(len(idx)):
         r = idx[b0:b1]
         H64 = _f64(H[r])
@@ -229,13 +235,21 @@ def flce_backward(H, W, bias, labels, ignore_index=-100, reduction="sum",
         if b64 is not None:
             Z += b64[None, :]
         lse = logsumexp_rows(Z)
+        if with_forward:
+            lse_all[b0:b1] = lse
+            v = np.nonzero(valid_all[r])[0]
+            zy[b0 + v] = Z[v, y_all[r][v]]
         dZ = _dlogits(Z, lse, y_all[r], valid_all[r], coef)
         if want_grad_H:
             grad_H[b0:b1] = dZ @ W64
         if want_grad_W:
             grad_W += dZ.T @ H64
         grad_b += dZ.sum(axis=0)
-    return {"grad_H": grad_H, "grad_W": grad_W, "grad_b": grad_b}
+    out = {"grad_H": grad_H, "grad_W": grad_W, "grad_b": grad_b}
+    if with_forward:
+        out["forward"] = _finish_forward(lse_all, zy, valid_all[idx], reduction,
+                                         num_label_tokens)
+    return out
 
 
 # ------------------------------------------------------------------ comparison metrics

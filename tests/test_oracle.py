@@ -348,3 +348,149 @@ def test_planted_transposed_grad_W_is_caught(monkeypatch):
     monkeypatch.setattr(oracle, "flce_backward", bad)
     with pytest.raises(AssertionError):
         test_flce_matches_torch_autograd(False)
+
+
+# ------------------------------------------ comparison metrics and the logits helper
+#
+# Every GPU gradient assertion goes through max_rel_err and normwise_err, and the
+# invariant tests build dZ through flce_logits, so each is pinned here by values
+# worked out by hand (the "derivation" comments), with a case that tells apart
+# the plausible wrong versions: a denominator taken from `got`, a dropped abs,
+# 0 returned for a zero reference, a max-row or spectral norm in place of the
+# Frobenius norm, a dropped bias, a transposed weight, the wrong rows.
+
+def _pin_max_rel(fn):
+    # diff = [0, 0, -1] -> max|diff| = 1; max|ref| = 4 -> 0.25
+    assert fn(np.array([1.0, 2.0, 3.0]), np.array([1.0, 2.0, 4.0])) == pytest.approx(0.25, abs=1e-15)
+    # ref has its largest magnitude on a negative entry (-2): max|ref| = 2, not
+    # max(ref) = 1; got - ref = [[-1, -0.5], [0, 0]] is never positive, so a
+    # max without abs would give 0 -> 1 / 2 = 0.5
+    assert fn(np.array([[-3.0, 0.0], [0.0, 1.0]]),
+              np.array([[-2.0, 0.5], [0.0, 1.0]])) == pytest.approx(0.5, abs=1e-15)
+    # the denominator is the reference's: max|got - ref| = 9, max|ref| = 1 -> 9
+    assert fn(np.array([10.0, 0.0]), np.array([1.0, 0.0])) == pytest.approx(9.0, abs=1e-14)
+    # zero reference: the absolute error, max|got| = 0.5 (0 would hide any error)
+    assert fn(np.array([0.0, -0.5]), np.zeros(2)) == pytest.approx(0.5, abs=1e-15)
+    assert fn(np.zeros((2, 3)), np.zeros((2, 3))) == 0.0
+    # identical inputs, and bf16 torch tensors widened exactly: 1.5 and 3.0 are
+    # bf16 values; |1.5 - 1.25| / 3 = 1/12
+    t = torch.tensor([1.5, 3.0], dtype=torch.bfloat16)
+    assert fn(t, t) == 0.0
+    assert fn(t, np.array([1.25, 3.0])) == pytest.approx(1.0 / 12.0, abs=1e-15)
+
+
+def _pin_normwise(fn):
+    # ref = diag(3, 4): Frobenius norm 5 (spectral norm 4); got - ref = e_22:
+    # norm 1 -> 1/5 = 0.2 (a spectral ratio would also give 1/4 = 0.25)
+    ref = np.array([[3.0, 0.0], [0.0, 4.0]])
+    assert fn(ref + np.array([[0.0, 0.0], [0.0, 1.0]]), ref) == pytest.approx(0.2, abs=1e-15)
+    # the error spread over two rows: diff = [[0, 0.3], [0.4, 0]] -> 0.5 / 5 = 0.1
+    # (a max-row norm would give 0.4 / 4 = 0.1 by accident here, so the next case)
+    assert fn(ref + np.array([[0.0, 0.3], [0.4, 0.0]]), ref) == pytest.approx(0.1, abs=1e-15)
+    # the whole error in one row: diff = [[0.6, 0.8], [0, 0]] -> 1 / 5 = 0.2
+    # (max-row ratio 1 / 4 = 0.25)
+    assert fn(ref + np.array([[0.6, 0.8], [0.0, 0.0]]), ref) == pytest.approx(0.2, abs=1e-15)
+    # the denominator is the reference's: got = 2 ref -> ||ref|| / ||ref|| = 1
+    # (dividing by ||got|| would give 1/2)
+    assert fn(2.0 * ref, ref) == pytest.approx(1.0, abs=1e-15)
+    # zero reference: the absolute norm, ||(3, 4)|| = 5
+    assert fn(np.array([3.0, -4.0]), np.zeros(2)) == pytest.approx(5.0, abs=1e-15)
+    assert fn(np.zeros(3), np.zeros(3)) == 0.0
+
+
+def test_max_rel_err_hand_values():
+    _pin_max_rel(oracle.max_rel_err)
+
+
+def test_normwise_err_hand_values():
+    _pin_normwise(oracle.normwise_err)
+
+
+# H [3, 2], W [3, 2] (V = 3), bias [3]; the values of each case are worked out
+# by hand in its comment.
+_H = np.array([[1.0, 2.0], [3.0, -1.0], [0.0, 0.5]])
+_W = np.array([[1.0, 0.0], [0.0, 1.0], [2.0, -1.0]])
+_B = np.array([0.5, -1.0, 0.0])
+
+
+def _pin_flce_logits(fn):
+    # row 2, h = (0, 0.5): h.w_v = (0, 0.5, -0.5); + bias -> (0.5, -0.5, -0.5)
+    # row 0, h = (1, 2):   h.w_v = (1, 2, 0);      + bias -> (1.5, 1, 0)
+    np.testing.assert_array_equal(fn(_H, _W, _B, np.array([2, 0])),
+                                  [[0.5, -0.5, -0.5], [1.5, 1.0, 0.0]])
+    # row 1, h = (3, -1), no bias: (3, -1, 7)
+    np.testing.assert_array_equal(fn(_H, _W, None, np.array([1])), [[3.0, -1.0, 7.0]])
+    # a non-square weight (V = 4, D = 2) and bf16 inputs widened exactly:
+    # h = (2, 0.5): w = (1, 1), (-1, 0), (0, 4), (0.25, -2) -> (2.5, -2, 2, -0.5)
+    W4 = torch.tensor([[1.0, 1.0], [-1.0, 0.0], [0.0, 4.0], [0.25, -2.0]], dtype=torch.bfloat16)
+    H1 = torch.tensor([[2.0, 0.5]], dtype=torch.bfloat16)
+    np.testing.assert_array_equal(fn(H1, W4, None, np.array([0])), [[2.5, -2.0, 2.0, -0.5]])
+
+
+def test_flce_logits_hand_values():
+    _pin_flce_logits(oracle.flce_logits)
+
+
+def _fails(check, fn):
+    try:
+        check(fn)
+    except (AssertionError, ValueError):
+        return True
+    return False
+
+
+@pytest.mark.parametrize("bad", [
+    lambda g, r: float(np.max(np.abs(olc._f64(g) - olc._f64(r))) / max(np.max(np.abs(olc._f64(g))), 1e-300)),
+    lambda g, r: float(np.max(olc._f64(g) - olc._f64(r)) / np.max(np.abs(olc._f64(r))))
+    if np.max(np.abs(olc._f64(r))) else 0.0,
+    lambda g, r: float(np.max(np.abs(olc._f64(g) - olc._f64(r))) / np.max(olc._f64(r)))
+    if np.max(olc._f64(r)) else 0.0,
+    lambda g, r: float(np.max(np.abs(olc._f64(g) - olc._f64(r))) / np.max(np.abs(olc._f64(r))))
+    if np.max(np.abs(olc._f64(r))) else 0.0,
+], ids=["den_from_got", "no_abs_on_diff", "no_abs_on_ref", "zero_ref_gives_0"])
+def test_planted_max_rel_err_mistakes_are_caught(bad):
+    assert _fails(_pin_max_rel, bad)
+
+
+@pytest.mark.parametrize("bad", [
+    lambda g, r: float(np.linalg.norm(olc._f64(g) - olc._f64(r)) / np.linalg.norm(olc._f64(g)))
+    if np.linalg.norm(olc._f64(g)) else 0.0,
+    lambda g, r: float(np.linalg.norm(np.atleast_2d(olc._f64(g) - olc._f64(r)), 2) /
+                       np.linalg.norm(np.atleast_2d(olc._f64(r)), 2))
+    if np.linalg.norm(olc._f64(r)) else float(np.linalg.norm(olc._f64(g))),
+    lambda g, r: float(np.max(np.linalg.norm(np.atleast_2d(olc._f64(g) - olc._f64(r)), axis=1)) /
+                       np.max(np.linalg.norm(np.atleast_2d(olc._f64(r)), axis=1)))
+    if np.linalg.norm(olc._f64(r)) else float(np.linalg.norm(olc._f64(g))),
+    lambda g, r: float(np.linalg.norm(olc._f64(g) - olc._f64(r)) / np.linalg.norm(olc._f64(r)))
+    if np.linalg.norm(olc._f64(r)) else 0.0,
+], ids=["den_from_got", "spectral", "max_row_norm", "zero_ref_gives_0"])
+def test_planted_normwise_err_mistakes_are_caught(bad):
+    assert _fails(_pin_normwise, bad)
+
+
+@pytest.mark.parametrize("bad", [
+    lambda H, W, b, rows: olc._f64(H[rows]) @ olc._f64(W).T,                     # bias dropped
+    lambda H, W, b, rows: olc._f64(H)[rows] @ olc._f64(W).T[:, ::-1] +
+    (0 if b is None else olc._f64(b)),                                            # columns reversed
+    lambda H, W, b, rows: olc._f64(H[np.sort(rows)]) @ olc._f64(W).T +
+    (0 if b is None else olc._f64(b)),                                            # rows reordered
+    lambda H, W, b, rows: (olc._f64(W) @ olc._f64(H[rows]).T).T[:, :olc._f64(W).shape[0]] * 1.0 +
+    (0 if b is None else -olc._f64(b)),                                           # bias subtracted
+], ids=["no_bias", "reversed_columns", "sorted_rows", "bias_sign"])
+def test_planted_flce_logits_mistakes_are_caught(bad):
+    assert _fails(_pin_flce_logits, bad)
+
+
+def test_backward_with_forward_returns_the_forward():
+    N, D, V = 33, 7, 301
+    H, W, b, y = _rand(N, D, V, 41, ignore=(0, 9))
+    rows = np.array([1, 4, 9, 30])
+    for kw in ({}, {"rows": rows, "n_valid_total": N - 2}):
+        gr = oracle.flce_backward(H, W, b, y, -100, "sum", 20, with_forward=True, **kw)
+        f = oracle.flce_forward(H, W, b, y, -100, "sum", 20, rows=kw.get("rows"))
+        for k in ("lse", "loss_rows", "label_logit"):
+            np.testing.assert_array_equal(gr["forward"][k], f[k])
+        assert gr["forward"]["loss"] == f["loss"] and gr["forward"]["n_valid"] == f["n_valid"]
+        plain = oracle.flce_backward(H, W, b, y, -100, "sum", 20, **kw)
+        for k in ("grad_H", "grad_W", "grad_b"):
+            np.testing.assert_array_equal(gr[k], plain[k])
