@@ -173,8 +173,11 @@ FLCE_API int flce_mask_packed_labels(int64_t* labels, const int64_t* doc_ids, in
  * or other allocating call is made.
  *
  * The first call on each device looks up the device address of the scratch
- * array (cudaGetSymbolAddress, with that device current) and caches it; make
- * that first call before any stream capture on the device.
+ * array (cudaGetSymbolAddress, with that device current) and caches it with
+ * the id of the current context; make that first call before any stream
+ * capture on the device.  After a cudaDeviceReset (a new primary context) the
+ * next call looks the address up again, in the new context: make that call
+ * before any stream capture as well.
  *
  * All calls share the one array and it keeps the last call's contents (none
  * of which has to be cleared: each call writes every row it later reads).
@@ -306,7 +309,7 @@ FLCE_API int flce_bwd(const void* H, const void* W, const void* bias, int dt, in
  *   5. flce_shard_finish  lse = (m_global + log2 s_global) ln 2, loss rows,
  *                         reduction (identical on every rank)
  * and the backward is flce_bwd_shard with the global lse (the shard's columns
- * of dZ), followed by an all-reduce SUM of the grad_H partials; grad_W and
+ * of dZ), followed by an all-reduce SUM of the fp32 grad_H partials; grad_W and
  * grad_bias stay with their shard.  Workspaces: flce_workspace_bytes(dt, N, D,
  * V_shard, chunk).  The collectives are the caller's (e.g. NCCL). */
 FLCE_API int flce_fwd_shard(const void* H, const void* W_shard, const void* bias_shard, int dt,
@@ -330,7 +333,10 @@ FLCE_API int flce_shard_finish(const float* m_global, const float* s_global,
                                int32_t* status, flce_stream_t stream);
 
 /* Backward of one shard: as flce_bwd over the shard's columns, with the
- * global lse and n_valid; grad_H_partial is this shard's term of grad_H. */
+ * global lse and n_valid; grad_H_partial is this shard's term of grad_H,
+ * written as fp32 [N, D] whatever dt is, so that the ranks' partials are
+ * summed in fp32 and rounded to the input dtype once, after the sum (a sum
+ * of partials already rounded to bf16 would add one rounding per rank). */
 FLCE_API int flce_bwd_shard(const void* H, const void* W_shard, const void* bias_shard, int dt,
                             int64_t N, int64_t D, int64_t V_shard, int64_t vocab_offset,
                             int64_t V_total, const int64_t* labels, int64_t ignore_index,

@@ -1438,25 +1438,70 @@ extern "C" int flce_mask_packed_labels(int64_t* labels, const int64_t* doc_ids, 
 // library holds this array (4 MiB) until the process exits.  All calls share it.
 static __device__ __align__(256) float g_noalloc_rows[CE_LOGITS_NOALLOC_MAX_ROWS];
 
+// The address is cached per device together with the id of the context it was
+// looked up in: after a cudaDeviceReset (or any other end of the device's
+// primary context) the process runs in a new context, whose id differs, and
+// the address is looked up again there.
+struct NoallocAddr {
+  unsigned long long ctx_id = 0;
+  float* ptr = nullptr;
+};
 static std::mutex g_noalloc_mutex;
-static std::vector<float*> g_noalloc_ptr;  // device address of the array, per device id
+static std::vector<NoallocAddr> g_noalloc_addr;  // per device id
+
+typedef CUresult (*NoallocCtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*NoallocCtxGetIdFn)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+static Fn noalloc_driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<Fn>(p);
+  return nullptr;
+}
+
+// Id of the context current on the calling thread (binding the current
+// device's primary context first if none is), 0 if the driver cannot say.
+static int noalloc_context_id(int dev, unsigned long long* id) {
+  static const NoallocCtxGetCurrentFn get =
+      noalloc_driver_fn<NoallocCtxGetCurrentFn>("cuCtxGetCurrent");
+  static const NoallocCtxGetIdFn get_id = noalloc_driver_fn<NoallocCtxGetIdFn>("cuCtxGetId");
+  *id = 0;
+  if (get == nullptr || get_id == nullptr) return FLCE_OK;
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS || ctx == nullptr) {
+    int rc = cuda_status(cudaSetDevice(dev), "cudaSetDevice");
+    if (rc != FLCE_OK) return rc;
+    if (get(&ctx) != CUDA_SUCCESS || ctx == nullptr) return FLCE_OK;
+  }
+  unsigned long long v = 0;
+  if (get_id(ctx, &v) == CUDA_SUCCESS) *id = v;
+  return FLCE_OK;
+}
 
 // Device address of g_noalloc_rows on the current device.  In host code the
-// array's name only stands in for the symbol, so the address is looked up once
-// per device, with that device current, and cached.
+// array's name only stands in for the symbol, so the address is looked up
+// with the device current (once per device and context) and cached.
 static int noalloc_scratch(float** out) {
   int dev = 0;
   int rc = cuda_status(cudaGetDevice(&dev), "cudaGetDevice");
   if (rc != FLCE_OK) return rc;
+  unsigned long long ctx_id = 0;
+  rc = noalloc_context_id(dev, &ctx_id);
+  if (rc != FLCE_OK) return rc;
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (static_cast<int>(g_noalloc_ptr.size()) <= dev) g_noalloc_ptr.resize(dev + 1, nullptr);
-  if (g_noalloc_ptr[dev] == nullptr) {
+  if (static_cast<int>(g_noalloc_addr.size()) <= dev) g_noalloc_addr.resize(dev + 1);
+  NoallocAddr& a = g_noalloc_addr[dev];
+  if (a.ptr == nullptr || a.ctx_id != ctx_id) {
     void* p = nullptr;
     rc = cuda_status(cudaGetSymbolAddress(&p, g_noalloc_rows), "cudaGetSymbolAddress");
     if (rc != FLCE_OK) return rc;
-    g_noalloc_ptr[dev] = static_cast<float*>(p);
+    a.ptr = static_cast<float*>(p);
+    a.ctx_id = ctx_id;
   }
-  *out = g_noalloc_ptr[dev];
+  *out = a.ptr;
   return FLCE_OK;
 }
 

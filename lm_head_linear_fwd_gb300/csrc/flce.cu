@@ -956,17 +956,27 @@ struct FlcePlan {
   size_t total;
 };
 
-// Rows per backward chunk.  The dZ buffer of one chunk is C x ldV elements of
-// the input dtype, kept at or below about 1.25 GiB (and never above 4864 rows);
-// within that, C (a multiple of 128) is chosen so that the grad_H contraction,
-// whose tile count C/128 x D/256 is the smallest of the backward's, fills whole
-// waves of the GPU's SMs over all chunks of N.
+static FlcePlan plan(int dt, int64_t N, int64_t D, int64_t V, int64_t chunk);
+
+// Bytes of extra device memory the default chunk may use: one [2048, V] fp32
+// tile, the transient that Automodel PR #2996 bounds its chunked loss by
+// (first commit message and "Motivation": the fp32 upcast of a chunk is
+// chunk_size x V x 4 bytes).
+static size_t extra_memory_budget(int64_t V) { return static_cast<size_t>(2048) * V * 4; }
+
+// Rows per backward chunk.  The largest multiple of 128 rows (at most 4864)
+// whose workspace, for flce_bwd and for flce_fwd_bwd alike, stays within the
+// budget above (the dZ chunk buffer of C x ldV input elements dominates it)
+// is the cap; within [cap/2, cap], C is chosen so that the grad_H contraction,
+// whose tile count C/128 x D/256 is the smallest of the backward's, fills
+// whole waves of the GPU's SMs over all chunks of N (the largest such C).
+// fp32 inputs also keep transposed operands of D x V floats, which the
+// budget cannot hold at large sizes: their cap falls to 128 rows.
 static int64_t default_chunk(int dt, int64_t N, int64_t D, int64_t V) {
   const int64_t n128 = (N + 127) / 128 * 128;
-  const int64_t ldV = (V + 63) / 64 * 64;
-  const int64_t row_bytes = ldV * static_cast<int64_t>(dtype_size(dt));
-  int64_t cap = std::min<int64_t>(4864, ((5ll << 28) / row_bytes) / 128 * 128);
-  cap = std::max<int64_t>(cap, 128);
+  const size_t budget = extra_memory_budget(V);
+  int64_t cap = std::min<int64_t>(4864, n128);
+  while (cap > 128 && plan(dt, N, D, V, cap).fused_bytes > budget) cap -= 128;
   if (n128 <= cap) return n128;
   const int64_t sms = sm_count();
   const int64_t nNt = (D + 255) / 256;
@@ -1217,11 +1227,16 @@ extern "C" int flce_shard_finish(const float* m_global, const float* s_global,
 
 // Steps 2-4 of a backward chunk, shared by flce_bwd and flce_fwd_bwd: bias
 // column sums, grad_H of the chunk, grad_W accumulation, from the chunk's dZ.
+//
+// grad_H_f32: grad_H_chunk is fp32 whatever the input dtype (the partial of a
+// vocabulary shard, summed over the ranks before one rounding).
 template <typename T>
 static int bwd_tail(const void* W, const T* Hc, int64_t D, int64_t V, int C, bool first_chunk,
                     const FlcePlan& p, char* w, void* grad_H_chunk, float* grad_W,
-                    int accumulate_grad_W, float* grad_bias, int32_t* status, cudaStream_t s) {
+                    int accumulate_grad_W, float* grad_bias, int32_t* status, cudaStream_t s,
+                    bool grad_H_f32 = false) {
   const int dt = sizeof(T) == 2 ? FLCE_BF16 : FLCE_F32;
+  const int dt_h = grad_H_f32 ? FLCE_F32 : dt;
   constexpr bool kTf32 = sizeof(T) == 4;
   T* dz = reinterpret_cast<T*>(w + p.off_dz);
   float* colsum = reinterpret_cast<float*>(w + p.off_colsum);
@@ -1261,15 +1276,29 @@ static int bwd_tail(const void* W, const T* Hc, int64_t D, int64_t V, int C, boo
     if (rc != FLCE_OK) return rc;
     const int64_t n = static_cast<int64_t>(C) * D;
     const int grid = static_cast<int>(std::min<int64_t>((n + 255) / 256, sm_count() * 8));
-    splitk_reduce_kernel<T><<<grid, 256, 0, s>>>(hpart, S, rows * D, C, (int)D,
-                                                 static_cast<T*>(grad_H_chunk));
+    if (grad_H_f32)
+      splitk_reduce_kernel<float><<<grid, 256, 0, s>>>(hpart, S, rows * D, C, (int)D,
+                                                       static_cast<float*>(grad_H_chunk));
+    else
+      splitk_reduce_kernel<T><<<grid, 256, 0, s>>>(hpart, S, rows * D, C, (int)D,
+                                                   static_cast<T*>(grad_H_chunk));
     rc = launch_status("splitk_reduce_kernel launch");
+    if (rc != FLCE_OK) return rc;
+  } else if (grad_H_chunk != nullptr && grad_H_f32 && !kTf32) {
+    // bf16 operands, fp32 output: the split-K partial's epilogue with one split
+    using E = EpiStore<float, false>;
+    typename E::Params ep{C, static_cast<int>(D), 0};
+    const Operand a{dz, C, V, p.ldV, false};
+    const OutDesc o{grad_H_chunk, FLCE_F32, C, D, D};
+    const Operand b{W, D, V, D, true};
+    rc = launch_gemm<T, 256, false, true, E>(kRoleGradH, a, b, &o, C, (int)D, (int)V, 8, ep,
+                                             status, s);
     if (rc != FLCE_OK) return rc;
   } else if (grad_H_chunk != nullptr) {
     using E = EpiStore<T, false>;
     typename E::Params ep{C, static_cast<int>(D), 0};
     const Operand a{dz, C, V, p.ldV, false};
-    const OutDesc o{grad_H_chunk, dt, C, D, D};
+    const OutDesc o{grad_H_chunk, dt_h, C, D, D};
     if (kTf32) {
       const Operand b{Wt, D, V, p.ldVt, false};
       rc = launch_gemm<T, 256, false, false, E>(kRoleGradH, a, b, &o, C, (int)D, (int)V, 8, ep,
@@ -1323,10 +1352,11 @@ static int flce_bwd_impl(const void* H, const void* W, const void* bias, int64_t
                          int64_t num_label_tokens, const float* lse, const int64_t* n_valid,
                          const float* grad_loss, const FlcePlan& p, void* grad_H,
                          float* grad_W, int accumulate_grad_W, float* grad_bias, char* w,
-                         int32_t* status, cudaStream_t s) {
+                         int32_t* status, cudaStream_t s, bool grad_H_f32 = false) {
   const int dt = sizeof(T) == 2 ? FLCE_BF16 : FLCE_F32;
   T* dz = reinterpret_cast<T*>(w + p.off_dz);
   const T* Ht = static_cast<const T*>(H);
+  const size_t h_es = grad_H_f32 ? sizeof(float) : sizeof(T);
   int rc = transpose_W_if_needed<T>(W, D, V, p, w, grad_H, s);
   if (rc != FLCE_OK) return rc;
   for (int64_t r0 = 0; r0 < N; r0 += p.chunk) {
@@ -1344,8 +1374,8 @@ static int flce_bwd_impl(const void* H, const void* W, const void* bias, int64_t
                                                  group_for(D, dt, nMt), ep, status, s);
     if (rc != FLCE_OK) return rc;
     rc = bwd_tail<T>(W, Ht + r0 * D, D, V, C, r0 == 0, p, w,
-                     grad_H != nullptr ? static_cast<T*>(grad_H) + r0 * D : nullptr, grad_W,
-                     accumulate_grad_W, grad_bias, status, s);
+                     grad_H != nullptr ? static_cast<char*>(grad_H) + r0 * D * h_es : nullptr,
+                     grad_W, accumulate_grad_W, grad_bias, status, s, grad_H_f32);
     if (rc != FLCE_OK) return rc;
   }
   return rc;
@@ -1418,7 +1448,7 @@ static int flce_bwd_entry(const void* H, const void* W, const void* bias, int dt
                           int64_t num_label_tokens, const float* lse, const int64_t* n_valid,
                           const float* grad_loss, int64_t chunk, void* grad_H, float* grad_W,
                           int accumulate_grad_W, float* grad_bias, void* ws, size_t ws_bytes,
-                          int32_t* status, flce_stream_t stream) {
+                          int32_t* status, flce_stream_t stream, bool grad_H_f32 = false) {
   int rc = flce_checks(H, W, dt, N, D, V, labels, reduction);
   if (rc != FLCE_OK) return rc;
   if (v0 < 0 || V_total < v0 + V || V_total >= (int64_t(1) << 31)) return FLCE_ESHAPE;
@@ -1446,7 +1476,7 @@ static int flce_bwd_entry(const void* H, const void* W, const void* bias, int dt
     return flce_bwd_impl<__nv_bfloat16>(H, W, bias, N, D, V, v0, V_total, labels, ignore_index,
                                         reduction, num_label_tokens, lse, n_valid, grad_loss, p,
                                         grad_H, grad_W, accumulate_grad_W, grad_bias, w, status,
-                                        s);
+                                        s, grad_H_f32);
   return flce_bwd_impl<float>(H, W, bias, N, D, V, v0, V_total, labels, ignore_index, reduction,
                               num_label_tokens, lse, n_valid, grad_loss, p, grad_H, grad_W,
                               accumulate_grad_W, grad_bias, w, status, s);
@@ -1474,7 +1504,7 @@ extern "C" int flce_bwd_shard(const void* H, const void* W_shard, const void* bi
   return flce_bwd_entry(H, W_shard, bias_shard, dt, N, D, V_shard, vocab_offset, V_total, labels,
                         ignore_index, reduction, num_label_tokens, lse, n_valid, grad_loss,
                         chunk, grad_H_partial, grad_W_shard, accumulate_grad_W, grad_bias_shard,
-                        ws, ws_bytes, status, stream);
+                        ws, ws_bytes, status, stream, /*grad_H_f32=*/true);
 }
 
 extern "C" size_t flce_fwd_bwd_workspace_bytes(int dt, int64_t N, int64_t D, int64_t V,

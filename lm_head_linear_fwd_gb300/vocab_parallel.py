@@ -101,7 +101,8 @@ class CudaShardOps:
         V = W_shard.shape[0]
         dt = _dtype_code(H)
         dev = H.device
-        gH = torch.empty((N, D), dtype=H.dtype, device=dev) if want_grad_H else None
+        # fp32 partial: summed over the ranks before the one rounding to H's dtype
+        gH = torch.empty((N, D), dtype=torch.float32, device=dev) if want_grad_H else None
         gW = torch.empty((V, D), dtype=torch.float32, device=dev) if want_grad_W else None
         gb = torch.empty(V, dtype=torch.float32, device=dev) if bias is not None else None
         ch = 0 if chunk is None else int(chunk)
@@ -191,12 +192,15 @@ def forward(H, W_shard, labels, vocab_offset, V_total, bias_shard=None, *, ignor
 def backward(H, W_shard, labels, vocab_offset, V_total, fwd: ShardForward, grad_loss,
              bias_shard=None, *, ignore_index=-100, reduction="mean", num_label_tokens=None,
              chunk=None, want_grad_H=True, want_grad_W=True, exchange=None, ops=None):
-    """(grad_H summed over the ranks, this shard's fp32 grad_W, its grad_bias)."""
+    """(grad_H summed over the ranks, this shard's fp32 grad_W, its grad_bias).
+
+    The ranks' grad_H partials are fp32; they are summed in fp32 and the sum is
+    rounded once to H's dtype."""
     ops = ops or CudaShardOps()
     exchange = exchange or TorchDistExchange()
     gH, gW, gb = ops.backward(H, W_shard, labels, vocab_offset, V_total, bias_shard, ignore_index,
                               reduction, num_label_tokens, fwd.lse, fwd.n_valid, grad_loss, chunk,
                               want_grad_H, want_grad_W, fwd.status)
     if gH is not None:
-        gH = exchange.sum_(gH)
+        gH = exchange.sum_(gH).to(H.dtype)
     return gH, gW, gb

@@ -61,10 +61,16 @@ def test_workspace_sizes(lib):
     n = _abi.flce_workspace_bytes(0, 8192, 4096, 128256, 0)
     chunk = _abi.flce_default_chunk(0, 8192, 4096, 128256)
     assert chunk % 128 == 0 and 128 <= chunk <= 8192
-    # the dZ chunk buffer (bf16) is at most half of a [chunk, V] fp32 tile,
-    # plus a per-row-and-vocab-tile partial buffer of the forward
+    # the workspace holds the dZ chunk buffer (bf16)
     assert n >= chunk * 128256 * 2
-    assert n <= chunk * 128256 * 4 + 2 * 8192 * ((128256 + 255) // 256) * 4 + (1 << 22)
+    # with the default chunk, the workspaces of the recomputing and of the
+    # one-call path stay within one [2048, V] fp32 tile (bf16 inputs), at the
+    # shapes of the workloads and at a few others
+    for N, D, V in ((8192, 4096, 128256), (65536, 5120, 151936), (2048, 768, 32777),
+                    (256, 128, 1000), (100000, 4096, 50257), (4096, 8192, 262144)):
+        budget = 2048 * V * 4
+        for fn in (_abi.flce_workspace_bytes, _abi.flce_fwd_bwd_workspace_bytes):
+            assert fn(0, N, D, V, 0) <= budget, (fn.__name__, N, D, V)
     assert _abi.flce_workspace_bytes(7, 8, 8, 8, 0) == 0  # bad dtype
 
 

@@ -1,12 +1,11 @@
 """Fused linear cross-entropy: CUDA path through the C ABI vs the fp64 oracle.
 
-Tolerances:
+Tolerances (derived in tests/tolerances.py):
 * loss: |gpu - ref| <= 1e-3 |ref|;
-* per-row lse: |gpu - ref| <= 2e-3 (1 + |ref|) for bf16 inputs (the logits are
-  fp32 accumulations of D products of bf16 values, exact products, so the lse
-  error is the fp32 accumulation error, ~1e-5 here; the bound leaves room)
-  and the same for tf32 (fp32 inputs rounded to 10 mantissa bits:
-  |z| * 2^-11 ~ 1e-4 at |z| ~ 0.3);
+* per-row lse: |gpu - ref| <= 2e-5 (1 + |ref|) for bf16 inputs (fp32
+  accumulation of exact bf16 products; a lost 256-column vocabulary tile moves
+  lse by ~2e-3 at V = 128256, 7x over); for fp32 inputs the fp64 effect of the
+  tf32 operand cut plus that bound; per-row loss twice the lse bound;
 * n_valid exact;
 * grad_H, grad_W, grad_b: max relative <= 2e-2, normwise <= 5e-3 (dZ is rounded
   to the input dtype before the two gradient contractions).
@@ -16,6 +15,7 @@ import pytest
 import torch
 
 import oracle
+import tolerances as tol
 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -33,9 +33,7 @@ def _to(p):
 
 
 def _grad_ok(got, want, name):
-    mr = oracle.max_rel_err(got.float().cpu(), want)
-    nw = oracle.normwise_err(got.float().cpu(), want)
-    assert mr <= 2e-2 and nw <= 5e-3, (name, mr, nw)
+    tol.check_grad(got.float().cpu(), want, name, oracle)
 
 
 def _run(lh, p, chunk=None, g=1.0, accumulate_init=None):
@@ -57,9 +55,10 @@ def _check_all(p, out, bw, g=1.0, grad_W_init=None, W64=None):
     W = p.W if W64 is None else W64
     ref = oracle.flce_forward(p.H, W, p.bias, p.labels, -100, p.reduction, p.num_label_tokens)
     assert int(out.n_valid.item()) == ref["n_valid"]
-    assert abs(out.loss.item() - ref["loss"]) <= 1e-3 * abs(ref["loss"]), (out.loss.item(), ref["loss"])
-    lse = out.lse.cpu().double().numpy()
-    assert np.max(np.abs(lse - ref["lse"]) / (1 + np.abs(ref["lse"]))) <= 2e-3
+    tol.check_loss(out.loss.item(), ref["loss"])
+    tol.check_flce_lse(out.lse, ref["lse"], p.H, W, p.bias)
+    if out.loss_rows is not None:
+        tol.check_flce_loss_rows(out.loss_rows, ref["loss_rows"], ref["lse"], p.H, W)
     gr = oracle.flce_backward(p.H, W, p.bias, p.labels, -100, p.reduction, p.num_label_tokens,
                               grad_loss=g, grad_W_init=grad_W_init)
     _grad_ok(bw.grad_H, gr["grad_H"], "grad_H")
@@ -119,7 +118,9 @@ def test_label_logit_and_rows(lh):
     ref = oracle.flce_forward(p.H, p.W, p.bias, p.labels, -100, "sum")
     zl = out.label_logit.cpu().double().numpy()
     v = p.labels.numpy() != -100
-    assert np.max(np.abs(zl[v] - ref["label_logit"][v])) <= 2e-3
+    # the label logit carries the accumulation error of one logit (the lse bound)
+    assert np.all(np.abs(zl[v] - ref["label_logit"][v]) <=
+                  tol.flce_lse_bound_bf16(ref["label_logit"][v]))
     assert np.all(np.isnan(zl[~v]))
     lr = out.loss_rows.cpu().double().numpy()
     assert np.all(lr[~v] == 0) and np.all(lr >= -1e-4)
@@ -186,9 +187,10 @@ def test_deterministic(lh):
 
 
 def _sampled_full_size(lh, p, n_rows=32, sub_rows=256):
-    """Full-size run (the benchmark's launches) checked on sampled rows and by the
-    row-linearity of grad_W; the complete gradients are then checked on a
-    row subset run as its own problem."""
+    """Full-size run (the benchmark's launches) of a problem too large for the
+    host oracle as a whole, checked on sampled rows and by the row-linearity
+    of grad_W; the complete gradients are then checked on a row subset run as
+    its own problem."""
     H, W, b, y = _to(p)
     out = lh.flce_fwd(H, W, y, b, -100, p.reduction, p.num_label_tokens, want_rows=True)
     one = torch.ones(1, device="cuda")
@@ -204,9 +206,9 @@ def _sampled_full_size(lh, p, n_rows=32, sub_rows=256):
     W64 = p.W.cpu().double().numpy()  # widened once, reused by every oracle call
     ref = oracle.flce_forward(Hc, W64, None, yc, -100, p.reduction, p.num_label_tokens, rows=rows)
     lse = out.lse.cpu().double().numpy()[rows]
-    assert np.max(np.abs(lse - ref["lse"]) / (1 + np.abs(ref["lse"]))) <= 2e-3
+    tol.check_flce_lse(lse, ref["lse"], Hc, W64)
     lr = out.loss_rows.cpu().double().numpy()
-    assert np.max(np.abs(lr[rows] - ref["loss_rows"])) <= 2e-3 * (1 + np.max(ref["loss_rows"]))
+    tol.check_flce_loss_rows(lr[rows], ref["loss_rows"], ref["lse"], Hc, W64)
     total = lr.sum() / (p.num_label_tokens if p.num_label_tokens else 1)
     assert abs(out.loss.item() - total) <= 1e-5 * abs(total)
     gr = oracle.flce_backward(Hc, W64, None, yc, -100, p.reduction, p.num_label_tokens, rows=rows,
@@ -229,10 +231,50 @@ def _sampled_full_size(lh, p, n_rows=32, sub_rows=256):
     _check_all(q, out_s, bw_s, W64=W64)
 
 
-def test_llama3_8b_workload_sampled(lh):
-    """N=8192, D=4096, V=128256 bf16, Zipf labels, 3% ignored, sum / num_label_tokens."""
+def test_llama3_8b_workload_against_the_full_oracle(lh):
+    """N=8192, D=4096, V=128256 bf16, Zipf labels, 3% ignored, sum / num_label_tokens,
+    in the launch configuration the benchmark times (default chunk): every row's
+    lse and loss, the loss, and all of grad_H and grad_W against the fp64 oracle
+    over the whole problem (8NDV = 3.4e13 fp64 flops on the host cores, one to
+    two minutes).  grad_W is also checked by its row-linearity (a full run
+    equals two half runs accumulated)."""
     p = wl.llama3_8b_flce(device="cuda")
-    _sampled_full_size(lh, p)
+    H, W, b, y = _to(p)
+    out = lh.flce_fwd(H, W, y, b, -100, p.reduction, p.num_label_tokens, want_rows=True)
+    one = torch.ones(1, device="cuda")
+    bw = lh.flce_bwd(H, W, y, out.lse, out.n_valid, one, b, -100, p.reduction,
+                     p.num_label_tokens)
+    torch.cuda.synchronize()
+    lh.check_status(out.status)
+    gH, gW = bw.grad_H.cpu(), bw.grad_W.cpu()
+    lse, rows, loss = out.lse.cpu(), out.loss_rows.cpu(), out.loss.item()
+    # row-linearity of grad_W on the device, before the host copies are compared
+    half = (p.N // 2) // 128 * 128
+    gW2 = torch.zeros_like(bw.grad_W)
+    for r0, r1, acc in ((0, half, False), (half, p.N, True)):
+        lh.flce_bwd(H[r0:r1], W, y[r0:r1], out.lse[r0:r1], out.n_valid, one, None, -100,
+                    p.reduction, p.num_label_tokens, want_grad_H=False, grad_W=gW2,
+                    accumulate_grad_W=acc)
+    torch.cuda.synchronize()
+    assert oracle.normwise_err(gW2.cpu(), gW.double().numpy()) <= 1e-5
+    nv = int(out.n_valid.item())
+    Hc, yc, Wc = p.H.cpu(), p.labels.cpu(), p.W.cpu()
+    del H, W, y, bw, out, gW2, p
+    torch.cuda.empty_cache()
+    W64 = Wc.double().numpy()
+    del Wc
+    gr = oracle.flce_backward(Hc, W64, None, yc, -100, "sum", nv, with_forward=True)
+    ref = gr["forward"]
+    assert nv == ref["n_valid"]
+    tol.check_loss(loss, ref["loss"])
+    tol.check_flce_lse(lse, ref["lse"], Hc, W64)
+    tol.check_flce_loss_rows(rows, ref["loss_rows"], ref["lse"], Hc, W64)
+    # the loss is the sum of the rows: within the sum of their bounds
+    row_bound = 2.0 * tol.flce_lse_bound_bf16(ref["lse"])
+    assert abs(loss - ref["loss"]) <= row_bound[ref["loss_rows"] != 0].sum() / nv
+    _grad_ok(gH, gr["grad_H"], "grad_H")
+    del gr["grad_H"]
+    _grad_ok(gW, gr["grad_W"], "grad_W")
 
 
 def test_long_packed_workload_sampled(lh):

@@ -1,12 +1,16 @@
 """Seeded random shapes for both paths (recomputing and fused FLCE, CE on
 logits) against the fp64 oracle: sizes drawn across tile, chunk and vector
 boundaries, random dtype, bias, reduction and chunk.  Tolerances as in
-tests/test_gpu_flce.py and tests/test_gpu_ce_logits.py."""
+tests/test_gpu_flce.py and tests/test_gpu_ce_logits.py (tests/tolerances.py):
+the per-row lse of both FLCE paths is held to 2e-5 (1 + |lse|) for bf16, so a
+lost 256-column vocabulary tile fails, also at the large vocabularies of the
+third draw."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
+import tolerances as tol
 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -43,6 +47,22 @@ for i in range(8):
         seed=2000 + i))
 
 
+# a third draw: vocabularies of 1.2e5 to 1.6e5 words (470 to 625 tiles of 256
+# columns, the range of the Llama3-8B and long packed heads), few rows
+_rng3 = np.random.default_rng(128256)
+for i in range(4):
+    CASES.append(dict(
+        N=int(_rng3.integers(1, 400)),
+        D=int(_rng3.integers(1, 24)) * 8,
+        V=int(_rng3.integers(120000, 160000)),
+        dtype=torch.bfloat16 if i < 3 else torch.float32,
+        bias=bool(i % 2),
+        reduction=str(_rng3.choice(["sum", "mean"])),
+        nlt=None,
+        chunk=None if i % 2 else 128,
+        seed=3000 + i))
+
+
 def _grad_ok(got, want, name):
     mr = oracle.max_rel_err(got.float().cpu(), want)
     nw = oracle.normwise_err(got.float().cpu(), want)
@@ -69,6 +89,8 @@ def test_flce_random_shape(case):
     for o in (out, fo):
         assert int(o.n_valid.item()) == ref["n_valid"]
         assert abs(o.loss.item() - ref["loss"]) <= 1e-3 * abs(ref["loss"]) + 1e-6
+    tol.check_flce_lse(out.lse, ref["lse"], p.H, p.W, p.bias, what="lse (flce_fwd)")
+    tol.check_flce_lse(fo.lse, ref["lse"], p.H, p.W, p.bias, what="lse (flce_fwd_bwd)")
     if ref["loss"] == 0.0:
         return
     for g in (bw, fb):

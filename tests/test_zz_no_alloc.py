@@ -9,13 +9,14 @@ has already run every other test; it also passes when run alone.
 
 Two calls in a row on different problems (the second smaller, so stale rows of
 the first stay in the shared array) must each match the workspace entry point
-within the tolerances of the other CE tests: loss 1e-3 relative, per-row lse
-5e-5 (1 + |lse|), n_valid exact.
+and the fp64 oracle within the tolerances of the other CE tests: loss 1e-3
+relative, per-row lse 5e-5 (1 + |lse|), n_valid exact.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -56,6 +57,10 @@ def test_noalloc_matches_workspace_entry_point():
         a = lse.cpu().double().numpy()
         b = ref.lse.cpu().double().numpy()
         assert np.all(np.abs(a - b) <= 5e-5 * (1 + np.abs(b)))
+        want = oracle.ce_forward(p.logits, p.labels, -100, red)
+        assert int(n_valid.item()) == want["n_valid"]
+        assert abs(loss.item() - want["loss"]) <= 1e-3 * abs(want["loss"])
+        assert np.all(np.abs(a - want["lse"]) <= 5e-5 * (1 + np.abs(want["lse"])))
 
 
 def test_noalloc_rejects_too_many_rows():
