@@ -22,8 +22,9 @@
 // fp32 the MN-major operands of steps 3 and 4 are first transposed into the
 // workspace (W once per call, dZ and H[chunk] once per chunk).  When a chunk
 // has too few grad_H tiles to fill the GPU, step 3 splits its long K (= V)
-// and reduces the fp32 partials in a fixed order.  grad_W runs on CTA pairs
-// (tc_gemm_pair_kernel) by default; flce_gemm_set_pair selects per contraction.
+// and reduces the fp32 partials in a fixed order.  The dZ recompute and grad_W
+// run on CTA pairs (tc_gemm_pair_kernel) by default; flce_gemm_set_pair
+// selects per contraction.
 //
 // Also here: the fused forward + backward (flce_fwd_bwd: the forward epilogue
 // keeps the chunk's logits as offsets from each tile's maximum, dZ is formed
@@ -811,7 +812,7 @@ struct OutDesc {
 // Which bf16 contractions run on CTA pairs (tc_gemm_pair_kernel) instead of one
 // CTA per tile: a bit mask of GemmRole.
 enum GemmRole : int { kRoleFwd = 1, kRoleDz = 2, kRoleGradH = 4, kRoleGradW = 8, kRoleRaw = 16 };
-static std::atomic<int> g_pair_mask{kRoleGradW | kRoleRaw};
+static std::atomic<int> g_pair_mask{kRoleDz | kRoleGradW | kRoleRaw};
 
 template <int BN, bool A_MN, bool B_MN, class Epi>
 static int launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
