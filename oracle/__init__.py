@@ -4,6 +4,6 @@ Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
 may import this package.  It shares no code with ``lm_head_linear_fwd_gb300``.
 """
 from .lm_head_ce import (  # noqa: F401
-    ce_backward, ce_forward, divisor, flce_backward, flce_forward, flce_logits,
-    logsumexp_rows, max_rel_err, normwise_err, scale, valid_rows,
+    BlockwiseError, ce_backward, ce_forward, divisor, flce_backward, flce_forward, flce_logits,
+    logsumexp_rows, max_rel_err, normwise_err, packed_document_labels, scale, valid_rows,
 )

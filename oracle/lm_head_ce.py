@@ -274,3 +274,56 @@ def normwise_err(got, ref):
     if den == 0.0:
         return float(num)
     return float(num / den)
+
+
+class BlockwiseError:
+    """max_rel_err and normwise_err of a tensor compared block by block (rows
+    of a tensor too large to hold in float64 at once): the running
+    max|got - ref|, max|ref|, sum (got - ref)^2 and sum ref^2 over the blocks
+    give the same two numbers as the whole-tensor functions above."""
+
+    def __init__(self):
+        self.max_diff = 0.0
+        self.max_ref = 0.0
+        self.sq_diff = 0.0
+        self.sq_ref = 0.0
+
+    def add(self, got, ref):
+        got = _f64(got)
+        ref = _f64(ref)
+        if ref.size == 0:
+            return
+        d = got - ref
+        self.max_diff = max(self.max_diff, float(np.max(np.abs(d))))
+        self.max_ref = max(self.max_ref, float(np.max(np.abs(ref))))
+        self.sq_diff += float(np.sum(d * d))
+        self.sq_ref += float(np.sum(ref * ref))
+
+    def max_rel(self):
+        return self.max_diff if self.max_ref == 0.0 else self.max_diff / self.max_ref
+
+    def normwise(self):
+        num = float(np.sqrt(self.sq_diff))
+        den = float(np.sqrt(self.sq_ref))
+        return num if den == 0.0 else num / den
+
+
+# ----------------------------------------------------- packed-document label masking
+
+def packed_document_labels(labels, doc_ids, ignore_index=-100):
+    """Labels of packed sequences with the tokens that have no target ignored.
+
+    Automodel PR #2996, "Summary" (packing-mask fix): an indexed packing mask
+    holds 1, 2, ... for the packed documents of a row and 0 for padding.  A
+    padding token has no label; neither has the last token of a document,
+    whose next token starts another document (or the padding, or lies past
+    the row).  labels and doc_ids are [B, T]; returns a new int64 [B, T]."""
+    y = _i64(labels).copy()
+    d = _i64(doc_ids)
+    B, T = d.shape
+    for r in range(B):
+        for t in range(T):
+            last = t == T - 1 or d[r, t + 1] != d[r, t]
+            if d[r, t] == 0 or last:
+                y[r, t] = ignore_index
+    return y

@@ -1,6 +1,7 @@
 """Data-parallel sharding with the CUDA kernels on one GPU: shards run one
 after the other with the global valid count as num_label_tokens; their losses
 and gradients must add up to the single-call mean."""
+import numpy as np
 import pytest
 import torch
 
@@ -41,25 +42,27 @@ def test_shards_add_up_to_the_global_mean():
     assert oracle.normwise_err(gW.cpu(), full_b.grad_W.cpu().double().numpy()) <= 1e-5
 
 
-def test_mask_packed_labels_matches_the_workload_recipe():
-    """The kernel reproduces the long packed workload's masking: padding tail
-    and last token of each document ignored."""
+def test_mask_packed_labels_matches_the_oracle():
+    """The kernel against the oracle's packed-document masking (padding and the
+    last token of each document ignored), bit-exact, on rows laid out like the
+    long packed workload (a padding tail, four documents at random cuts) and
+    on rows with padding first, one-token documents and no padding."""
     import lm_head_linear_fwd_gb300 as lh
     B, T, V = 4, 4096, 151936
     doc = torch.zeros(B, T, dtype=torch.int64)
     rng = torch.Generator().manual_seed(7)
     pad = 327
-    ref = torch.randint(0, V, (B, T), generator=rng)
-    labels = ref.clone()
+    labels = torch.randint(0, V, (B, T), generator=rng)
     for r in range(B):
         cuts = sorted((torch.randperm(T - pad - 2, generator=rng)[:3] + 1).tolist())
-        ends = cuts + [T - pad]
         start = 0
-        for k, e in enumerate(ends):
+        for k, e in enumerate(cuts + [T - pad]):
             doc[r, start:e] = k + 1
-            ref[r, e - 1] = -100
             start = e
-        ref[r, T - pad:] = -100
-    out = lh.mask_packed_labels(labels.cuda(), doc.cuda())
-    torch.cuda.synchronize()
-    assert torch.equal(out.cpu(), ref)
+    doc2 = torch.tensor([[0, 0, 1, 2, 2, 3, 4, 4], [5, 5, 5, 5, 5, 5, 5, 5]], dtype=torch.int64)
+    labels2 = torch.randint(0, V, (2, 8), generator=rng)
+    for d, y in ((doc, labels), (doc2, labels2)):
+        out = lh.mask_packed_labels(y.cuda(), d.cuda())
+        torch.cuda.synchronize()
+        want = oracle.packed_document_labels(y, d)
+        assert np.array_equal(out.cpu().numpy(), want)

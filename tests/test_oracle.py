@@ -494,3 +494,68 @@ def test_backward_with_forward_returns_the_forward():
         plain = oracle.flce_backward(H, W, b, y, -100, "sum", 20, **kw)
         for k in ("grad_H", "grad_W", "grad_b"):
             np.testing.assert_array_equal(gr[k], plain[k])
+
+
+def _blockwise(blocks_got, blocks_ref):
+    acc = oracle.BlockwiseError()
+    for g, r in zip(blocks_got, blocks_ref):
+        acc.add(g, r)
+    return acc
+
+
+def test_blockwise_error_hand_values():
+    # ref = [[3, 0], [0, 4]] in two row blocks; got - ref = [[0, 0], [0, 1]]:
+    # max|diff| = 1, max|ref| = 4 -> 0.25; ||diff|| = 1, ||ref|| = 5 -> 0.2
+    acc = _blockwise([np.array([[3.0, 0.0]]), np.array([[0.0, 5.0]])],
+                     [np.array([[3.0, 0.0]]), np.array([[0.0, 4.0]])])
+    assert acc.max_rel() == pytest.approx(0.25, abs=1e-15)
+    assert acc.normwise() == pytest.approx(0.2, abs=1e-15)
+    # zero reference: the absolute errors, max 0.5 and norm sqrt(0.5^2 + 1.2^2) = 1.3
+    acc = _blockwise([np.array([0.5]), np.array([-1.2])], [np.zeros(1), np.zeros(1)])
+    assert acc.max_rel() == pytest.approx(1.2, abs=1e-15)
+    assert acc.normwise() == pytest.approx(1.3, abs=1e-15)
+    # an empty block changes nothing
+    acc.add(np.zeros((0, 3)), np.zeros((0, 3)))
+    assert acc.normwise() == pytest.approx(1.3, abs=1e-15)
+
+
+def test_blockwise_error_equals_the_whole_tensor_functions():
+    rng = np.random.default_rng(12)
+    ref = rng.standard_normal((37, 11))
+    got = ref + rng.standard_normal((37, 11)) * 1e-3
+    acc = _blockwise([got[a:a + 8] for a in range(0, 37, 8)], [ref[a:a + 8] for a in range(0, 37, 8)])
+    assert acc.max_rel() == pytest.approx(oracle.max_rel_err(got, ref), rel=1e-14)
+    assert acc.normwise() == pytest.approx(oracle.normwise_err(got, ref), rel=1e-12)
+
+
+_PACK_DOC = np.array([[1, 1, 1, 2, 2, 0, 0],
+                      [1, 1, 1, 1, 1, 1, 1],
+                      [0, 1, 2, 2, 2, 2, 2]])
+# row 0: documents 1 (t 0-2) and 2 (t 3-4), then padding (t 5-6)
+# row 1: one document over the whole row
+# row 2: padding first (t 0), a one-token document (t 1), document 2 (t 2-6)
+_PACK_WANT = np.array([[100, 101, -100, 103, -100, -100, -100],
+                       [107, 108, 109, 110, 111, 112, -100],
+                       [-100, -100, 116, 117, 118, 119, -100]])
+
+
+def _check_packed(fn):
+    y = np.arange(21).reshape(3, 7) + 100
+    np.testing.assert_array_equal(fn(y, _PACK_DOC), _PACK_WANT)
+    np.testing.assert_array_equal(y, np.arange(21).reshape(3, 7) + 100)  # input unchanged
+
+
+def test_packed_document_labels_hand_values():
+    _check_packed(oracle.packed_document_labels)
+    y = np.arange(21).reshape(3, 7) + 100
+    assert oracle.packed_document_labels(y, _PACK_DOC, ignore_index=-1)[0, 2] == -1
+
+
+@pytest.mark.parametrize("bad", [
+    lambda y, d: np.where(d == 0, -100, y),                                        # ends kept
+    lambda y, d: np.where((d == 0) | (np.roll(d, 1, axis=1) != d), -100, y),       # first tokens
+    lambda y, d: np.where(np.roll(d, -1, axis=1) != d, -100, y),                   # padding kept
+], ids=["document_ends_kept", "first_tokens_dropped", "padding_kept"])
+def test_planted_packed_label_mistakes_are_caught(bad):
+    with pytest.raises(AssertionError):
+        _check_packed(bad)
