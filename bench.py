@@ -48,7 +48,7 @@ TRAFFIC = {
                   "files": ["ce_logits.cu", "common.cuh", "host.h"]},
     # profiles/flce_llama3_8b_kernel_traffic.md: the ten GEMM launches of one
     # step (forward; dZ, grad_H, grad_W of chunks of 3584, 3584 and 1024 rows)
-    "flce": {"bytes_per_step": 32.31e9, "sha": "f88daf40cce25f33",
+    "flce": {"bytes_per_step": 32.31e9, "sha": "98f3f30cdd6502b8",
              "files": ["flce.cu", "tc_gemm.cuh", "common.cuh", "host.h"]},
 }
 
@@ -285,8 +285,14 @@ def run_ours(args, rank, ws, local):
     flops = 8.0 * N * D * V
     tflops = flops / (flce_ms * 1e-3) / 1e12
     tok_s = N * ws / (flce_ms * 1e-3)
-    n_chunks = (N + chunk - 1) // chunk
-    launches_flce = 3 + n_chunks * (3 + (2 if b is not None else 0))
+    if chunk > 0:   # row chunks: dZ, grad_H, grad_W (+ 2 bias kernels) per chunk
+        n_chunks = (N + chunk - 1) // chunk
+        launches_flce = 3 + n_chunks * (3 + (2 if b is not None else 0))
+        split = f"chunk={chunk}"
+    else:           # vocabulary slices, then one rounding of the fp32 grad_H
+        n_chunks = (V + (-chunk) - 1) // (-chunk)
+        launches_flce = 3 + n_chunks * (3 + (2 if b is not None else 0)) + 1
+        split = f"vocabulary slices of {-chunk} columns"
     if args.only == "flce-step":
         # profiling runs: the timed FLCE step alone, nothing else held on the device
         if rank == 0:
@@ -294,7 +300,7 @@ def run_ours(args, rank, ws, local):
                               "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
                               "ms_per_step": round(flce_ms, 4),
                               "config": {"workload": f"FLCE step only {args.workload} N={N} "
-                                                     f"D={D} V={V}, chunk={chunk}"},
+                                                     f"D={D} V={V}, {split}"},
                               "flce_tflops_8NDV": round(tflops, 2), "fwd_ms": round(fwd_avg, 4),
                               "peak_extra_gib": round(peak_extra / 2**30, 4), "clocks": clocks,
                               "note": "profiling run: FLCE step only"}))
@@ -509,7 +515,7 @@ def run_ours(args, rank, ws, local):
         "dtype": "bf16",
         "data": "synthetic (seeded; random-init weights of the workload's shape)",
         "config": {
-            "workload": (f"FLCE fwd+bwd {args.workload}: N={N} D={D} V={V} bf16, chunk={chunk} "
+            "workload": (f"FLCE fwd+bwd {args.workload}: N={N} D={D} V={V} bf16, {split} "
                          "(value and ms_per_step); CE on given logits [16384,128256] bf16 "
                          "fwd + in-place bwd timed on its own (ce_logits)"),
             "global_batch": N * ws,
@@ -926,7 +932,8 @@ def main():
     ap.add_argument("--only", choices=["all", "flce", "flce-step", "ce"], default="all",
                     help="run one part only (profiling runs)")
     ap.add_argument("--chunk", type=int, default=0,
-                    help="rows per FLCE backward chunk (default: the library's choice)")
+                    help="FLCE backward split: rows per chunk, or minus the columns of each "
+                         "vocabulary slice (default: the library's row chunk)")
     ap.add_argument("--ce-rows", type=int, default=16384,
                     help="rows of the given-logits workload (smaller cases for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

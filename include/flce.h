@@ -252,12 +252,22 @@ FLCE_API int ce_logits_fwd_bwd(const void* logits, int dt, int64_t N, int64_t V,
 /* ------------------------------------------------------------------------ */
 
 /* Bytes of device workspace for flce_fwd and flce_bwd with these sizes.
- * `chunk` is the number of rows the backward processes per step (<= 0 picks
- * the library default, flce_default_chunk).  The same workspace serves both
- * calls. */
+ * `chunk` says how the backward splits its work: chunk > 0, row chunks of
+ * that many rows (a multiple of 128 unless it covers all N); chunk < 0
+ * (bf16 only), slices of -chunk vocabulary columns (a multiple of 256) over
+ * all rows at once; chunk == 0, the library default (flce_default_chunk).
+ * The same workspace serves both calls.  With the default, the workspace
+ * stays within one [2048, V] fp32 tile (2048 * V * 4 bytes) for bf16 inputs:
+ * the fp32 transient Automodel PR #2996 ("Motivation") bounds its chunked
+ * loss by. */
 FLCE_API size_t flce_workspace_bytes(int dt, int64_t N, int64_t D, int64_t V, int64_t chunk);
 
-/* Row chunk the backward uses when `chunk` <= 0 is passed. */
+/* Row chunk the backward uses when chunk == 0 is passed (0 for invalid
+ * sizes).  Row chunks read and write the fp32 grad_W once more per chunk
+ * after the first; vocabulary slices (a negative chunk) write grad_W once and
+ * accumulate an fp32 [N, D] grad_H in the workspace instead (one rounding to
+ * dt at the end), at the cost of grad_W summed in one tensor-core sweep over
+ * all N rows. */
 FLCE_API int64_t flce_default_chunk(int dt, int64_t N, int64_t D, int64_t V);
 
 /* Forward.  H: [N, D], W: [V, D] (row v is the embedding of token v), bias:
@@ -283,9 +293,11 @@ FLCE_API int flce_fwd(const void* H, const void* W, const void* bias, int dt, in
  *   grad_W    [V, D] f32           = dZ^T H, added to the existing contents if
  *                                    accumulate_grad_W != 0 (addmm beta = 1)
  *   grad_bias [V]    f32           = sum over rows of dZ (overwritten)
- * dZ is formed per row chunk in fp32 and rounded to dt before the two
- * gradient contractions.  chunk <= 0 picks flce_default_chunk; the workspace
- * must have been sized with the same chunk. */
+ * dZ is formed per row chunk (or vocabulary slice) in fp32 and rounded to dt
+ * before the two gradient contractions.  chunk as in flce_workspace_bytes
+ * (0: flce_default_chunk); the workspace must have been sized with the same
+ * chunk.  A negative chunk with fp32 inputs returns FLCE_ENOSUP, one that is
+ * not a multiple of 256 FLCE_ESHAPE. */
 FLCE_API int flce_bwd(const void* H, const void* W, const void* bias, int dt, int64_t N, int64_t D,
              int64_t V, const int64_t* labels, int64_t ignore_index, int reduction,
              int64_t num_label_tokens, const float* lse, const int64_t* n_valid,
@@ -370,7 +382,10 @@ FLCE_API int ce_logits_bwd_shard(const void* logits_shard, int dt, int64_t N, in
 /* Fused linear cross-entropy, forward and backward in one call             */
 /* ------------------------------------------------------------------------ */
 
-/* Workspace bytes for flce_fwd_bwd (same chunk rule as flce_workspace_bytes). */
+/* Workspace bytes for flce_fwd_bwd.  chunk > 0: rows per chunk as for
+ * flce_workspace_bytes; chunk <= 0 (a negative value included): the row chunk
+ * of the library default.  The one-call path always chunks rows: each chunk's
+ * lse must be complete before its gradient is formed. */
 FLCE_API size_t flce_fwd_bwd_workspace_bytes(int dt, int64_t N, int64_t D, int64_t V,
                                              int64_t chunk);
 

@@ -335,12 +335,14 @@ def mask_packed_labels(labels: torch.Tensor, doc_ids: torch.Tensor, ignore_index
 # ---------------------------------------------------------- fused linear CE
 
 def flce_workspace_bytes(dt_code: int, N: int, D: int, V: int, chunk: int = 0) -> int:
-    """Bytes of device workspace flce_fwd / flce_bwd need (chunk 0: the default)."""
+    """Bytes of device workspace flce_fwd / flce_bwd need (chunk 0: the default;
+    chunk > 0: rows per backward chunk; chunk < 0: vocabulary slices of -chunk
+    columns)."""
     return int(_abi.flce_workspace_bytes(dt_code, N, D, V, chunk))
 
 
 def flce_default_chunk(dt_code: int, N: int, D: int, V: int) -> int:
-    """Rows per backward chunk when none is given (sizes the dZ buffer)."""
+    """Rows per backward chunk when no chunk is given (sizes the dZ buffer)."""
     return int(_abi.flce_default_chunk(dt_code, N, D, V))
 
 

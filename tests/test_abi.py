@@ -63,6 +63,15 @@ def test_workspace_sizes(lib):
     assert chunk % 128 == 0 and 128 <= chunk <= 8192
     # the workspace holds the dZ chunk buffer (bf16)
     assert n >= chunk * 128256 * 2
+    # explicit row chunks and vocabulary slices size their own workspaces: a
+    # slice holds the dZ of all rows for its columns and the fp32 grad_H
+    assert _abi.flce_workspace_bytes(0, 8192, 4096, 128256, 4096) >= 4096 * 128256 * 2
+    assert _abi.flce_workspace_bytes(0, 8192, 4096, 128256, -256) >= 8192 * 256 * 2 + 8192 * 4096 * 4
+    # the one-call path always chunks rows: a negative chunk means its default
+    assert (_abi.flce_fwd_bwd_workspace_bytes(0, 8192, 4096, 128256, -256) ==
+            _abi.flce_fwd_bwd_workspace_bytes(0, 8192, 4096, 128256, 0))
+    assert _abi.flce_default_chunk(0, 2048, 768, 32777) == 2048
+    assert _abi.flce_default_chunk(7, 8, 8, 8) == 0
     # with the default chunk, the workspaces of the recomputing and of the
     # one-call path stay within one [2048, V] fp32 tile (bf16 inputs), at the
     # shapes of the workloads and at a few others
@@ -178,6 +187,12 @@ def test_flce_rejects_bad_arguments(lib):
     b3 = list(bb)
     b3[17] = 2
     assert _abi.flce_bwd(*b3) == -1
+    b4 = list(bb)
+    b4[14] = -300                    # vocabulary slice not a multiple of 256
+    assert _abi.flce_bwd(*b4) == -2
+    b5 = list(bb)
+    b5[3], b5[14] = 1, -256          # vocabulary slices with fp32 inputs
+    assert _abi.flce_bwd(*b5) == -8
 
 
 @no_gpu

@@ -281,3 +281,62 @@ def test_long_packed_workload_sampled(lh):
     """N=65536 (4 x 16384 packed), D=5120, V=151936 bf16, ~8% ignored, sum."""
     p = wl.long_packed_flce(device="cuda")
     _sampled_full_size(lh, p, n_rows=16, sub_rows=128)
+
+
+@pytest.mark.parametrize("pair", [31, 0], ids=["pair", "single"])
+@pytest.mark.parametrize("N,D,V,vslice,bias,reduction", [
+    (700, 256, 3001, 1024, True, "mean"),    # three slices, the last 953 columns
+    (1000, 520, 2048, 256, False, "sum"),    # eight slices of one tile each
+    (129, 64, 777, 512, True, "sum"),        # a ragged row tile and a ragged slice
+    (300, 128, 20000, 20224, False, "mean"),  # one slice wider than V
+])
+def test_vocabulary_slices(lh, N, D, V, vslice, bias, reduction, pair):
+    """The backward split over vocabulary slices (chunk = -columns): all rows
+    per slice, grad_W written slice by slice, grad_H accumulated in fp32 and
+    rounded once, bias columns per slice."""
+    from lm_head_linear_fwd_gb300 import _abi
+    prev = _abi.flce_gemm_set_pair(pair)
+    try:
+        p = wl.random_flce(N, D, V, torch.bfloat16, bias=bias, seed=N + 7, reduction=reduction)
+        out, bw = _run(lh, p, chunk=-vslice, g=0.75)
+        _check_all(p, out, bw, g=0.75)
+    finally:
+        _abi.flce_gemm_set_pair(prev)
+
+
+def test_vocabulary_slices_accumulate_grad_W(lh):
+    p = wl.random_flce(256, 128, 1000, torch.bfloat16, seed=43)
+    init = torch.randn(1000, 128) * 0.01
+    out, bw = _run(lh, p, chunk=-256, accumulate_init=init)
+    _check_all(p, out, bw, grad_W_init=init.double().numpy())
+
+
+def test_vocabulary_slices_match_row_chunks(lh):
+    """Both splits of the same backward: the same dZ values feed the same
+    contractions, in another order of fp32 additions for grad_H (slices) and
+    grad_W (chunks): the gradients agree to fp32 summation order plus one bf16
+    rounding of grad_H."""
+    p = wl.random_flce(1536, 256, 6000, torch.bfloat16, bias=True, seed=5, reduction="mean")
+    H, W, b, y = _to(p)
+    out = lh.flce_fwd(H, W, y, b, -100, "mean")
+    g = torch.ones(1, device="cuda")
+    rows = lh.flce_bwd(H, W, y, out.lse, out.n_valid, g, b, -100, "mean", None, 512)
+    sl = lh.flce_bwd(H, W, y, out.lse, out.n_valid, g, b, -100, "mean", None, -1536)
+    torch.cuda.synchronize()
+    lh.check_status(out.status)
+    # fp32 sums of 1536 products in another order (one tensor-core sweep
+    # against three of 512 added in L2): ~1e-6, the bound of the row-linearity
+    # checks
+    assert oracle.normwise_err(sl.grad_W.cpu(), rows.grad_W.cpu().double().numpy()) <= 1e-5
+    assert oracle.normwise_err(sl.grad_bias.cpu(), rows.grad_bias.cpu().double().numpy()) <= 1e-5
+    assert oracle.normwise_err(sl.grad_H.float().cpu(),
+                               rows.grad_H.float().cpu().double().numpy()) <= 4e-3
+
+
+def test_vocabulary_slices_rejected_for_fp32(lh):
+    p = wl.random_flce(64, 64, 300, torch.float32, seed=8)
+    H, W, b, y = _to(p)
+    out = lh.flce_fwd(H, W, y, b)
+    with pytest.raises(lh.FlceError):
+        lh.flce_bwd(H, W, y, out.lse, out.n_valid, torch.ones(1, device="cuda"), b, -100, "sum",
+                    None, -256)

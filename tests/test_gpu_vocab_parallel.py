@@ -20,10 +20,13 @@ def _grad_ok(got, want, name):
     assert mr <= 2e-2 and nw <= 5e-3, (name, mr, nw)
 
 
-@pytest.mark.parametrize("reduction,nlt,bias,dtype", [("mean", None, True, torch.bfloat16),
-                                                      ("sum", 900, False, torch.bfloat16),
-                                                      ("sum", None, True, torch.float32)])
-def test_three_vocab_shards_match_the_oracle(reduction, nlt, bias, dtype):
+@pytest.mark.parametrize("reduction,nlt,bias,dtype,chunk", [
+    ("mean", None, True, torch.bfloat16, None),
+    ("sum", 900, False, torch.bfloat16, None),
+    ("sum", None, True, torch.float32, None),
+    ("mean", None, True, torch.bfloat16, -512),   # each shard's backward in vocabulary slices
+])
+def test_three_vocab_shards_match_the_oracle(reduction, nlt, bias, dtype, chunk):
     import lm_head_linear_fwd_gb300 as lh
     from lm_head_linear_fwd_gb300 import vocab_parallel as vp
     p = wl.random_flce(1000, 128, 3001, dtype, bias=bias, seed=21, reduction=reduction,
@@ -43,7 +46,7 @@ def test_three_vocab_shards_match_the_oracle(reduction, nlt, bias, dtype):
     lse, loss, n_valid = ops.finish(m_g, s_g, zy_g, y, V, -100, reduction, nlt, st)
     g = torch.ones(1, device="cuda")
     grads = [ops.backward(H, W[a:c], y, a, V, None if b is None else b[a:c], -100, reduction, nlt,
-                          lse, n_valid, g, None, True, True, st) for a, c in bounds]
+                          lse, n_valid, g, chunk, True, True, st) for a, c in bounds]
     gH = torch.stack([q[0].float() for q in grads]).sum(0)                # all-reduce SUM
     gW = torch.cat([q[1] for q in grads])
     torch.cuda.synchronize()
