@@ -258,8 +258,9 @@ FLCE_API int ce_logits_fwd_bwd(const void* logits, int dt, int64_t N, int64_t V,
  * all rows at once; chunk == 0, the library default (flce_default_chunk).
  * The same workspace serves both calls.  With the default, the workspace
  * stays within one [2048, V] fp32 tile (2048 * V * 4 bytes) for bf16 inputs:
- * the fp32 transient Automodel PR #2996 ("Motivation") bounds its chunked
- * loss by. */
+ * Automodel PR #2996 ("Motivation") bounds the fp32 transient of its chunked
+ * loss by chunk_size * V * 4 bytes, and the chunk of that bound is fixed here
+ * at 2048 rows. */
 FLCE_API size_t flce_workspace_bytes(int dt, int64_t N, int64_t D, int64_t V, int64_t chunk);
 
 /* Row chunk the backward uses when chunk == 0 is passed (0 for invalid

@@ -966,9 +966,9 @@ static FlcePlan plan(int dt, int64_t N, int64_t D, int64_t V, int64_t chunk,
                      bool bwd_split = false);
 
 // Bytes of extra device memory the default chunk may use: one [2048, V] fp32
-// tile, the transient that Automodel PR #2996 bounds its chunked loss by
-// (first commit message and "Motivation": the fp32 upcast of a chunk is
-// chunk_size x V x 4 bytes).
+// tile.  Automodel PR #2996 ("Motivation") bounds the fp32 transient of its
+// chunked loss by chunk_size x V x 4 bytes whatever the sequence length; the
+// chunk of that bound is fixed here at 2048 rows.
 static size_t extra_memory_budget(int64_t V) { return static_cast<size_t>(2048) * V * 4; }
 
 // Rows per backward chunk.  The largest multiple of 128 rows (at most 4864)
