@@ -41,8 +41,11 @@ FLCE_API int flce_gemm(int dt, int a_mn_major, int b_mn_major, int64_t M, int64_
  * 8 grad_W, 16 flce_gemm itself.  A set bit runs each 256 x 256 tile on a pair
  * of CTAs on two SMs (tcgen05.mma.cta_group::2, each SM loading half of B); a
  * clear bit runs each 128 x 256 tile on one CTA.  Both give the same results up
- * to fp32 summation order.  The default (2 | 8 | 16) is the faster choice per
- * contraction measured on GB300.  Returns the previous mask.  Process-wide; do
+ * to fp32 summation order.  Bit 32 is not a contraction: when set, the dZ
+ * recompute at K = D <= 1024 runs on one CTA per tile with eight epilogue
+ * warps instead (two per TMEM lane quarter, each forming half of the tile's
+ * columns), whatever bit 2 says.  The default (2 | 8 | 16 | 32) is the faster
+ * choice per contraction measured on GB300.  Returns the previous mask.  Process-wide; do
  * not change it while calls run. */
 FLCE_API int flce_gemm_set_pair(int mask);
 

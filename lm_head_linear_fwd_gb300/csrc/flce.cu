@@ -272,6 +272,14 @@ struct EpiDlogits {
   template <int BN>
   __device__ static void tile(const Params& p, int mt, int nt, int row_in_tile, uint32_t taddr,
                               EpiCtx& ctx) {
+    tile_part<BN>(p, mt, nt, row_in_tile, taddr, ctx, 0, BN);
+  }
+  // Columns [c_lo, c_hi) of the tile (multiples of the 128-byte slab width):
+  // with eight epilogue warps two warps share a TMEM lane quarter, each
+  // forming and storing half of the tile's columns.
+  template <int BN>
+  __device__ static void tile_part(const Params& p, int mt, int nt, int row_in_tile,
+                                   uint32_t taddr, EpiCtx& ctx, int c_lo, int c_hi) {
     constexpr int CPS = 128 / static_cast<int>(sizeof(T));  // columns per 128-byte row slab
     constexpr int EPV = Elem<T>::kPerVec;
     const int row = mt * kBM + row_in_tile;
@@ -290,7 +298,7 @@ struct EpiDlogits {
     const int64_t ylocal = valid ? (y - p.v0) - col_base : -1;
     const int r0 = mt * kBM + (row_in_tile & ~31);
 #pragma unroll 1
-    for (int g = 0; g < BN / CPS; ++g) {
+    for (int g = c_lo / CPS; g < c_hi / CPS; ++g) {
       const int col0 = col_base + g * CPS;
       if (col0 >= p.V) break;  // uniform across the warp
       uint4 packed[8];
@@ -811,8 +819,11 @@ struct OutDesc {
 
 // Which bf16 contractions run on CTA pairs (tc_gemm_pair_kernel) instead of one
 // CTA per tile: a bit mask of GemmRole.
+// kWideDz (not a contraction): the dZ contraction at K <= 1024 runs on one CTA
+// per tile with eight epilogue warps instead (launch_dz_gemm).
 enum GemmRole : int { kRoleFwd = 1, kRoleDz = 2, kRoleGradH = 4, kRoleGradW = 8, kRoleRaw = 16 };
-static std::atomic<int> g_pair_mask{kRoleDz | kRoleGradW | kRoleRaw};
+constexpr int kWideDz = 32;
+static std::atomic<int> g_pair_mask{kRoleDz | kRoleGradW | kRoleRaw | kWideDz};
 
 template <int BN, bool A_MN, bool B_MN, class Epi>
 static int launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
@@ -864,15 +875,15 @@ static int launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const 
                      "cudaLaunchKernelEx(tc_gemm_pair_kernel)");
 }
 
-template <typename T, int BN, bool A_MN, bool B_MN, class Epi>
+template <typename T, int BN, bool A_MN, bool B_MN, class Epi, int EW = 4>
 static int launch_gemm(int role, const Operand& a, const Operand& b, const OutDesc* out, int M,
                        int N, int K, int group_m, const typename Epi::Params& ep,
                        int32_t* status, cudaStream_t s, int k_splits = 1) {
-  using G = GemmGeo<T, BN>;
+  using G = GemmGeo<T, BN, EW>;
   const int dt = sizeof(T) == 2 ? FLCE_BF16 : FLCE_F32;
   CUtensorMap ma, mb, mc;
-  const bool pair =
-      sizeof(T) == 2 && BN == 256 && k_splits == 1 && (g_pair_mask.load() & role) != 0;
+  const bool pair = EW == 4 && sizeof(T) == 2 && BN == 256 && k_splits == 1 &&
+                    (g_pair_mask.load() & role) != 0;
   int rc = make_operand_map(&ma, a, dt, kBM);
   if (rc != FLCE_OK) return rc;
   rc = make_operand_map(&mb, b, dt, pair ? BN / 2 : BN);
@@ -883,7 +894,7 @@ static int launch_gemm(int role, const Operand& a, const Operand& b, const OutDe
   } else {
     mc = ma;  // unused by epilogues that do not store through TMA
   }
-  if constexpr (sizeof(T) == 2 && BN == 256) {
+  if constexpr (sizeof(T) == 2 && BN == 256 && EW == 4) {
     if (pair) return launch_gemm_pair<BN, A_MN, B_MN, Epi>(ma, mb, mc, M, N, K, group_m, ep,
                                                          status, s);
   }
@@ -901,11 +912,11 @@ static int launch_gemm(int role, const Operand& a, const Operand& b, const OutDe
   ga.status = status;
   const int tiles = ga.nMt * ga.k_splits * ga.nNt;
   if (tiles == 0) return FLCE_OK;
-  auto kern = tc_gemm_kernel<T, BN, A_MN, B_MN, Epi>;
+  auto kern = tc_gemm_kernel<T, BN, A_MN, B_MN, Epi, EW>;
   rc = raise_smem_once(kern, G::kSmemBytes, "cudaFuncSetAttribute(tc_gemm_kernel)");
   if (rc != FLCE_OK) return rc;
   const int grid = std::min(tiles, sm_count());
-  kern<<<grid, kGemmThreads, G::kSmemBytes, s>>>(ma, mb, mc, ga, ep);
+  kern<<<grid, G::kThreads, G::kSmemBytes, s>>>(ma, mb, mc, ga, ep);
   return launch_status("tc_gemm_kernel launch");
 }
 
@@ -1261,6 +1272,25 @@ extern "C" int flce_shard_finish(const float* m_global, const float* s_global,
                          loss, n_valid, s);
 }
 
+// The dZ contraction of the backward (step 1).  At a short K (K = D <= 1024)
+// the dZ epilogue, which forms and stores a bf16 tile, is as long as the
+// tile's main loop; eight epilogue warps (two per TMEM lane quarter) halve
+// it.  At a long K four warps keep up and the extra stage of the ring pays
+// more (see the kernel's GemmGeo).
+template <typename T>
+static int launch_dz_gemm(const Operand& a, const Operand& b, const OutDesc& o, int M, int N,
+                          int K, int group_m, const typename EpiDlogits<T>::Params& ep,
+                          int32_t* status, cudaStream_t s) {
+  using E = EpiDlogits<T>;
+  if constexpr (sizeof(T) == 2) {
+    if (K <= 1024 && (g_pair_mask.load() & kWideDz) != 0)
+      return launch_gemm<T, kBNFwd, false, false, E, 8>(kRoleDz, a, b, &o, M, N, K, group_m, ep,
+                                                        status, s);
+  }
+  return launch_gemm<T, kBNFwd, false, false, E>(kRoleDz, a, b, &o, M, N, K, group_m, ep,
+                                                 status, s);
+}
+
 // Steps 2-4 of a backward chunk, shared by flce_bwd and flce_fwd_bwd: bias
 // column sums, grad_H of the chunk, grad_W accumulation, from the chunk's dZ.
 //
@@ -1433,8 +1463,8 @@ static int flce_bwd_impl(const void* H, const void* W, const void* bias, int64_t
         const Operand a{Ht, N, D, D, false};
         const Operand b{Wc, Vc, D, D, false};
         const OutDesc o{dz, dt, N, Vc, p.ldVc};
-        rc = launch_gemm<T, kBNFwd, false, false, E>(kRoleDz, a, b, &o, static_cast<int>(N), Vc,
-                                                     (int)D, group_for(D, dt, nMt), ep, status, s);
+        rc = launch_dz_gemm<T>(a, b, o, static_cast<int>(N), Vc, (int)D, group_for(D, dt, nMt),
+                               ep, status, s);
         if (rc != FLCE_OK) return rc;
         rc = bwd_tail<T>(Wc, Ht, D, Vc, static_cast<int>(N), /*first_chunk=*/true, pv, w,
                          grad_H != nullptr ? hacc : nullptr,
@@ -1466,8 +1496,7 @@ static int flce_bwd_impl(const void* H, const void* W, const void* bias, int64_t
     const Operand a{Ht + r0 * D, C, D, D, false};
     const Operand b{W, V, D, D, false};
     const OutDesc o{dz, dt, C, V, p.ldV};
-    rc = launch_gemm<T, kBNFwd, false, false, E>(kRoleDz, a, b, &o, C, (int)V, (int)D,
-                                                 group_for(D, dt, nMt), ep, status, s);
+    rc = launch_dz_gemm<T>(a, b, o, C, (int)V, (int)D, group_for(D, dt, nMt), ep, status, s);
     if (rc != FLCE_OK) return rc;
     rc = bwd_tail<T>(W, Ht + r0 * D, D, V, C, r0 == 0, p, w,
                      grad_H != nullptr ? static_cast<char*>(grad_H) + r0 * D * h_es : nullptr,
@@ -1680,7 +1709,7 @@ extern "C" int flce_grad_scale(void* x, int dt, int64_t n, const float* g, flce_
 
 // ------------------------------------------------------ raw GEMM entry point
 
-extern "C" int flce_gemm_set_pair(int mask) { return g_pair_mask.exchange(mask & 31); }
+extern "C" int flce_gemm_set_pair(int mask) { return g_pair_mask.exchange(mask & 63); }
 
 extern "C" int flce_gemm_pair_slots(void) {
   using E = EpiStore<float, true>;

@@ -49,18 +49,23 @@ struct MmaTraits<float> {
   }
 };
 
-template <typename T, int BN>
+// EW: epilogue warps, 4 (one per TMEM lane quarter) or 8 (two per quarter,
+// each draining half of the tile's columns; one stage fewer to make room for
+// their staging buffers).
+template <typename T, int BN, int EW = 4>
 struct GemmGeo {
+  static_assert(EW == 4 || EW == 8, "four or eight epilogue warps");
   static constexpr int kEK = 128 / static_cast<int>(sizeof(T));  // K elements per stage
   static constexpr int kStageA = kBM * 128;
   static constexpr int kStageB = BN * 128;
   static constexpr int kStageBytes = kStageA + kStageB;
-  static constexpr int kStages = (BN == 256) ? 4 : 6;
+  static constexpr int kStages = ((BN == 256) ? 4 : 6) - (EW == 8 ? 1 : 0);
   static constexpr int kTmemCols = 2 * BN;
-  static constexpr int kEpiSmem = 4 * 2 * 4096;  // 4 epilogue warps x 2 staging buffers
+  static constexpr int kEpiSmem = EW * 2 * 4096;  // epilogue warps x 2 staging buffers
   static constexpr int kSmemBytes =
       kStages * kStageBytes + kEpiSmem + 1024;  // + 1024-byte alignment slack
   static constexpr int kMmaPerStage = 128 / (MmaTraits<T>::kUmmaK * static_cast<int>(sizeof(T)));
+  static constexpr int kThreads = 64 + 32 * EW;
 };
 
 struct GemmArgs {
@@ -151,12 +156,12 @@ struct EpiCtx {
   }
 };
 
-template <typename T, int BN, bool A_MN, bool B_MN, class Epi>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+template <typename T, int BN, bool A_MN, bool B_MN, class Epi, int EW = 4>
+__global__ void __launch_bounds__(64 + 32 * EW, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmArgs ga,
                    const typename Epi::Params ep) {
-  using G = GemmGeo<T, BN>;
+  using G = GemmGeo<T, BN, EW>;
   constexpr int S = G::kStages;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[S], empty_bar[S], accf_bar[2], acce_bar[2], drain_bar;
@@ -176,7 +181,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&accf_bar[i], 1);
-      mbar_init(&acce_bar[i], 4);
+      mbar_init(&acce_bar[i], EW);
     }
     mbar_init(&drain_bar, 1);
     // checked builds: the stages and staging buffers fit the launch's shared memory
@@ -307,6 +312,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // -------------------------------------------------------------- epilogue
     const int quad = warp & 3;  // TMEM lanes this warp may access: 32*quad .. +31
     const int row_in_tile = quad * 32 + lane;
+    const int half = (warp - 2) >> 2;  // EW == 8: which half of the tile's columns
     EpiCtx ctx;
     ctx.map = &tmC;
     ctx.buf = smem + S * G::kStageBytes + (warp - 2) * 2 * 4096;
@@ -328,7 +334,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tile_coords(t, nMtE, ga.nNt, ga.group_m, mte, nt);
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(buf * BN);
-      Epi::template tile<BN>(ep, mte, nt, row_in_tile, taddr, ctx);
+      if constexpr (EW == 4)
+        Epi::template tile<BN>(ep, mte, nt, row_in_tile, taddr, ctx);
+      else
+        Epi::template tile_part<BN>(ep, mte, nt, row_in_tile, taddr, ctx, half * (BN / 2),
+                                    (half + 1) * (BN / 2));
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acce_bar[buf]);

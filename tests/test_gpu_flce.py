@@ -82,7 +82,7 @@ def test_small_model_workload(lh):
     _check_all(p, out, bw)
 
 
-@pytest.mark.parametrize("pair", [31, 0], ids=["pair", "single"])
+@pytest.mark.parametrize("pair", [31, 0, 32], ids=["pair", "single", "wide_dz"])
 @pytest.mark.parametrize("N,D,V,chunk,bias", [(700, 256, 3001, 256, True), (129, 64, 777, 128, False),
                                               (1000, 520, 2048, None, False)])
 def test_ragged_multi_chunk(lh, N, D, V, chunk, bias, pair):
