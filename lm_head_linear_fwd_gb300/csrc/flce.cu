@@ -71,6 +71,41 @@ __device__ __forceinline__ void add_bias32(const void* bias, int col0, int V, fl
   }
 }
 
+// The bias of one 32-column chunk, fetched a chunk ahead of its use so that
+// the loads are in flight while the previous chunk is reduced (an epilogue
+// warp has no other warp on its scheduler to hide their latency).  Only whole,
+// aligned chunks are fetched; add_bias32 takes the others element by element.
+template <typename T>
+struct BiasAhead {
+  static constexpr int kVecs = 32 / Elem<T>::kPerVec;
+  uint4 w[kVecs];
+  __device__ static bool vec_ok(const void* bias, int col0, int V) {
+    return col0 + 32 <= V &&
+           (reinterpret_cast<uintptr_t>(static_cast<const T*>(bias) + col0) & 15u) == 0;
+  }
+  __device__ void fetch(const void* bias, int col0, int V) {
+    if (vec_ok(bias, col0, V)) {
+      const uint4* bv = reinterpret_cast<const uint4*>(static_cast<const T*>(bias) + col0);
+#pragma unroll
+      for (int k = 0; k < kVecs; ++k) w[k] = __ldg(bv + k);
+    }
+  }
+  __device__ void add(const void* bias, int col0, int V, float (&v)[32]) const {
+    if (vec_ok(bias, col0, V)) {
+      constexpr int EPV = Elem<T>::kPerVec;
+#pragma unroll
+      for (int k = 0; k < kVecs; ++k) {
+        float x[EPV];
+        Elem<T>::unpack(w[k], x);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) v[k * EPV + e] += x[e];
+      }
+    } else {
+      add_bias32<T>(bias, col0, V, v);
+    }
+  }
+};
+
 // Adds the first n (<= 32) of 32 logits v to a base-2 online log-sum-exp: the
 // chunk maximum (the order of v equals the order of v*log2e), one rescale,
 // then 2^(v*log2e - m) by packed pairs (FFMA2) summed into four independent
@@ -142,13 +177,19 @@ struct EpiLse {
     const int64_t ylocal = (y < 0) ? -1 : (y - p.v0) - col_base;
     Lse2 st;
     float zy = 0.0f;
+    BiasAhead<T> bnext;
+    if (p.bias != nullptr) bnext.fetch(p.bias, col_base, p.V);
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       const int col0 = col_base + c * 32;
       if (col0 >= p.V) break;  // uniform across the warp
       float v[32];
       tmem_ld32(taddr + c * 32, v);
-      if (p.bias != nullptr) add_bias32<T>(p.bias, col0, p.V, v);
+      if (p.bias != nullptr) {
+        const BiasAhead<T> bcur = bnext;
+        if (c + 1 < BN / 32) bnext.fetch(p.bias, col0 + 32, p.V);
+        bcur.add(p.bias, col0, p.V, v);
+      }
       // the label's logit, in the one chunk that holds it (rarely any lane of a warp)
       if (static_cast<uint64_t>(ylocal - c * 32) < 32u) zy = pick32(v, ylocal, c * 32);
       lse_add32(v, p.V - col0, st);
@@ -185,13 +226,19 @@ struct EpiLseStore {
     // pass 1: the tile maximum (the order of z equals the order of z*log2e)
     // and the label's logit, in the one chunk that holds it
     float mx = -INFINITY, zy = 0.0f;
+    BiasAhead<T> bnext;
+    if (p.bias != nullptr) bnext.fetch(p.bias, col_base, p.V);
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       const int col0 = col_base + c * 32;
       if (col0 >= p.V) break;
       float v[32];
       tmem_ld32(taddr + c * 32, v);
-      if (p.bias != nullptr) add_bias32<T>(p.bias, col0, p.V, v);
+      if (p.bias != nullptr) {
+        const BiasAhead<T> bcur = bnext;
+        if (c + 1 < BN / 32) bnext.fetch(p.bias, col0 + 32, p.V);
+        bcur.add(p.bias, col0, p.V, v);
+      }
       if (static_cast<uint64_t>(ylocal - c * 32) < 32u) zy = pick32(v, ylocal, c * 32);
       if (col0 + 32 <= p.V) {
 #pragma unroll
@@ -208,6 +255,7 @@ struct EpiLseStore {
     const float2 lg = make_float2(kLog2e, kLog2e), nm = make_float2(-m, -m);
     float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
                      make_float2(0.0f, 0.0f)};
+    if (p.bias != nullptr) bnext.fetch(p.bias, col_base, p.V);
 #pragma unroll 1
     for (int g = 0; g < BN / CPS; ++g) {
       const int col0 = col_base + g * CPS;
@@ -218,7 +266,11 @@ struct EpiLseStore {
         float v[32];
         tmem_ld32(taddr + g * CPS + h * 32, v);
         const int cb = col0 + h * 32;
-        if (p.bias != nullptr) add_bias32<T>(p.bias, cb, p.V, v);
+        if (p.bias != nullptr) {
+          const BiasAhead<T> bcur = bnext;
+          if (cb + 32 < col_base + BN) bnext.fetch(p.bias, cb + 32, p.V);
+          bcur.add(p.bias, cb, p.V, v);
+        }
         const bool full = cb + 32 <= p.V;
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
@@ -297,6 +349,8 @@ struct EpiDlogits {
     const int col_base = nt * BN;
     const int64_t ylocal = valid ? (y - p.v0) - col_base : -1;
     const int r0 = mt * kBM + (row_in_tile & ~31);
+    BiasAhead<T> bnext;
+    if (p.bias != nullptr) bnext.fetch(p.bias, col_base + c_lo, p.V);
 #pragma unroll 1
     for (int g = c_lo / CPS; g < c_hi / CPS; ++g) {
       const int col0 = col_base + g * CPS;
@@ -307,7 +361,11 @@ struct EpiDlogits {
         float v[32];
         tmem_ld32(taddr + g * CPS + h * 32, v);
         const int cl = g * CPS + h * 32;  // column within the tile
-        if (p.bias != nullptr) add_bias32<T>(p.bias, col_base + cl, p.V, v);
+        if (p.bias != nullptr) {
+          const BiasAhead<T> bcur = bnext;
+          if (cl + 32 < c_hi) bnext.fetch(p.bias, col_base + cl + 32, p.V);
+          bcur.add(p.bias, col_base + cl, p.V, v);
+        }
         if (c == 0.0f) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = 0.0f;
