@@ -320,6 +320,11 @@ struct EpiDlogits {
     int M, V;               // M = rows in this chunk; V = columns of this shard
     int64_t v0;             // vocabulary id of this shard's column 0
     int64_t V_total;        // vocabulary size (labels are checked against it)
+    // bf16 only, or null: per 32-row group g of the chunk, the column sums of
+    // the stored dZ at colsum[g * colsum_ld + column] (colsum_ld even), for
+    // the bias gradient
+    float* colsum = nullptr;
+    int64_t colsum_ld = 0;
   };
   template <int BN>
   __device__ static void tile(const Params& p, int mt, int nt, int row_in_tile, uint32_t taddr,
@@ -401,6 +406,17 @@ struct EpiDlogits {
         }
       }
       ctx.store_slab(packed, col0, r0, false);
+      if constexpr (sizeof(T) == 2) {
+        if (p.colsum != nullptr) {  // this warp's 32 rows of the slab, summed
+          const float2 cs = ctx.last_slab_bf16_column_sums();
+          const int col = col0 + 2 * (row_in_tile & 31);
+          float* dst = p.colsum + static_cast<int64_t>(r0 >> 5) * p.colsum_ld + col;
+          if (col + 1 < p.V)
+            *reinterpret_cast<float2*>(dst) = cs;
+          else if (col < p.V)
+            dst[0] = cs.x;
+        }
+      }
     }
   }
 };
@@ -557,6 +573,12 @@ __global__ void __launch_bounds__(256) shard_finish_kernel(
 
 constexpr int kColSplits = 32;
 
+// Rows of partial column sums the eight-warp dZ epilogue writes for a chunk
+// of C rows (one per 32 rows of its 128-row tiles); 0 where it cannot run.
+static int64_t dz_colsum_rows(int dt, int64_t D, int64_t C) {
+  return dt == FLCE_BF16 && D <= 1024 ? (C + kBM - 1) / kBM * (kBM / 32) : 0;
+}
+
 // Column sums of dZ [M, ldd] over row slices: part[s, v] = sum of rows in slice
 // s.  Each thread sums one 16-byte vector of columns (the chunk buffer's row
 // stride is a multiple of 64 elements and its start 256-byte aligned, so every
@@ -588,13 +610,29 @@ __global__ void __launch_bounds__(256) colsum_partial_kernel(const T* __restrict
     if (v0 + e < V) part[static_cast<int64_t>(s) * V + v0 + e] = acc[e];
 }
 
-__global__ void __launch_bounds__(256) colsum_final_kernel(const float* __restrict__ part, int V,
-                                                           float* __restrict__ out, int beta) {
-  const int v = blockIdx.x * blockDim.x + threadIdx.x;
-  if (v >= V) return;
-  float acc = beta ? out[v] : 0.0f;
-  for (int s = 0; s < kColSplits; ++s) acc += part[static_cast<int64_t>(s) * V + v];
-  out[v] = acc;
+// out[v] (+)= the sum of the nparts partial column sums part[s * ld + v].  A
+// block takes 32 columns: warp w sums the partials s = w, w + 8, ... in order
+// (each load of a warp reads 32 consecutive columns), then the eight warp sums
+// are added in warp order, so the result is the same on every run.
+constexpr int kColFinalWarps = 8;
+
+__global__ void __launch_bounds__(32 * kColFinalWarps) colsum_final_kernel(
+    const float* __restrict__ part, int nparts, int64_t ld, int V, float* __restrict__ out,
+    int beta) {
+  __shared__ float red[kColFinalWarps][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int v = blockIdx.x * 32 + lane;
+  float acc = 0.0f;
+  if (v < V) {
+#pragma unroll 4
+    for (int s = warp; s < nparts; s += kColFinalWarps) acc += part[static_cast<int64_t>(s) * ld + v];
+  }
+  red[warp][lane] = acc;
+  __syncthreads();
+  if (warp != 0 || v >= V) return;
+  float total = beta ? out[v] : 0.0f;
+  for (int w = 0; w < kColFinalWarps; ++w) total += red[w][lane];
+  out[v] = total;
 }
 
 // out[c, r] = in[r, c] for a [R, Cc] matrix of 4-byte elements (32 x 32 tiles
@@ -1127,7 +1165,11 @@ static FlcePlan plan(int dt, int64_t N, int64_t D, int64_t V, int64_t chunk, boo
   p.off_dz = o;
   o += round_up(static_cast<size_t>(std::min<int64_t>(p.chunk, N)) * p.ldV * es, 256);
   p.off_colsum = o;
-  o += round_up(static_cast<size_t>(kColSplits) * V * 4, 256);
+  o += round_up(std::max(static_cast<size_t>(kColSplits) * V,
+                         static_cast<size_t>(dz_colsum_rows(dt, D, std::min<int64_t>(p.chunk, N))) *
+                             p.ldV) *
+                    4,
+                256);
   {
     // split-K partials of grad_H, for the full chunk and for the last one
     const int64_t c1 = std::min<int64_t>(p.chunk, N);
@@ -1157,7 +1199,10 @@ static FlcePlan plan(int dt, int64_t N, int64_t D, int64_t V, int64_t chunk, boo
     p.off_dz = o;
     o += round_up(static_cast<size_t>(N) * p.ldVc * es, 256);
     p.off_colsum = o;
-    o += round_up(static_cast<size_t>(kColSplits) * p.vchunk * 4, 256);
+    o += round_up(std::max(static_cast<size_t>(kColSplits) * p.vchunk,
+                           static_cast<size_t>(dz_colsum_rows(dt, D, N)) * p.ldVc) *
+                      4,
+                  256);
     p.off_hpart = o;
     p.off_hacc = o;
     o += round_up(static_cast<size_t>(N) * D * 4, 256);
@@ -1350,12 +1395,17 @@ extern "C" int flce_shard_finish(const float* m_global, const float* s_global,
 // it.  At a long K four warps keep up and the extra stage of the ring pays
 // more (see the kernel's GemmGeo).
 template <typename T>
+static bool dz_wide(int64_t K) {
+  return sizeof(T) == 2 && K <= 1024 && (g_pair_mask.load() & kWideDz) != 0;
+}
+
+template <typename T>
 static int launch_dz_gemm(const Operand& a, const Operand& b, const OutDesc& o, int M, int N,
                           int K, int group_m, const typename EpiDlogits<T>::Params& ep,
-                          int32_t* status, cudaStream_t s) {
+                          int32_t* status, cudaStream_t s, bool wide) {
   using E = EpiDlogits<T>;
   if constexpr (sizeof(T) == 2) {
-    if (K <= 1024 && (g_pair_mask.load() & kWideDz) != 0)
+    if (wide)
       return launch_gemm<T, kBNFwd, false, false, E, 8>(kRoleDz, a, b, &o, M, N, K, group_m, ep,
                                                         status, s);
   }
@@ -1371,11 +1421,15 @@ static int launch_dz_gemm(const Operand& a, const Operand& b, const OutDesc& o, 
 //
 // grad_H_acc_beta >= 0 (vocabulary slices, bf16): grad_H_chunk is an fp32
 // accumulator that this slice's term is stored into (0) or reduce-added to (1).
+//
+// dz_colsum_parts > 0: the dZ epilogue has already written that many rows of
+// partial column sums (row stride p.ldV) into the column-sum buffer.
 template <typename T>
 static int bwd_tail(const void* W, const T* Hc, int64_t D, int64_t V, int C, bool first_chunk,
                     const FlcePlan& p, char* w, void* grad_H_chunk, float* grad_W,
                     int accumulate_grad_W, float* grad_bias, int32_t* status, cudaStream_t s,
-                    bool grad_H_f32 = false, int grad_H_acc_beta = -1) {
+                    bool grad_H_f32 = false, int grad_H_acc_beta = -1,
+                    int dz_colsum_parts = 0) {
   const int dt = sizeof(T) == 2 ? FLCE_BF16 : FLCE_F32;
   const int dt_h = grad_H_f32 ? FLCE_F32 : dt;
   constexpr bool kTf32 = sizeof(T) == 4;
@@ -1385,13 +1439,20 @@ static int bwd_tail(const void* W, const T* Hc, int64_t D, int64_t V, int C, boo
   float* dzT = reinterpret_cast<float*>(w + p.off_dzT);  // [V, ldCt]  (fp32 only)
   float* HT = reinterpret_cast<float*>(w + p.off_HT);    // [D, ldCt]  (fp32 only)
   int rc = FLCE_OK;
-  // 2. bias gradient
+  // 2. bias gradient: the column sums of dZ, from the dZ epilogue's partial
+  // sums or from the stored dZ
   if (grad_bias != nullptr) {
-    constexpr int kEpv = Elem<T>::kPerVec;
-    dim3 g1(static_cast<unsigned>(((V + kEpv - 1) / kEpv + 255) / 256), kColSplits);
-    colsum_partial_kernel<T><<<g1, 256, 0, s>>>(dz, C, p.ldV, (int)V, colsum);
-    colsum_final_kernel<<<static_cast<unsigned>((V + 255) / 256), 256, 0, s>>>(
-        colsum, (int)V, grad_bias, first_chunk ? 0 : 1);
+    int nparts = dz_colsum_parts;
+    int64_t ld = p.ldV;
+    if (nparts == 0) {
+      constexpr int kEpv = Elem<T>::kPerVec;
+      dim3 g1(static_cast<unsigned>(((V + kEpv - 1) / kEpv + 255) / 256), kColSplits);
+      colsum_partial_kernel<T><<<g1, 256, 0, s>>>(dz, C, p.ldV, (int)V, colsum);
+      nparts = kColSplits;
+      ld = V;
+    }
+    colsum_final_kernel<<<static_cast<unsigned>((V + 31) / 32), 32 * kColFinalWarps, 0, s>>>(
+        colsum, nparts, ld, (int)V, grad_bias, first_chunk ? 0 : 1);
     rc = launch_status("colsum kernels launch");
     if (rc != FLCE_OK) return rc;
   }
@@ -1532,17 +1593,24 @@ static int flce_bwd_impl(const void* H, const void* W, const void* bias, int64_t
         typename E::Params ep{bias_t != nullptr ? bias_t + c0 : nullptr, labels, ignore_index,
                               lse, reduction, num_label_tokens, n_valid, grad_loss,
                               static_cast<int>(N), Vc, v0 + c0, V_total};
+        const bool wide = dz_wide<T>(D);
+        const int parts = wide && grad_bias != nullptr
+                              ? static_cast<int>(dz_colsum_rows(dt, D, N)) : 0;
+        if (parts > 0) {
+          ep.colsum = reinterpret_cast<float*>(w + pv.off_colsum);
+          ep.colsum_ld = pv.ldV;
+        }
         const Operand a{Ht, N, D, D, false};
         const Operand b{Wc, Vc, D, D, false};
         const OutDesc o{dz, dt, N, Vc, p.ldVc};
         rc = launch_dz_gemm<T>(a, b, o, static_cast<int>(N), Vc, (int)D, group_for(D, dt, nMt),
-                               ep, status, s);
+                               ep, status, s, wide);
         if (rc != FLCE_OK) return rc;
         rc = bwd_tail<T>(Wc, Ht, D, Vc, static_cast<int>(N), /*first_chunk=*/true, pv, w,
                          grad_H != nullptr ? hacc : nullptr,
                          grad_W != nullptr ? grad_W + c0 * D : nullptr, accumulate_grad_W,
                          grad_bias != nullptr ? grad_bias + c0 : nullptr, status, s, false,
-                         /*grad_H_acc_beta=*/k > 0 ? 1 : 0);
+                         /*grad_H_acc_beta=*/k > 0 ? 1 : 0, parts);
         if (rc != FLCE_OK) return rc;
       }
       if (grad_H != nullptr && !grad_H_f32) {
@@ -1565,14 +1633,22 @@ static int flce_bwd_impl(const void* H, const void* W, const void* bias, int64_t
     typename E::Params ep{bias, labels + r0, ignore_index, lse + r0, reduction,
                           num_label_tokens, n_valid, grad_loss, C, static_cast<int>(V), v0,
                           V_total};
+    // the eight-warp epilogue also forms the bias gradient's column sums
+    const bool wide = dz_wide<T>(D);
+    const int parts = wide && grad_bias != nullptr ? static_cast<int>(dz_colsum_rows(dt, D, C)) : 0;
+    if (parts > 0) {
+      ep.colsum = reinterpret_cast<float*>(w + p.off_colsum);
+      ep.colsum_ld = p.ldV;
+    }
     const Operand a{Ht + r0 * D, C, D, D, false};
     const Operand b{W, V, D, D, false};
     const OutDesc o{dz, dt, C, V, p.ldV};
-    rc = launch_dz_gemm<T>(a, b, o, C, (int)V, (int)D, group_for(D, dt, nMt), ep, status, s);
+    rc = launch_dz_gemm<T>(a, b, o, C, (int)V, (int)D, group_for(D, dt, nMt), ep, status, s,
+                           wide);
     if (rc != FLCE_OK) return rc;
     rc = bwd_tail<T>(W, Ht + r0 * D, D, V, C, r0 == 0, p, w,
                      grad_H != nullptr ? static_cast<char*>(grad_H) + r0 * D * h_es : nullptr,
-                     grad_W, accumulate_grad_W, grad_bias, status, s, grad_H_f32);
+                     grad_W, accumulate_grad_W, grad_bias, status, s, grad_H_f32, -1, parts);
     if (rc != FLCE_OK) return rc;
   }
   return rc;

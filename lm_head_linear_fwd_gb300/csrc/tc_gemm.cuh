@@ -150,6 +150,22 @@ struct EpiCtx {
     next ^= 1;
   }
 
+  // Column sums, in row order, of the bf16 slab staged last: lane l sums the
+  // 32-bit word at byte 4l of each of the 32 rows, i.e. columns 2l (x) and
+  // 2l + 1 (y).  For a fixed row the 32 lanes read 32 distinct banks.
+  __device__ float2 last_slab_bf16_column_sums() const {
+    const uint8_t* b = buf + (next ^ 1) * 4096;
+    const int chunk = lane >> 2, off = (lane & 3) << 2;
+    float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll 8
+    for (int r = 0; r < 32; ++r) {
+      const uint32_t w =
+          *reinterpret_cast<const uint32_t*>(b + r * 128 + ((chunk ^ (r & 7)) << 4) + off);
+      acc = __fadd2_rn(acc, make_float2(bf16_lo(w), bf16_hi(w)));
+    }
+    return acc;
+  }
+
   __device__ void drain() {
     if (lane == 0) bulk_wait_all();
     __syncwarp();
