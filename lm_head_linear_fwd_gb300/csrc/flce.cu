@@ -1392,8 +1392,8 @@ extern "C" int flce_shard_finish(const float* m_global, const float* s_global,
 // The dZ contraction of the backward (step 1).  At a short K (K = D <= 1024)
 // the dZ epilogue, which forms and stores a bf16 tile, is as long as the
 // tile's main loop; eight epilogue warps (two per TMEM lane quarter) halve
-// it.  At a long K four warps keep up and the extra stage of the ring pays
-// more (see the kernel's GemmGeo).
+// it.  At a long K four warps keep up (eight, for every contraction, made the
+// Llama-3 8B head's step 1.7% slower).
 template <typename T>
 static bool dz_wide(int64_t K) {
   return sizeof(T) == 2 && K <= 1024 && (g_pair_mask.load() & kWideDz) != 0;

@@ -59,9 +59,13 @@ struct GemmGeo {
   static constexpr int kStageA = kBM * 128;
   static constexpr int kStageB = BN * 128;
   static constexpr int kStageBytes = kStageA + kStageB;
-  static constexpr int kStages = ((BN == 256) ? 4 : 6) - (EW == 8 ? 1 : 0);
+  static constexpr int kStages = (BN == 256) ? 4 : 6;
   static constexpr int kTmemCols = 2 * BN;
-  static constexpr int kEpiSmem = EW * 2 * 4096;  // epilogue warps x 2 staging buffers
+  // Output staging: two 4 KB buffers per epilogue warp, or one with eight
+  // warps (which keeps the fourth stage: at K = 768 the deeper ring took the
+  // dZ contraction from 86.1 to 81.8 us, the single buffer costing less)
+  static constexpr int kStagingBufs = EW == 8 ? 1 : 2;
+  static constexpr int kEpiSmem = EW * kStagingBufs * 4096;
   static constexpr int kSmemBytes =
       kStages * kStageBytes + kEpiSmem + 1024;  // + 1024-byte alignment slack
   static constexpr int kMmaPerStage = 128 / (MmaTraits<T>::kUmmaK * static_cast<int>(sizeof(T)));
@@ -121,19 +125,25 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int k) {
   }
 }
 
-// Output staging of one epilogue warp: two 4 KB buffers (32 rows x 128 B,
-// 1024-byte aligned) written with the 128-byte swizzle the output tensor map
-// uses, each then stored (or reduce-added) to global memory by one TMA
-// instruction.  Rows and columns outside the tensor are clipped by the TMA.
+// Output staging of one epilogue warp: one or two 4 KB buffers (32 rows x
+// 128 B, 1024-byte aligned) written with the 128-byte swizzle the output
+// tensor map uses, each then stored (or reduce-added) to global memory by one
+// TMA instruction.  Rows and columns outside the tensor are clipped by the TMA.
 struct EpiCtx {
   const CUtensorMap* map;
   uint8_t* buf;
   int next;
   int lane;
+  int nbuf = 2;  // staging buffers (1 or 2)
 
   __device__ void store_slab(const uint4 (&row)[8], int c0, int r0, bool reduce) {
     uint8_t* b = buf + next * 4096;
-    if (lane == 0) bulk_wait_read_le1();  // the buffer's previous store has read it
+    if (lane == 0) {  // the buffer's previous store has read it
+      if (nbuf == 2)
+        bulk_wait_read_le1();
+      else
+        bulk_wait_read_all();
+    }
     __syncwarp();
 #pragma unroll
     for (int j = 0; j < 8; ++j)
@@ -147,14 +157,14 @@ struct EpiCtx {
         tma_store_2d(map, b, c0, r0);
       bulk_commit();
     }
-    next ^= 1;
+    next ^= nbuf - 1;
   }
 
   // Column sums, in row order, of the bf16 slab staged last: lane l sums the
   // 32-bit word at byte 4l of each of the 32 rows, i.e. columns 2l (x) and
   // 2l + 1 (y).  For a fixed row the 32 lanes read 32 distinct banks.
   __device__ float2 last_slab_bf16_column_sums() const {
-    const uint8_t* b = buf + (next ^ 1) * 4096;
+    const uint8_t* b = buf + ((next ^ 1) & (nbuf - 1)) * 4096;
     const int chunk = lane >> 2, off = (lane & 3) << 2;
     float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll 8
@@ -331,7 +341,8 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
     const int half = (warp - 2) >> 2;  // EW == 8: which half of the tile's columns
     EpiCtx ctx;
     ctx.map = &tmC;
-    ctx.buf = smem + S * G::kStageBytes + (warp - 2) * 2 * 4096;
+    ctx.buf = smem + S * G::kStageBytes + (warp - 2) * G::kStagingBufs * 4096;
+    ctx.nbuf = G::kStagingBufs;
     ctx.next = 0;
     ctx.lane = lane;
     int local = 0;
