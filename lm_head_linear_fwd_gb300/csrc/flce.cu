@@ -938,7 +938,7 @@ static std::atomic<int> g_pair_mask{kRoleDz | kRoleGradW | kRoleRaw | kWideDz};
 template <int BN, bool A_MN, bool B_MN, class Epi>
 static int launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
                             int M, int N, int K, int group_m, const typename Epi::Params& ep,
-                            int32_t* status, cudaStream_t s) {
+                            int32_t* status, cudaStream_t s, const EpiPre& pre) {
   using G = PairGeo<BN>;
   GemmArgs ga;
   ga.M = M;
@@ -951,8 +951,9 @@ static int launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const 
   ga.status = status;
   ga.k_splits = 1;
   ga.kb_per_split = ga.nK;
+  ga.pre = pre;
   const int tiles = ga.nMt * ga.nNt;
-  if (tiles == 0) return FLCE_OK;
+  if (tiles == 0) return pre.kind != 0 ? FLCE_EINVAL : FLCE_OK;  // the work would be lost
   auto kern = tc_gemm_pair_kernel<BN, A_MN, B_MN, Epi>;
   int rc = raise_smem_once(kern, G::kSmemBytes, "cudaFuncSetAttribute(tc_gemm_pair_kernel)");
   if (rc != FLCE_OK) return rc;
@@ -985,10 +986,12 @@ static int launch_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const 
                      "cudaLaunchKernelEx(tc_gemm_pair_kernel)");
 }
 
+// pre: work for the epilogue warps before their first tile (EpiPre).
 template <typename T, int BN, bool A_MN, bool B_MN, class Epi, int EW = 4>
 static int launch_gemm(int role, const Operand& a, const Operand& b, const OutDesc* out, int M,
                        int N, int K, int group_m, const typename Epi::Params& ep,
-                       int32_t* status, cudaStream_t s, int k_splits = 1) {
+                       int32_t* status, cudaStream_t s, int k_splits = 1,
+                       const EpiPre& pre = EpiPre()) {
   using G = GemmGeo<T, BN, EW>;
   const int dt = sizeof(T) == 2 ? FLCE_BF16 : FLCE_F32;
   CUtensorMap ma, mb, mc;
@@ -1006,7 +1009,7 @@ static int launch_gemm(int role, const Operand& a, const Operand& b, const OutDe
   }
   if constexpr (sizeof(T) == 2 && BN == 256 && EW == 4) {
     if (pair) return launch_gemm_pair<BN, A_MN, B_MN, Epi>(ma, mb, mc, M, N, K, group_m, ep,
-                                                         status, s);
+                                                         status, s, pre);
   }
   GemmArgs ga;
   ga.M = M;
@@ -1020,8 +1023,9 @@ static int launch_gemm(int role, const Operand& a, const Operand& b, const OutDe
   ga.k_splits = (ga.nK + ga.kb_per_split - 1) / ga.kb_per_split;  // no empty split
   ga.group_m = std::max(1, std::min(group_m, ga.nMt * ga.k_splits));
   ga.status = status;
+  ga.pre = pre;
   const int tiles = ga.nMt * ga.k_splits * ga.nNt;
-  if (tiles == 0) return FLCE_OK;
+  if (tiles == 0) return pre.kind != 0 ? FLCE_EINVAL : FLCE_OK;  // the work would be lost
   auto kern = tc_gemm_kernel<T, BN, A_MN, B_MN, Epi, EW>;
   rc = raise_smem_once(kern, G::kSmemBytes, "cudaFuncSetAttribute(tc_gemm_kernel)");
   if (rc != FLCE_OK) return rc;
@@ -1440,7 +1444,11 @@ static int bwd_tail(const void* W, const T* Hc, int64_t D, int64_t V, int C, boo
   float* HT = reinterpret_cast<float*>(w + p.off_HT);    // [D, ldCt]  (fp32 only)
   int rc = FLCE_OK;
   // 2. bias gradient: the column sums of dZ, from the dZ epilogue's partial
-  // sums or from the stored dZ
+  // sums or from partial sums over row slices of the stored dZ; the partial
+  // rows are added up by the epilogue warps of the next contraction before
+  // their first tile (bias_pre), or by a kernel of their own when no
+  // contraction follows
+  EpiPre bias_pre;
   if (grad_bias != nullptr) {
     int nparts = dz_colsum_parts;
     int64_t ld = p.ldV;
@@ -1451,11 +1459,23 @@ static int bwd_tail(const void* W, const T* Hc, int64_t D, int64_t V, int C, boo
       nparts = kColSplits;
       ld = V;
     }
-    colsum_final_kernel<<<static_cast<unsigned>((V + 31) / 32), 32 * kColFinalWarps, 0, s>>>(
-        colsum, nparts, ld, (int)V, grad_bias, first_chunk ? 0 : 1);
+    if (grad_H_chunk != nullptr || grad_W != nullptr) {
+      bias_pre.kind = 1;
+      bias_pre.part = colsum;
+      bias_pre.nparts = nparts;
+      bias_pre.ld = ld;
+      bias_pre.n = V;
+      bias_pre.out = grad_bias;
+      bias_pre.beta = first_chunk ? 0 : 1;
+    } else {
+      colsum_final_kernel<<<static_cast<unsigned>((V + 31) / 32), 32 * kColFinalWarps, 0, s>>>(
+          colsum, nparts, ld, (int)V, grad_bias, first_chunk ? 0 : 1);
+    }
     rc = launch_status("colsum kernels launch");
     if (rc != FLCE_OK) return rc;
   }
+  // the closing work that grad_W's epilogue warps take on (see bias_pre)
+  EpiPre w_pre;
   // 3. grad_H[chunk] = dZ W
   const int S =
       grad_H_chunk != nullptr && grad_H_acc_beta < 0 ? grad_h_splits(C, D, V, dt) : 1;
@@ -1467,7 +1487,7 @@ static int bwd_tail(const void* W, const T* Hc, int64_t D, int64_t V, int C, boo
       const Operand b{W, D, V, D, true};
       const OutDesc o{grad_H_chunk, FLCE_F32, C, D, D};
       rc = launch_gemm<T, 256, false, true, E>(kRoleGradH, a, b, &o, C, (int)D, (int)V, 8, ep,
-                                               status, s);
+                                               status, s, 1, bias_pre);
       if (rc != FLCE_OK) return rc;
     } else {
       return FLCE_ENOSUP;
@@ -1483,23 +1503,33 @@ static int bwd_tail(const void* W, const T* Hc, int64_t D, int64_t V, int C, boo
     if (kTf32) {
       const Operand b{reinterpret_cast<float*>(w + p.off_Wt), D, V, p.ldVt, false};
       rc = launch_gemm<T, 256, false, false, E>(kRoleGradH, a, b, &o, C, (int)D, (int)V, 8, ep,
-                                                status, s, S);
+                                                status, s, S, bias_pre);
     } else {
       const Operand b{W, D, V, D, true};
       rc = launch_gemm<T, 256, false, true, E>(kRoleGradH, a, b, &o, C, (int)D, (int)V, 8, ep,
-                                               status, s, S);
+                                               status, s, S, bias_pre);
     }
     if (rc != FLCE_OK) return rc;
     const int64_t n = static_cast<int64_t>(C) * D / 4;
-    const int grid = static_cast<int>(std::min<int64_t>((n + 255) / 256, sm_count() * 8));
-    if (grad_H_f32)
-      splitk_reduce_kernel<float><<<grid, 256, 0, s>>>(hpart, S, rows * D, C, (int)D,
-                                                       static_cast<float*>(grad_H_chunk));
-    else
-      splitk_reduce_kernel<T><<<grid, 256, 0, s>>>(hpart, S, rows * D, C, (int)D,
-                                                   static_cast<T*>(grad_H_chunk));
-    rc = launch_status("splitk_reduce_kernel launch");
-    if (rc != FLCE_OK) return rc;
+    if (grad_W != nullptr) {  // closed by grad_W's epilogue warps
+      w_pre.kind = 2;
+      w_pre.part = hpart;
+      w_pre.nparts = S;
+      w_pre.ld = rows * D;
+      w_pre.n = n;
+      w_pre.out = grad_H_chunk;
+      w_pre.out_bf16 = !grad_H_f32 && sizeof(T) == 2 ? 1 : 0;
+    } else {
+      const int grid = static_cast<int>(std::min<int64_t>((n + 255) / 256, sm_count() * 8));
+      if (grad_H_f32)
+        splitk_reduce_kernel<float><<<grid, 256, 0, s>>>(hpart, S, rows * D, C, (int)D,
+                                                         static_cast<float*>(grad_H_chunk));
+      else
+        splitk_reduce_kernel<T><<<grid, 256, 0, s>>>(hpart, S, rows * D, C, (int)D,
+                                                     static_cast<T*>(grad_H_chunk));
+      rc = launch_status("splitk_reduce_kernel launch");
+      if (rc != FLCE_OK) return rc;
+    }
   } else if (grad_H_chunk != nullptr && grad_H_f32 && !kTf32) {
     // bf16 operands, fp32 output: the split-K partial's epilogue with one split
     using E = EpiStore<float, false>;
@@ -1508,7 +1538,7 @@ static int bwd_tail(const void* W, const T* Hc, int64_t D, int64_t V, int C, boo
     const OutDesc o{grad_H_chunk, FLCE_F32, C, D, D};
     const Operand b{W, D, V, D, true};
     rc = launch_gemm<T, 256, false, true, E>(kRoleGradH, a, b, &o, C, (int)D, (int)V, 8, ep,
-                                             status, s);
+                                             status, s, 1, bias_pre);
     if (rc != FLCE_OK) return rc;
   } else if (grad_H_chunk != nullptr) {
     using E = EpiStore<T, false>;
@@ -1518,15 +1548,16 @@ static int bwd_tail(const void* W, const T* Hc, int64_t D, int64_t V, int C, boo
     if (kTf32) {
       const Operand b{Wt, D, V, p.ldVt, false};
       rc = launch_gemm<T, 256, false, false, E>(kRoleGradH, a, b, &o, C, (int)D, (int)V, 8, ep,
-                                                status, s);
+                                                status, s, 1, bias_pre);
     } else {
       const Operand b{W, D, V, D, true};
       rc = launch_gemm<T, 256, false, true, E>(kRoleGradH, a, b, &o, C, (int)D, (int)V, 8, ep,
-                                               status, s);
+                                               status, s, 1, bias_pre);
     }
     if (rc != FLCE_OK) return rc;
   }
   // 4. grad_W (+)= dZ^T H[chunk]
+  if (grad_H_chunk == nullptr) w_pre = bias_pre;  // no grad_H launch took the bias sums
   if (grad_W != nullptr) {
     using E = EpiStore<float, true>;
     typename E::Params ep{static_cast<int>(V), static_cast<int>(D),
@@ -1540,12 +1571,12 @@ static int bwd_tail(const void* W, const T* Hc, int64_t D, int64_t V, int C, boo
       const Operand a{dzT, V, C, p.ldCt, false};
       const Operand b{HT, D, C, p.ldCt, false};
       rc = launch_gemm<T, 256, false, false, E>(kRoleGradW, a, b, &o, (int)V, (int)D, C, 8, ep,
-                                                status, s);
+                                                status, s, 1, w_pre);
     } else {
       const Operand a{dz, V, C, p.ldV, true};
       const Operand b{Hc, D, C, D, true};
       rc = launch_gemm<T, 256, true, true, E>(kRoleGradW, a, b, &o, (int)V, (int)D, C, 8, ep,
-                                              status, s);
+                                              status, s, 1, w_pre);
     }
     if (rc != FLCE_OK) return rc;
   }

@@ -72,6 +72,56 @@ struct GemmGeo {
   static constexpr int kThreads = 64 + 32 * EW;
 };
 
+// Work the epilogue warps do before their first tile, while the producer and
+// MMA warps run the first main loops: a small reduction that closes an output
+// of the kernels before this one (launches are stream-ordered, so those have
+// completed).  Every epilogue warp of the grid takes a fixed share, in a fixed
+// order, so the result is the same on every run.
+struct EpiPre {
+  int kind = 0;                // 0 none, 1 column sums, 2 split-K close
+  const float* part = nullptr;
+  int nparts = 0;              // 1: partial rows; 2: splits
+  int64_t ld = 0;              // 1: row stride; 2: split stride (floats)
+  int64_t n = 0;               // 1: columns; 2: output elements / 4
+  void* out = nullptr;         // 1: float [n]; 2: bf16 or float [4 n]
+  int out_bf16 = 0;            // 2: the output is bf16
+  int beta = 0;                // 1: add to the existing out
+};
+
+// kind 1: out[v] (+)= sum over s of part[s * ld + v], s in order; kind 2:
+// out[4i .. 4i + 3] = sum over splits of part[s * ld + 4i ..], 16-byte loads.
+// worker / workers: this warp's index among all epilogue warps of the grid.
+__device__ __forceinline__ void epi_pre_run(const EpiPre& q, int worker, int workers, int lane) {
+  if (q.kind == 1) {
+    for (int64_t c = static_cast<int64_t>(worker) * 32 + lane; c - lane < q.n;
+         c += static_cast<int64_t>(workers) * 32) {
+      if (c >= q.n) continue;
+      float acc = 0.0f;
+#pragma unroll 8
+      for (int sp = 0; sp < q.nparts; ++sp) acc += q.part[sp * q.ld + c];
+      float* o = static_cast<float*>(q.out) + c;
+      *o = q.beta ? *o + acc : acc;
+    }
+  } else if (q.kind == 2) {
+    for (int64_t i = static_cast<int64_t>(worker) * 32 + lane; i < q.n;
+         i += static_cast<int64_t>(workers) * 32) {
+      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      for (int sp = 0; sp < q.nparts; ++sp) {
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(q.part + sp * q.ld) + i);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      if (q.out_bf16)
+        reinterpret_cast<uint2*>(q.out)[i] =
+            make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+      else
+        reinterpret_cast<float4*>(q.out)[i] = acc;
+    }
+  }
+}
+
 struct GemmArgs {
   int M, N, K;     // problem size (elements)
   int nMt, nNt, nK;
@@ -82,6 +132,7 @@ struct GemmArgs {
   // s * nMt + mt, so each split fills its own row band of the output.
   int k_splits;
   int kb_per_split;
+  EpiPre pre;
 };
 
 __device__ __forceinline__ void tile_coords(int t, int nMt, int nNt, int group_m, int& mt,
@@ -345,6 +396,8 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
     ctx.nbuf = G::kStagingBufs;
     ctx.next = 0;
     ctx.lane = lane;
+    epi_pre_run(ga.pre, static_cast<int>(blockIdx.x) * EW + (warp - 2),
+                static_cast<int>(gridDim.x) * EW, lane);
     int local = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
       const int buf = local & 1;
@@ -580,6 +633,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     ctx.buf = smem + S * G::kStageBytes + (warp - 2) * 2 * 4096;
     ctx.next = 0;
     ctx.lane = lane;
+    epi_pre_run(ga.pre, static_cast<int>(blockIdx.x) * 4 + (warp - 2),
+                static_cast<int>(gridDim.x) * 4, lane);
     int local = 0;
     for (int t = cluster_id; t < num_tiles; t += nclusters, ++local) {
       const int buf = local & 1;

@@ -283,7 +283,7 @@ def test_long_packed_workload_sampled(lh):
     _sampled_full_size(lh, p, n_rows=16, sub_rows=128)
 
 
-@pytest.mark.parametrize("pair", [31, 0], ids=["pair", "single"])
+@pytest.mark.parametrize("pair", [31, 0, 32], ids=["pair", "single", "wide_dz"])
 @pytest.mark.parametrize("N,D,V,vslice,bias,reduction", [
     (700, 256, 3001, 1024, True, "mean"),    # three slices, the last 953 columns
     (1000, 520, 2048, 256, False, "sum"),    # eight slices of one tile each
