@@ -340,3 +340,40 @@ def test_vocabulary_slices_rejected_for_fp32(lh):
     with pytest.raises(lh.FlceError):
         lh.flce_bwd(H, W, y, out.lse, out.n_valid, torch.ones(1, device="cuda"), b, -100, "sum",
                     None, -256)
+
+
+@pytest.mark.parametrize("pair", [58, 31], ids=["default", "no_wide_dz"])
+@pytest.mark.parametrize("chunk", [None, 128], ids=["one_chunk", "three_chunks"])
+@pytest.mark.parametrize("want", [(True, True, True), (False, True, True), (True, False, True),
+                                  (False, False, True), (True, True, False)],
+                         ids=["all", "no_H", "no_W", "bias_only", "no_bias"])
+def test_gradient_subsets_with_split_k(lh, want, chunk, pair):
+    """Every subset of the gradients at a shape whose grad_H is split over K
+    (three 128-row tiles, V = 5000): the bias column sums and the split-K close
+    are done by the epilogue warps of whichever contraction follows, or by
+    kernels of their own when none does; each requested gradient against the
+    oracle, whatever the others."""
+    from lm_head_linear_fwd_gb300 import _abi
+    want_h, want_w, want_b = want
+    prev = _abi.flce_gemm_set_pair(pair)
+    try:
+        p = wl.random_flce(300, 256, 5000, torch.bfloat16, bias=True, seed=303, reduction="mean")
+        H, W, b, y = _to(p)
+        out = lh.flce_fwd(H, W, y, b, -100, p.reduction, p.num_label_tokens)
+        bw = lh.flce_bwd(H, W, y, out.lse, out.n_valid, torch.tensor([0.75], device="cuda"), b,
+                         -100, p.reduction, p.num_label_tokens, chunk, want_grad_H=want_h,
+                         want_grad_W=want_w, want_grad_bias=want_b, status=out.status)
+        torch.cuda.synchronize()
+        lh.check_status(out.status)
+        gr = oracle.flce_backward(p.H, p.W, p.bias, p.labels, -100, p.reduction,
+                                  p.num_label_tokens, grad_loss=0.75)
+        assert (bw.grad_H is not None) == want_h and (bw.grad_W is not None) == want_w
+        assert (bw.grad_bias is not None) == want_b
+        if want_h:
+            _grad_ok(bw.grad_H, gr["grad_H"], "grad_H")
+        if want_w:
+            _grad_ok(bw.grad_W, gr["grad_W"], "grad_W")
+        if want_b:
+            _grad_ok(bw.grad_bias, gr["grad_b"], "grad_b")
+    finally:
+        _abi.flce_gemm_set_pair(prev)
