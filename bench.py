@@ -36,21 +36,29 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per step, from
 # in-limit ncu captures (one kernel, a few launches, a few GB resident) that
 # are summarised under profiles/; each figure holds only for the kernel sources
-# it was taken from (sha256 prefix of the listed files) and is reported as null
-# once any of them changes.  CE on logits: the traffic of a [2048, 128256]
+# it was taken from (sha256 prefix of the listed files, comments left out) and
+# is reported as null once the code of any of them changes.  CE on logits: the traffic of a [2048, 128256]
 # capture scaled by the rows (every row is read, and written, once, so the
 # traffic grows in proportion).  FLCE: the per-kernel captures of the
 # benchmark's launches, summed over one step.
 TRAFFIC = {
     # profiles/ce_logits_16384x128256_launch_list_and_small_case.md: 8 x the
     # 2048-row capture of the forward and the in-place backward
-    "ce_logits": {"bytes_per_step": 12.12e9, "sha": "4538f21b851b345c",
+    "ce_logits": {"bytes_per_step": 12.12e9, "sha": "6a37ed3f5b95d51a",
                   "files": ["ce_logits.cu", "common.cuh", "host.h"]},
     # profiles/flce_llama3_8b_kernel_traffic.md: the ten GEMM launches of one
     # step (forward; dZ, grad_H, grad_W of chunks of 3584, 3584 and 1024 rows)
-    "flce": {"bytes_per_step": 32.55e9, "sha": "2879403193dc9ae5",
+    "flce": {"bytes_per_step": 32.55e9, "sha": "7d2f0573ae4fdb13",
              "files": ["flce.cu", "tc_gemm.cuh", "common.cuh", "host.h"]},
 }
+
+
+def _code_only(text: bytes) -> bytes:
+    """The source without its comments: the hash follows the code the counters
+    were taken on, not its commentary."""
+    import re
+    t = re.sub(rb"/\*.*?\*/", b" ", text, flags=re.S)
+    return re.sub(rb"//[^\n]*", b"", t)
 
 
 def csrc_sha(files=None):
@@ -65,7 +73,7 @@ def csrc_sha(files=None):
     h = hashlib.sha256()
     for f in paths:
         h.update(os.path.basename(f).encode())
-        h.update(open(f, "rb").read())
+        h.update(_code_only(open(f, "rb").read()))
     return h.hexdigest()[:16]
 
 

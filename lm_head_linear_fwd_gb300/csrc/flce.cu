@@ -14,7 +14,11 @@
 //      dZ = valid (exp(z - lse) - onehot) g scale and writes it, rounded to the
 //      input dtype, to a [C, ldV] workspace buffer (Liger's feature pitch
 //      casts the chunk's gradient to the input dtype before the addmm);
-//   2. grad_bias += column sums of dZ (two fixed-order passes, no atomics);
+//   2. grad_bias += column sums of dZ, in a fixed order without atomics:
+//      partial sums per 32 rows, formed by the dZ epilogue from its staged
+//      tiles (eight epilogue warps, K <= 1024) or by a pass over the stored
+//      dZ, then added up by the epilogue warps of step 3 (or 4) before their
+//      first tile;
 //   3. grad_H[chunk] = dZ W                (A = dZ K-major, B = W MN-major);
 //   4. grad_W (+)= dZ^T H[chunk] in fp32   (A = dZ MN-major, B = H MN-major),
 //      the addmm with beta = 1 of the same page, chunk after chunk.
@@ -22,7 +26,8 @@
 // fp32 the MN-major operands of steps 3 and 4 are first transposed into the
 // workspace (W once per call, dZ and H[chunk] once per chunk).  When a chunk
 // has too few grad_H tiles to fill the GPU, step 3 splits its long K (= V)
-// and reduces the fp32 partials in a fixed order.  The dZ recompute and grad_W
+// and the fp32 partials are added in a fixed order (by step 4's epilogue
+// warps before their first tile, or by a kernel).  The dZ recompute and grad_W
 // run on CTA pairs (tc_gemm_pair_kernel) by default; flce_gemm_set_pair
 // selects per contraction.
 //
