@@ -44,21 +44,22 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 TRAFFIC = {
     # profiles/ce_logits_16384x128256_launch_list_and_small_case.md: 8 x the
     # 2048-row capture of the forward and the in-place backward
-    "ce_logits": {"bytes_per_step": 12.12e9, "sha": "6a37ed3f5b95d51a",
+    "ce_logits": {"bytes_per_step": 12.12e9, "sha": "24b0a218c3d21127",
                   "files": ["ce_logits.cu", "common.cuh", "host.h"]},
     # profiles/flce_llama3_8b_kernel_traffic.md: the ten GEMM launches of one
     # step (forward; dZ, grad_H, grad_W of chunks of 3584, 3584 and 1024 rows)
-    "flce": {"bytes_per_step": 32.55e9, "sha": "7d2f0573ae4fdb13",
+    "flce": {"bytes_per_step": 32.55e9, "sha": "2da017c1049273c9",
              "files": ["flce.cu", "tc_gemm.cuh", "common.cuh", "host.h"]},
 }
 
 
 def _code_only(text: bytes) -> bytes:
-    """The source without its comments: the hash follows the code the counters
-    were taken on, not its commentary."""
+    """The source without its comments and blank lines: the hash follows the
+    code the counters were taken on, not its commentary."""
     import re
     t = re.sub(rb"/\*.*?\*/", b" ", text, flags=re.S)
-    return re.sub(rb"//[^\n]*", b"", t)
+    t = re.sub(rb"//[^\n]*", b"", t)
+    return b"\n".join(line.rstrip() for line in t.splitlines() if line.strip())
 
 
 def csrc_sha(files=None):
