@@ -294,13 +294,18 @@ def run_ours(args, rank, ws, local):
     flops = 8.0 * N * D * V
     tflops = flops / (flce_ms * 1e-3) / 1e12
     tok_s = N * ws / (flce_ms * 1e-3)
-    if chunk > 0:   # row chunks: dZ, grad_H, grad_W (+ 2 bias kernels) per chunk
+    # the bias gradient's partial column sums come from the eight-warp dZ
+    # epilogue (bf16, D <= 1024) or from one pass over dZ; grad_H's epilogue
+    # warps add them up and grad_W's close a split-K grad_H, so neither takes
+    # a launch of its own
+    bias_kernels = 0 if b is None or (H.dtype == torch.bfloat16 and D <= 1024) else 1
+    if chunk > 0:   # row chunks: dZ, grad_H, grad_W (+ the bias pass) per chunk
         n_chunks = (N + chunk - 1) // chunk
-        launches_flce = 3 + n_chunks * (3 + (2 if b is not None else 0))
+        launches_flce = 3 + n_chunks * (3 + bias_kernels)
         split = f"chunk={chunk}"
     else:           # vocabulary slices, then one rounding of the fp32 grad_H
         n_chunks = (V + (-chunk) - 1) // (-chunk)
-        launches_flce = 3 + n_chunks * (3 + (2 if b is not None else 0)) + 1
+        launches_flce = 3 + n_chunks * (3 + bias_kernels) + 1
         split = f"vocabulary slices of {-chunk} columns"
     if args.only == "flce-step":
         # profiling runs: the timed FLCE step alone, nothing else held on the device
