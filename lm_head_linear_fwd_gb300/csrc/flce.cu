@@ -148,6 +148,59 @@ __device__ __forceinline__ void lse_add32(const float (&v)[32], int n, Lse2& st)
   st.s += a.x + a.y;
 }
 
+// As lse_add32, for 32 values already in the base-2 domain (t = z log2(e)).
+__device__ __forceinline__ void lse_add32_base2(const float (&t)[32], int n, Lse2& st) {
+  float mx = -INFINITY;
+  if (n >= 32) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) mx = fmaxf(mx, t[j]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < n) mx = fmaxf(mx, t[j]);
+  }
+  if (mx > st.m) {
+    st.s *= ex2(st.m - mx);
+    st.m = mx;
+  }
+  if (st.m == -INFINITY) return;
+  const float2 nm = make_float2(-st.m, -st.m);
+  float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                   make_float2(0.0f, 0.0f)};
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    const float2 u = __fadd2_rn(make_float2(t[j], t[j + 1]), nm);
+    float2 e = make_float2(ex2(u.x), ex2(u.y));
+    if (n < 32) {
+      e.x = j < n ? e.x : 0.0f;
+      e.y = j + 1 < n ? e.y : 0.0f;
+    }
+    acc[(j >> 1) & 3] = __fadd2_rn(acc[(j >> 1) & 3], e);
+  }
+  const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+  st.s += a.x + a.y;
+}
+
+// The bias of 8 consecutive columns from col0 (those at or past V read as 0):
+// one 16-byte load (bf16) or two (fp32) when the 8 lie inside and aligned.
+template <typename T>
+__device__ __forceinline__ void bias8(const T* bias, int col0, int V, float (&x)[8]) {
+  const T* b = bias + col0;
+  if (col0 + 8 <= V && (reinterpret_cast<uintptr_t>(b) & 15u) == 0) {
+    constexpr int EPV = Elem<T>::kPerVec;
+#pragma unroll
+    for (int k = 0; k < 8 / EPV; ++k) {
+      float y[EPV];
+      Elem<T>::unpack(__ldg(reinterpret_cast<const uint4*>(b) + k), y);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) x[k * EPV + e] = y[e];
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = col0 + e < V ? Elem<T>::load(b + e) : 0.0f;
+  }
+}
+
 // v[j] for the one j with base + j == idx (idx in [base, base + 32)).
 __device__ __forceinline__ float pick32(const float (&v)[32], int64_t idx, int base) {
   float r = 0.0f;
@@ -174,30 +227,77 @@ struct EpiLse {
   };
   template <int BN>
   __device__ static void tile(const Params& p, int mt, int nt, int row_in_tile, uint32_t taddr,
-                              EpiCtx&) {
+                              EpiCtx& ctx) {
+    static_assert(BN == 256, "one bias value per lane and 8-column group");
     const int row = mt * kBM + row_in_tile;
     const bool row_ok = row < p.M;
     const int64_t y = row_ok ? p.labels[row] : -1;
     const int col_base = nt * BN;
     const int64_t ylocal = (y < 0) ? -1 : (y - p.v0) - col_base;
+    const T* bias = static_cast<const T*>(p.bias);
+    const int lane = row_in_tile & 31;
+    // The tile's bias as fp32 times log2(e) in this warp's staging buffer
+    // (this epilogue stores nothing through it; two halves, this tile's and
+    // the next one's): each logit then costs one FFMA, t = z log2(e) +
+    // b log2(e).  The next tile's bias is loaded while this tile is reduced.
+    const float* b2 = nullptr;
+    float nb[8];
+    const bool fetch_next = bias != nullptr && ctx.next_nt >= 0 && ctx.next_nt != nt;
+    if (bias != nullptr) {
+      float* sb = reinterpret_cast<float*>(ctx.buf);
+      if (ctx.aux_nt != nt) {  // not fetched ahead (the CTA's first tile)
+        float x[8];
+        bias8<T>(bias, col_base + 8 * lane, p.V, x);
+        __syncwarp();
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sb[ctx.aux * BN + 8 * lane + e] = x[e] * kLog2e;
+        __syncwarp();
+        ctx.aux_nt = nt;
+      }
+      b2 = sb + ctx.aux * BN;
+      if (fetch_next) bias8<T>(bias, ctx.next_nt * BN + 8 * lane, p.V, nb);
+    }
     Lse2 st;
     float zy = 0.0f;
-    BiasAhead<T> bnext;
-    if (p.bias != nullptr) bnext.fetch(p.bias, col_base, p.V);
+    const float2 lg = make_float2(kLog2e, kLog2e);
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       const int col0 = col_base + c * 32;
       if (col0 >= p.V) break;  // uniform across the warp
       float v[32];
       tmem_ld32(taddr + c * 32, v);
-      if (p.bias != nullptr) {
-        const BiasAhead<T> bcur = bnext;
-        if (c + 1 < BN / 32) bnext.fetch(p.bias, col0 + 32, p.V);
-        bcur.add(p.bias, col0, p.V, v);
-      }
       // the label's logit, in the one chunk that holds it (rarely any lane of a warp)
-      if (static_cast<uint64_t>(ylocal - c * 32) < 32u) zy = pick32(v, ylocal, c * 32);
-      lse_add32(v, p.V - col0, st);
+      if (static_cast<uint64_t>(ylocal - c * 32) < 32u)
+        zy = pick32(v, ylocal, c * 32) +
+             (bias != nullptr ? Elem<T>::load(bias + col_base + ylocal) : 0.0f);
+      if (b2 != nullptr) {
+        float t[32];
+        const float4* bq = reinterpret_cast<const float4*>(b2 + c * 32);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float4 bb = bq[k];
+          const float2 t0 = __ffma2_rn(make_float2(v[4 * k], v[4 * k + 1]), lg,
+                                       make_float2(bb.x, bb.y));
+          const float2 t1 = __ffma2_rn(make_float2(v[4 * k + 2], v[4 * k + 3]), lg,
+                                       make_float2(bb.z, bb.w));
+          t[4 * k] = t0.x;
+          t[4 * k + 1] = t0.y;
+          t[4 * k + 2] = t1.x;
+          t[4 * k + 3] = t1.y;
+        }
+        lse_add32_base2(t, p.V - col0, st);
+      } else {
+        lse_add32(v, p.V - col0, st);
+      }
+    }
+    if (fetch_next) {  // the next tile's bias into the other half
+      float* sn = reinterpret_cast<float*>(ctx.buf) + (ctx.aux ^ 1) * BN;
+      __syncwarp();
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sn[8 * lane + e] = nb[e] * kLog2e;
+      __syncwarp();
+      ctx.aux ^= 1;
+      ctx.aux_nt = ctx.next_nt;
     }
     if (row_ok && in_range(row, p.part_ld, p.status)) {
       p.part_m[nt * p.part_ld + row] = st.m;

@@ -186,6 +186,8 @@ struct EpiCtx {
   int next;
   int lane;
   int nbuf = 2;  // staging buffers (1 or 2)
+  int next_nt = -1;  // the N-tile of this CTA's next tile (-1: none), for prefetches
+  int aux = 0, aux_nt = -1;  // an epilogue's own state across tiles
 
   __device__ void store_slab(const uint4 (&row)[8], int c0, int r0, bool reduce) {
     uint8_t* b = buf + next * 4096;
@@ -412,6 +414,12 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
       tc_fence_after();
       int mte, nt;
       tile_coords(t, nMtE, ga.nNt, ga.group_m, mte, nt);
+      if (t + static_cast<int>(gridDim.x) < num_tiles) {
+        int mte2;
+        tile_coords(t + static_cast<int>(gridDim.x), nMtE, ga.nNt, ga.group_m, mte2, ctx.next_nt);
+      } else {
+        ctx.next_nt = -1;
+      }
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(buf * BN);
       if constexpr (EW == 4)
@@ -649,6 +657,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       int mt, nt;
       tile_coords(t, ga.nMt, ga.nNt, ga.group_m, mt, nt);
+      if (t + nclusters < num_tiles) {
+        int mt2;
+        tile_coords(t + nclusters, ga.nMt, ga.nNt, ga.group_m, mt2, ctx.next_nt);
+      } else {
+        ctx.next_nt = -1;
+      }
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(buf * BN);
       // this CTA's half of the 256-row tile is 128-row tile 2*mt + rank
